@@ -47,7 +47,10 @@ Readings taken where the pages are silent:
     [p >= tau or rank < top_k], the residual stays normalize(relu(p - q)), and
     mu(a) = q(a) acc(a) + (1 - sum_s q(s) acc(s)) res(a); exact gives mu = p;
   * a tree walk accepts at most max_depth nodes; at that depth a node with
-    children is treated as a leaf and STATUS_DEPTH_EXCEEDED is set.
+    children is treated as a leaf and STATUS_DEPTH_EXCEEDED is set;
+  * STATUS_NONFINITE_ROW is set for a row the decision reads (chain rows
+    0..n, draft rows 0..min(n, K-1), the tree path's rows) whose maximum is
+    not finite or which holds a NaN; rows after the decision are not read.
 
 Parity status: every function below is pinned by tests/test_oracle_*.py
 (closed forms, exact-rational brute force, scenario fixtures, Monte Carlo
@@ -208,9 +211,6 @@ def verify_greedy(target_logits, draft_tokens):
     assert d.shape == (B, K)
     out = _empty_outputs(B, R)
     for b in range(B):
-        for i in range(R):
-            if not row_is_finite(x[b, i]):
-                out["status"][b] |= STATUS_NONFINITE_ROW
         n = K
         for i in range(K):
             t = d[b, i]
@@ -224,6 +224,9 @@ def verify_greedy(target_logits, draft_tokens):
         for j in range(n):
             out["tokens"][b, j] = d[b, j]
         out["tokens"][b, n] = first_argmax(x[b, n])
+        for i in range(n + 1):          # the rows the decision read
+            if not row_is_finite(x[b, i]):
+                out["status"][b] |= STATUS_NONFINITE_ROW
         for j in range(n + 1):
             tok = out["tokens"][b, j]
             out["logprob"][b, j] = x[b, j, tok] - log_sum_exp(x[b, j], 1.0)
@@ -255,13 +258,6 @@ def verify_sample(target_logits, draft_logits, draft_tokens, temperature,
 
     for b in range(B):
         status = 0
-        for i in range(R):
-            if not row_is_finite(x[b, i]):
-                status |= STATUS_NONFINITE_ROW
-        if y is not None:
-            for i in range(K):
-                if not row_is_finite(y[b, i]):
-                    status |= STATUS_NONFINITE_ROW
         tie = -1
         n = K
         final_w = None
@@ -343,6 +339,11 @@ def verify_sample(target_logits, draft_logits, draft_tokens, temperature,
             out["mu"][b, n] = final_scale * final_w[j] / final_w.sum()
         else:
             out["mu"][b, n] = p_row[j]
+        for i in range(n + 1):          # the rows the decision read
+            if not row_is_finite(x[b, i]):
+                status |= STATUS_NONFINITE_ROW
+            if y is not None and i < K and not row_is_finite(y[b, i]):
+                status |= STATUS_NONFINITE_ROW
         out["num_accepted"][b] = n
         out["status"][b] = status
         out["tie_pos"][b] = tie
@@ -391,9 +392,6 @@ def verify_tree(target_logits, node_tokens, parents, max_depth, temperature,
 
     for b in range(B):
         status = 0
-        for n in range(N):
-            if not row_is_finite(x[b, n]):
-                status |= STATUS_NONFINITE_ROW
         children, links_ok = tree_children(par[b])
         if not links_ok:
             status |= STATUS_BAD_PARENT
@@ -471,6 +469,9 @@ def verify_tree(target_logits, node_tokens, parents, max_depth, temperature,
             out["logprob"][b, depth] = np.log(p[j])
             out["mu"][b, depth] = prod * w[j] / w.sum()
             break
+        for j in range(depth + 1):      # the rows the walk read
+            if not row_is_finite(x[b, out["nodes"][b, j]]):
+                status |= STATUS_NONFINITE_ROW
         out["num_accepted"][b] = depth
         out["status"][b] = status
         out["tie_pos"][b] = tie

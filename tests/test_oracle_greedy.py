@@ -95,6 +95,9 @@ def test_greedy_bad_token_and_nonfinite_row():
     x[1, 2, :] = -np.inf
     out = O.verify_greedy(x, np.array([[1, 1], [1, 1]]))
     assert out["status"][1] & O.STATUS_NONFINITE_ROW
+    # a row after the first mismatch is not read, so it is not flagged
+    out = O.verify_greedy(x, np.array([[1, 1], [0, 1]]))
+    assert out["status"][1] == 0 and out["num_accepted"][1] == 0
 
 
 def test_greedy_chain_equals_chain_shaped_tree():
