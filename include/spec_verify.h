@@ -1,0 +1,197 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify: batched speculative-decoding
+ * verification over vocabulary-sized logits on one GB300 (sm_103a).
+ *
+ * Operations (source pages, by title and section):
+ *   spec_verify_greedy  mini-sglang PR #134 "[Feature] Vanilla speculative
+ *                       decoding", Modifications (verify.py): accept the
+ *                       longest prefix of the K drafts that matches the
+ *                       target argmax over the K+1 verify-pass logits, then
+ *                       append the bonus token (argmax of the next row).
+ *   spec_verify_sample  spec-decode README, "How it works": accept draft t with
+ *                       probability min(1, p(t)/q(t)), stop at the first
+ *                       rejection and draw from normalize(relu(p - q)); if all
+ *                       K are accepted draw a bonus token from p. nanospec
+ *                       README, acceptance rules: exact / relaxed (p >= tau or
+ *                       top-k) / power (min(1, p/rest)^alpha), and a target
+ *                       log-prob and behaviour probability mu per token.
+ *   spec_verify_tree    nanospec README, EAGLE-3 tree configuration (depth 5,
+ *                       topk 4): walk a draft tree given by parent indices,
+ *                       accepting one root-to-node path.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, except
+ *     where a comment says otherwise. The library allocates nothing, keeps no
+ *     state between calls and never synchronises the stream.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream). Argument errors the host can see are returned
+ *     synchronously and nothing is launched. SV_ERR_CUDA means a launch failed.
+ *   - Logit rows: row r of a [rows, V] matrix starts at
+ *     base + r * row_stride ELEMENTS (row_stride >= V). bf16 rows need only
+ *     2-byte alignment and fp32 rows 4-byte alignment; the kernels handle
+ *     rows that do not start on a 16-byte boundary.
+ *   - Argmax ties go to the lowest vocabulary index; argmax is taken on raw
+ *     logits. Logits may contain -inf (masked tokens). A row whose maximum is
+ *     not finite, or that contains NaN, is flagged (SV_STATUS_NONFINITE_ROW)
+ *     when the decision reads it, and that request's outputs are unspecified.
+ *   - Temperature T scales both p = softmax(x/T) and q = softmax(y/T).
+ *     Log-probs are natural-log p_T(token) of the distribution used
+ *     (temperature 1 for the greedy rules).
+ *   - Output slots after the emitted tokens hold token -1, log-prob 0, mu 0.
+ *   - out_logprob, out_mu and out_status may be NULL.
+ *   - The workspace (device memory, 16-byte aligned, at least the size the
+ *     matching *_workspace_size function returns) needs no initialisation
+ *     and may be reused by later calls on the same stream. Two calls that
+ *     run concurrently must not share a workspace.
+ *   - A device-side problem found in one request sets bits in out_status[b]
+ *     (SV_STATUS_*); other requests are unaffected. Kernels never trap; every
+ *     wait inside them is bounded (SV_STATUS_TIMEOUT if one gives up).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_VERIFY_ABI_VERSION 1
+
+/* Return codes. */
+typedef int32_t sv_status;
+#define SV_OK                      0
+#define SV_ERR_INVALID_ARG         1  /* a pointer, size, stride or parameter is invalid */
+#define SV_ERR_UNSUPPORTED_DTYPE   2  /* dtype is neither SV_F32 nor SV_BF16 */
+#define SV_ERR_WORKSPACE_TOO_SMALL 3  /* workspace_bytes below the required size */
+#define SV_ERR_CUDA                4  /* a CUDA launch or attribute call failed */
+#define SV_ERR_NOT_SUPPORTED       5  /* valid request this build does not implement */
+
+/* Logit element types. */
+#define SV_F32  0
+#define SV_BF16 1
+
+/* Acceptance rules (nanospec README, acceptance rules). */
+#define SV_RULE_EXACT   0  /* lossless: accept with min(1, p/q) */
+#define SV_RULE_RELAXED 1  /* accept iff p >= tau or rank < top_k; mu = 1 on accepted drafts */
+#define SV_RULE_POWER   2  /* accept with probability min(1, p/rest)^alpha */
+
+/* Per-request status bits written to out_status[b]. */
+#define SV_STATUS_BAD_TOKEN      1   /* a consulted draft / node token is outside [0, V) */
+#define SV_STATUS_BAD_PARENT     2   /* parents[0] != -1 or some parents[n] not in [0, n) */
+#define SV_STATUS_NONFINITE_ROW  4   /* a consulted row has a non-finite max or a NaN */
+#define SV_STATUS_ZERO_MASS      8   /* a draft token with p(t) = q(t) = 0 (rejected) */
+#define SV_STATUS_DEPTH_EXCEEDED 16  /* the walk reached max_depth at a node with children */
+#define SV_STATUS_TIMEOUT        32  /* a bounded wait in a kernel gave up */
+
+/* Rule parameters. tau: relaxed threshold on p. top_k: relaxed rank bound
+ * (0 disables it; rank = number of logits strictly greater, so top_k = 1
+ * accepts the argmax). alpha > 0: power exponent (alpha = 1 is the exact
+ * rule). */
+typedef struct sv_rule_params {
+  int32_t rule;
+  float tau;
+  int32_t top_k;
+  float alpha;
+} sv_rule_params;
+
+/* Largest top_k the relaxed rule supports. */
+#define SV_MAX_TOP_K 16
+/* Largest node count a tree may have. */
+#define SV_MAX_TREE_NODES 1024
+
+/* ABI version of the loaded library (SPEC_VERIFY_ABI_VERSION). */
+int32_t spec_verify_abi_version(void);
+
+/* Static, NUL-terminated description of a return code. */
+const char* spec_verify_status_string(sv_status s);
+
+/* Workspace bytes for a call with these sizes; 0 if the sizes are invalid.
+ * Pure host functions: they touch no device. */
+size_t spec_verify_greedy_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype);
+size_t spec_verify_sample_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype,
+                                         int32_t has_draft_logits);
+size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V, int32_t dtype);
+
+/* Greedy chain verification (mini-sglang PR #134, verify_drafts).
+ *   target_logits  [B, K+1, V] rows of `dtype`, row (b, i) at row b*(K+1)+i.
+ *   draft_tokens   [B, K] int32, row-major.
+ *   B >= 0, K >= 0, V >= 1.
+ * Outputs (row-major, B rows):
+ *   out_tokens        [B, K+1] int32: d_0..d_{n-1}, argmax(row n), then -1.
+ *   out_num_accepted  [B] int32: n, the accepted draft count (n+1 tokens).
+ *   out_logprob       [B, K+1] float: log_softmax(row j)[token j] at T = 1.
+ *   out_mu            [B, K+1] float: 1 for emitted tokens (deterministic rule).
+ *   out_status        [B] int32: SV_STATUS_* bits.
+ * A draft outside [0, V) counts as a mismatch and sets SV_STATUS_BAD_TOKEN. */
+sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t row_stride,
+                             const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                             int32_t* out_tokens, int32_t* out_num_accepted,
+                             float* out_logprob, float* out_mu, int32_t* out_status,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stochastic chain verification (spec-decode README "How it works";
+ * nanospec README rules).
+ *   target_logits  [B, K+1, V]; draft_logits [B, K, V] of the same dtype with
+ *                  its own row stride, or NULL for deterministic drafts
+ *                  (q = one-hot of the draft token).
+ *   draft_tokens   [B, K] int32.  temperature: finite, >= 1e-4.
+ *   uniforms       [B, K+1] float in [0, 1): column i < K tests draft i
+ *                  (accepted iff u < acceptance), column K drives the single
+ *                  final draw (residual or bonus), which is the smallest
+ *                  index j whose inclusive prefix sum of the weights exceeds
+ *                  u * (total weight), in ascending vocabulary order.
+ * With draft logits: exact acceptance min(1, p/q); p(t) = q(t) = 0 rejects
+ * (SV_STATUS_ZERO_MASS); residual normalize(relu(p - q)), or p when that mass
+ * is zero; mu = p(token). The relaxed and power rules with draft logits are
+ * SV_ERR_NOT_SUPPORTED in this version.
+ * Without draft logits (deterministic drafts): exact a = p(d), power
+ * a = p(d)^alpha, relaxed a = [p(d) >= tau or rank(d) < top_k]; mu = a for
+ * an accepted draft; on rejection the draw is from p with d removed and mu is
+ * (1 - a) p(j) / (1 - p(d)).
+ * Outputs as for spec_verify_greedy. */
+sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t row_stride,
+                             const void* draft_logits, int64_t draft_row_stride,
+                             const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                             float temperature, const float* uniforms, sv_rule_params rule,
+                             int32_t* out_tokens, int32_t* out_num_accepted,
+                             float* out_logprob, float* out_mu, int32_t* out_status,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Tree verification (nanospec README, EAGLE-3 tree configuration).
+ *   target_logits  [B, N, V]: row n is the target's next-token logits after
+ *                  the path root..n (node 0 is the root).
+ *   node_tokens    [B, N] int32: token of node n (node 0's is unused).
+ *   parents        [B, N] int32: parents[b, 0] = -1, 0 <= parents[b, n] < n.
+ *                  A node with an invalid link is ignored (SV_STATUS_BAD_PARENT).
+ *   1 <= N <= SV_MAX_TREE_NODES, max_depth >= 0: at most max_depth nodes are
+ *   accepted; outputs have max_depth + 1 columns.
+ *   temperature == 0 selects the greedy walk (uniforms may be NULL): from the
+ *   current node move to the lowest-index child whose token is the argmax of
+ *   the current row; stop when none; append the argmax of the last row.
+ *   temperature > 0 (>= 1e-4) selects the stochastic walk with `rule`:
+ *   children are tested in increasing node index with uniforms[b, c]; with
+ *   rest_1 = 1 and rest_{j+1} = rest_j - p(c_j) over rejected distinct tokens,
+ *   exact a_j = min(1, p/rest_j), power a_j = min(1, p/rest_j)^alpha, relaxed
+ *   a_j = [p >= tau or rank < top_k]; a duplicate of a rejected sibling's
+ *   token has a_j = 0. On acceptance the walk descends; when every child is
+ *   rejected, or at a leaf, one token is drawn with uniforms[b, 0] from p with
+ *   the rejected tokens removed. mu is the probability of the branch taken.
+ * Outputs ([B, max_depth+1] unless noted):
+ *   out_tokens, out_logprob, out_mu as above; out_nodes: the path node whose
+ *   row scored each emitted token (out_nodes[b, 0] = 0; accepted nodes are
+ *   out_nodes[b, 1..n]); out_num_accepted [B]; out_status [B]. */
+sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row_stride,
+                           const int32_t* node_tokens, const int32_t* parents,
+                           int32_t B, int32_t N, int32_t V, int32_t max_depth,
+                           float temperature, const float* uniforms, sv_rule_params rule,
+                           int32_t* out_tokens, int32_t* out_nodes, int32_t* out_num_accepted,
+                           float* out_logprob, float* out_mu, int32_t* out_status,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */
