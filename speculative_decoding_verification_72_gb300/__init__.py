@@ -1,1 +1,15 @@
-"""GB300 (sm_103a) library for batched speculative-decoding verification."""
+"""GB300 (sm_103a) library for batched speculative-decoding verification.
+
+The compute path is the C-ABI shared library libspecverify.so (CUDA kernels in
+csrc/, declared in include/spec_verify.h); ``verify`` is its thin ctypes
+binding. Importing the package does not load the library: the first call
+does, and raises SpecVerifyError if it has not been built.
+"""
+
+from .verify import (  # noqa: F401
+    RULE_EXACT, RULE_POWER, RULE_RELAXED,
+    STATUS_BAD_PARENT, STATUS_BAD_TOKEN, STATUS_DEPTH_EXCEEDED,
+    STATUS_NONFINITE_ROW, STATUS_TIMEOUT, STATUS_ZERO_MASS,
+    SpecVerifyError, library_path, load_library,
+    spec_verify_greedy, spec_verify_sample, spec_verify_tree,
+)

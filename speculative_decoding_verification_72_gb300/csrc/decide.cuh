@@ -1,0 +1,400 @@
+// K2: per-request decisions, one CTA per request, launched as a programmatic
+// dependent of K1 (griddepcontrol.wait before reading K1's partials).
+//
+// chain_decide_kernel
+//   Greedy (mini-sglang PR #134, verify.py): row i's argmax is merged from its
+//   segment partials; n = first i < K whose draft is out of range or differs
+//   from that argmax; tokens d_0..d_{n-1}, then argmax(row n).
+//   Stochastic (spec-decode README, "How it works"; nanospec README rules):
+//   per draft i, a_i = min(1, p(d_i)/q(d_i)) (exact, power ^alpha) or
+//   [p(d_i) >= tau] (relaxed); accepted iff u_i < a_i; n = first rejection.
+//   The row n draw (residual or bonus) is described for K3.
+//   Rows are taken NT at a time; the first rejection is a block-wide min, so
+//   long chains (K+1 = 4096) stop after the block that holds it.
+//
+// tree_decide_kernel
+//   All N rows' statistics and every node's gathered logit (node token in its
+//   parent's row) are loaded into shared memory in parallel; one thread then
+//   walks from the root over children in increasing index (nanospec README,
+//   tree configuration), with rest / branch probabilities in double.
+#pragma once
+
+#include "sv_common.cuh"
+
+namespace sv {
+
+constexpr int kK2Threads = 256;
+constexpr int kMaxTreeNodes = 1024;
+
+struct RuleArgs {
+  int32_t rule;  // 0 exact, 1 relaxed, 2 power
+  float tau;
+  int32_t top_k;
+  float alpha;
+};
+
+struct ChainArgs {
+  const uint8_t* tgt;
+  int64_t tgt_stride;    // bytes
+  const uint8_t* dft;    // nullptr: deterministic drafts
+  int64_t dft_stride;    // bytes
+  const int32_t* drafts; // [B, K]
+  const float* uniforms; // [B, K+1] (stochastic)
+  int32_t B, K, V, S;
+  const Partial* part_t; // [B*(K+1)*S]
+  const Partial* part_d; // [B*K*S]
+  float c;               // log2(e) / T (greedy: T = 1)
+  int32_t greedy;
+  RuleArgs rule;
+  int32_t* out_tokens;
+  int32_t* out_num;
+  float* out_logprob;
+  float* out_mu;
+  int32_t* out_status;
+  DrawDesc* draws;
+  int32_t* excl;         // [B * excl_stride]
+  int32_t excl_stride;
+  uint32_t* draw_counters;  // [B], zeroed here for K3's tickets
+};
+
+template <int ES>
+__global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArgs a) {
+  grid_dep_wait();
+  __shared__ int s_first;
+  __shared__ int s_status;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int K = a.K, R = a.K + 1;
+  const float c = a.c;
+  if (tid == 0) {
+    s_status = 0;
+    if (a.draw_counters) a.draw_counters[b] = 0;
+  }
+  int n = -1;
+  int base = 0;
+  for (; base < R; base += kK2Threads) {
+    __syncthreads();   // every thread has read the previous block's s_first
+    if (tid == 0) s_first = INT_MAX;
+    __syncthreads();
+    const int i = base + tid;
+    const bool active = i < R;
+    float m = -INFINITY, s = 0.f, lp2row = 0.f, lq2row = 0.f, lp2 = 0.f, acc = 0.f;
+    int idx = INT_MAX, err = 0, tok = -1, st = 0;
+    bool bad = false, zero = false, rej = false;
+    if (active) {
+      const int64_t trow = static_cast<int64_t>(b) * R + i;
+      merge_partial_row(a.part_t + trow * a.S, a.S, c, m, s, idx, err);
+      lp2row = m * c + log2f(s);
+      if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= 4;   // NONFINITE_ROW
+      if (err) st |= 32;                                                     // TIMEOUT
+      if (i < K) {
+        tok = a.drafts[static_cast<int64_t>(b) * K + i];
+        bad = tok < 0 || tok >= a.V;
+        if (a.greedy) {
+          rej = bad || tok != idx;
+        } else {
+          float lq2 = 0.f;
+          if (!bad) {
+            const float x = Elem<ES>::load(a.tgt + trow * a.tgt_stride, tok);
+            lp2 = x * c - lp2row;  // log2 p(t)
+          }
+          if (a.dft) {
+            const int64_t drow = static_cast<int64_t>(b) * K + i;
+            float md, sd;
+            int id, ed;
+            merge_partial_row(a.part_d + drow * a.S, a.S, c, md, sd, id, ed);
+            lq2row = md * c + log2f(sd);
+            if (!(fabsf(md) <= FLT_MAX) || !(sd > 0.f && sd <= FLT_MAX)) st |= 4;
+            if (ed) st |= 32;
+            if (!bad) {
+              const float y = Elem<ES>::load(a.dft + drow * a.dft_stride, tok);
+              lq2 = y * c - lq2row;
+              if (lp2 == -INFINITY && lq2 == -INFINITY) {
+                zero = true;
+              } else {
+                const float r2 = fminf(0.f, lp2 - lq2);   // log2 min(1, p/q)
+                if (a.rule.rule == 1) acc = (ex2(lp2) >= a.rule.tau) ? 1.f : 0.f;
+                else if (a.rule.rule == 2) acc = ex2(a.rule.alpha * r2);
+                else acc = ex2(r2);
+              }
+            }
+          } else if (!bad) {   // deterministic draft, rest_1 = 1
+            const float r2 = fminf(0.f, lp2);
+            if (a.rule.rule == 1) acc = (ex2(lp2) >= a.rule.tau) ? 1.f : 0.f;
+            else if (a.rule.rule == 2) acc = ex2(a.rule.alpha * r2);
+            else acc = ex2(r2);
+          }
+          const float u = a.uniforms[static_cast<int64_t>(b) * R + i];
+          rej = bad || zero || !(u < acc);
+        }
+      }
+      if (rej) atomicMin(&s_first, i);
+    }
+    __syncthreads();
+    const int first = s_first;
+    const bool last_block = base + kK2Threads >= R;
+    const int nb = first != INT_MAX ? first : (last_block ? K : INT_MAX);
+    if (active) {
+      const int64_t o = static_cast<int64_t>(b) * R + i;
+      if (i <= nb) {
+        int stat = st;
+        if (i == nb && i < K) {
+          if (bad) stat |= 1;
+          if (zero) stat |= 8;
+        }
+        if (stat) atomicOr(&s_status, stat);
+      }
+      if (a.greedy) {
+        int out_tok = -1;
+        float lp = 0.f, mu = 0.f;
+        if (i < nb) {
+          out_tok = tok;
+          lp = -log2f(s) * kLn2;   // the draft is the argmax, so x[tok] = m
+          mu = 1.f;
+        } else if (i == nb) {
+          out_tok = idx;
+          lp = -log2f(s) * kLn2;
+          mu = 1.f;
+        }
+        a.out_tokens[o] = out_tok;
+        if (a.out_logprob) a.out_logprob[o] = lp;
+        if (a.out_mu) a.out_mu[o] = mu;
+      } else {
+        if (i < nb) {
+          a.out_tokens[o] = tok;
+          if (a.out_logprob) a.out_logprob[o] = lp2 * kLn2;
+          if (a.out_mu) a.out_mu[o] = a.dft ? ex2(lp2) : acc;
+        } else if (i == nb) {
+          DrawDesc d;
+          d.pos = i;
+          d.u = a.uniforms[static_cast<int64_t>(b) * R + K];
+          d.t_row = static_cast<int32_t>(static_cast<int64_t>(b) * R + i);
+          d.d_row = static_cast<int32_t>(static_cast<int64_t>(b) * K + i);
+          d.lp2 = lp2row;
+          d.lq2 = lq2row;
+          d.scale = 1.f;
+          d.n_excl = 0;
+          d.pad0 = d.pad1 = d.pad2 = 0;
+          if (i == K) {
+            d.type = kDrawP;
+          } else if (a.dft) {
+            d.type = kDrawResid;
+          } else {
+            d.type = kDrawMaskedP;
+            d.scale = 1.f - acc;
+            if (!bad) {
+              a.excl[static_cast<int64_t>(b) * a.excl_stride] = tok;
+              d.n_excl = 1;
+            }
+          }
+          a.draws[b] = d;
+          // K3 writes this position's token, log-prob and mu.
+        } else {
+          a.out_tokens[o] = -1;
+          if (a.out_logprob) a.out_logprob[o] = 0.f;
+          if (a.out_mu) a.out_mu[o] = 0.f;
+        }
+      }
+    }
+    if (nb != INT_MAX) {
+      n = nb;
+      break;
+    }
+  }
+  // Columns after the block that held the decision.
+  for (int j = base + kK2Threads + tid; j < R; j += kK2Threads) {
+    const int64_t o = static_cast<int64_t>(b) * R + j;
+    a.out_tokens[o] = -1;
+    if (a.out_logprob) a.out_logprob[o] = 0.f;
+    if (a.out_mu) a.out_mu[o] = 0.f;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.out_num[b] = n;
+    if (a.out_status) a.out_status[b] = s_status;
+  }
+  grid_dep_launch();
+}
+
+struct TreeArgs {
+  const uint8_t* tgt;
+  int64_t tgt_stride;      // bytes
+  const int32_t* tokens;   // [B, N]
+  const int32_t* parents;  // [B, N]
+  const float* uniforms;   // [B, N] (stochastic)
+  int32_t B, N, V, S, max_depth;
+  const Partial* part;     // [B*N*S]
+  float c;                 // log2(e) / T (greedy: T = 1)
+  int32_t greedy;
+  RuleArgs rule;
+  int32_t* out_tokens;     // [B, W], W = max_depth + 1
+  int32_t* out_nodes;
+  int32_t* out_num;
+  float* out_logprob;
+  float* out_mu;
+  int32_t* out_status;
+  DrawDesc* draws;
+  int32_t* excl;
+  int32_t excl_stride;
+  uint32_t* draw_counters;
+};
+
+template <int ES>
+__global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs a) {
+  grid_dep_wait();
+  __shared__ float sm_m[kMaxTreeNodes];     // row max
+  __shared__ float sm_l2[kMaxTreeNodes];    // row lse, log2 domain
+  __shared__ float sm_g[kMaxTreeNodes];     // node token's logit in its parent's row
+  __shared__ int sm_am[kMaxTreeNodes];      // row argmax
+  __shared__ int sm_tok[kMaxTreeNodes];
+  __shared__ int sm_par[kMaxTreeNodes];     // -1 for the root and bad links
+  __shared__ int sm_first[kMaxTreeNodes];   // first child
+  __shared__ int sm_next[kMaxTreeNodes];    // next sibling
+  __shared__ unsigned char sm_bad[kMaxTreeNodes];  // row not finite / timed out
+  __shared__ int s_status;
+
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int N = a.N, W = a.max_depth + 1;
+  const float c = a.c;
+  if (tid == 0) {
+    s_status = 0;
+    if (a.draw_counters) a.draw_counters[b] = 0;
+  }
+  __syncthreads();
+  for (int n = tid; n < N; n += kK2Threads) {
+    const int64_t row = static_cast<int64_t>(b) * N + n;
+    float m, s;
+    int idx, err;
+    merge_partial_row(a.part + row * a.S, a.S, c, m, s, idx, err);
+    sm_m[n] = m;
+    sm_l2[n] = m * c + log2f(s);
+    sm_am[n] = idx;
+    sm_bad[n] = static_cast<unsigned char>(((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? 4 : 0) |
+                                           (err ? 32 : 0));
+    const int par = a.parents[row];
+    const int tok = a.tokens[row];
+    const bool link_ok = (n == 0) ? (par == -1) : (par >= 0 && par < n);
+    if (!link_ok) atomicOr(&s_status, 2);   // BAD_PARENT
+    const int p = (n > 0 && link_ok) ? par : -1;
+    sm_par[n] = p;
+    sm_tok[n] = tok;
+    float g = -INFINITY;
+    if (p >= 0 && tok >= 0 && tok < a.V)
+      g = Elem<ES>::load(a.tgt + (static_cast<int64_t>(b) * N + p) * a.tgt_stride, tok);
+    sm_g[n] = g;
+    sm_first[n] = -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int n = N - 1; n >= 1; --n) {   // reverse insertion: lists in increasing index
+      const int p = sm_par[n];
+      if (p >= 0) {
+        sm_next[n] = sm_first[p];
+        sm_first[p] = n;
+      }
+    }
+    int status = 0;
+    int cur = 0, depth = 0;
+    const int64_t ob = static_cast<int64_t>(b) * W;
+    int32_t* excl = a.excl + static_cast<int64_t>(b) * a.excl_stride;
+    while (true) {
+      a.out_nodes[ob + depth] = cur;
+      status |= sm_bad[cur];
+      int kid = sm_first[cur];
+      if (depth == a.max_depth && kid >= 0) {
+        status |= 16;   // DEPTH_EXCEEDED
+        kid = -1;
+      }
+      if (a.greedy) {
+        const int am = sm_am[cur];
+        int nxt = -1;
+        for (; kid >= 0; kid = sm_next[kid]) {
+          const int t = sm_tok[kid];
+          if (t < 0 || t >= a.V) {
+            status |= 1;
+            continue;
+          }
+          if (t == am) {
+            nxt = kid;
+            break;
+          }
+        }
+        a.out_tokens[ob + depth] = am;
+        if (a.out_logprob) a.out_logprob[ob + depth] = (sm_m[cur] * c - sm_l2[cur]) * kLn2;
+        if (a.out_mu) a.out_mu[ob + depth] = 1.f;
+        if (nxt < 0) break;
+        cur = nxt;
+        ++depth;
+        continue;
+      }
+      double rest = 1.0, reach = 1.0;
+      int nrej = 0, accepted = -1;
+      for (; kid >= 0; kid = sm_next[kid]) {
+        const int t = sm_tok[kid];
+        double acc = 0.0;
+        float lp2 = -INFINITY;
+        bool counted = false;
+        if (t < 0 || t >= a.V) {
+          status |= 1;
+        } else {
+          bool dup = false;
+          for (int r = 0; r < nrej; ++r) dup |= (excl[r] == t);
+          if (!dup) {
+            counted = true;
+            lp2 = sm_g[kid] * c - sm_l2[cur];
+            const double p = static_cast<double>(ex2(lp2));
+            if (a.rule.rule == 1) {
+              acc = (p >= static_cast<double>(a.rule.tau)) ? 1.0 : 0.0;
+            } else {
+              const double ratio = rest <= 0.0 ? 1.0 : fmin(1.0, p / rest);
+              acc = (a.rule.rule == 2) ? pow(ratio, static_cast<double>(a.rule.alpha)) : ratio;
+            }
+            rest -= p;
+          }
+        }
+        const double u = static_cast<double>(a.uniforms[static_cast<int64_t>(b) * N + kid]);
+        if (u < acc) {
+          accepted = kid;
+          a.out_tokens[ob + depth] = t;
+          if (a.out_logprob) a.out_logprob[ob + depth] = lp2 * kLn2;
+          if (a.out_mu) a.out_mu[ob + depth] = static_cast<float>(reach * acc);
+          break;
+        }
+        reach *= (1.0 - acc);
+        if (counted) excl[nrej++] = t;
+      }
+      if (accepted >= 0) {
+        cur = accepted;
+        ++depth;
+        continue;
+      }
+      DrawDesc d;
+      d.type = nrej > 0 ? kDrawMaskedP : kDrawP;
+      d.t_row = static_cast<int32_t>(static_cast<int64_t>(b) * N + cur);
+      d.d_row = 0;
+      d.pos = depth;
+      d.u = a.uniforms[static_cast<int64_t>(b) * N];
+      d.lp2 = sm_l2[cur];
+      d.lq2 = 0.f;
+      d.scale = static_cast<float>(reach);
+      d.n_excl = nrej;
+      d.pad0 = d.pad1 = d.pad2 = 0;
+      a.draws[b] = d;
+      break;
+    }
+    a.out_num[b] = depth;
+    for (int j = depth + 1; j < W; ++j) {
+      a.out_tokens[ob + j] = -1;
+      a.out_nodes[ob + j] = -1;
+      if (a.out_logprob) a.out_logprob[ob + j] = 0.f;
+      if (a.out_mu) a.out_mu[ob + j] = 0.f;
+    }
+    atomicOr(&s_status, status);
+  }
+  __syncthreads();
+  if (tid == 0 && a.out_status) a.out_status[b] = s_status;
+  grid_dep_launch();
+}
+
+}  // namespace sv

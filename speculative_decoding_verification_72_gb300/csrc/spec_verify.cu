@@ -1,0 +1,414 @@
+// Host side of the libspecverify C ABI (include/spec_verify.h): argument
+// validation, the workspace plan shared by the *_workspace_size functions and
+// the launchers, and the kernel launches.
+//
+// One call is K1 (row statistics) -> K2 (decide) [-> K3 (draw)] on the
+// caller's stream. K2 and K3 are launched with programmatic stream
+// serialization, so their launch overlaps the tail of the kernel before them;
+// each waits (griddepcontrol.wait) before touching that kernel's results.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "spec_verify.h"
+#include "decide.cuh"
+#include "draw.cuh"
+#include "row_stats.cuh"
+
+namespace {
+
+using namespace sv;
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elem_size(int32_t dtype) {
+  if (dtype == SV_F32) return 4;
+  if (dtype == SV_BF16) return 2;
+  return 0;
+}
+
+struct Plan {
+  int32_t S = 0;            // K1 segments per row
+  int32_t seg_elems = 0;
+  int32_t P = 0;            // K3 chunks per row
+  int32_t chunk_elems = 0;
+  int32_t excl_stride = 0;
+  int64_t rows_total = 0;
+  size_t off_part = 0, off_draw = 0, off_excl = 0, off_k3part = 0, off_k3cnt = 0;
+  size_t total = 0;
+};
+
+// Split a V-element row into n pieces of at most max_bytes, each a multiple
+// of 64 elements (so every piece starts at the row's 16-byte phase).
+void split_row(int64_t V, int es, int64_t max_bytes, int32_t* n_out, int32_t* elems_out) {
+  int64_t n = (V * es + max_bytes - 1) / max_bytes;
+  if (n < 1) n = 1;
+  int64_t e = (V + n - 1) / n;
+  e = (e + 63) / 64 * 64;
+  n = (V + e - 1) / e;
+  *n_out = static_cast<int32_t>(n);
+  *elems_out = static_cast<int32_t>(e);
+}
+
+bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, bool draw,
+               int64_t excl_stride, Plan* pl) {
+  if (V < 1 || es == 0 || B < 0 || rows_t < 0 || rows_d < 0) return false;
+  split_row(V, es, kK1SegBytes, &pl->S, &pl->seg_elems);
+  split_row(V, es, kK3ChunkBytes, &pl->P, &pl->chunk_elems);
+  pl->rows_total = rows_t + rows_d;
+  if (pl->rows_total > INT32_MAX / 2) return false;
+  const int64_t k1_ctas = pl->rows_total * pl->S;
+  if (k1_ctas >= INT32_MAX) return false;
+  if (draw && B * pl->P >= INT32_MAX) return false;
+  pl->excl_stride = static_cast<int32_t>(excl_stride < 1 ? 1 : excl_stride);
+  size_t off = 0;
+  pl->off_part = off;
+  off += align_up(static_cast<size_t>(k1_ctas) * sizeof(Partial), kAlign);
+  if (draw) {
+    pl->off_draw = off;
+    off += align_up(static_cast<size_t>(B) * sizeof(DrawDesc), kAlign);
+    pl->off_excl = off;
+    off += align_up(static_cast<size_t>(B) * pl->excl_stride * sizeof(int32_t), kAlign);
+    pl->off_k3part = off;
+    off += align_up(static_cast<size_t>(B) * pl->P * sizeof(float2), kAlign);
+    pl->off_k3cnt = off;
+    off += align_up(static_cast<size_t>(B) * sizeof(uint32_t), kAlign);
+  }
+  pl->total = off < kAlign ? kAlign : off;
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_temperature(float t) { return std::isfinite(t) && t >= 1e-4f; }
+
+sv_status check_rule(const sv_rule_params& r) {
+  if (r.rule != SV_RULE_EXACT && r.rule != SV_RULE_RELAXED && r.rule != SV_RULE_POWER)
+    return SV_ERR_INVALID_ARG;
+  if (r.rule == SV_RULE_POWER && !(std::isfinite(r.alpha) && r.alpha > 0.f)) return SV_ERR_INVALID_ARG;
+  if (r.rule == SV_RULE_RELAXED) {
+    if (std::isnan(r.tau)) return SV_ERR_INVALID_ARG;
+    if (r.top_k < 0 || r.top_k > SV_MAX_TOP_K) return SV_ERR_INVALID_ARG;
+    if (r.top_k > 0) return SV_ERR_NOT_SUPPORTED;
+  }
+  return SV_OK;
+}
+
+RuleArgs rule_args(const sv_rule_params& r) {
+  RuleArgs a;
+  a.rule = r.rule;
+  a.tau = r.tau;
+  a.top_k = r.top_k;
+  a.alpha = r.rule == SV_RULE_POWER ? r.alpha : 1.f;
+  return a;
+}
+
+template <typename Kern, typename Args>
+cudaError_t launch(Kern kernel, int grid, int block, size_t smem, cudaStream_t stream, bool pdl,
+                   const Args& args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
+template <int ES>
+cudaError_t launch_row_stats(const RowStatsArgs& a, int64_t ctas, cudaStream_t stream) {
+  return launch(row_stats_kernel<ES>, static_cast<int>(ctas), kK1Threads, kK1SegBytes, stream, false, a);
+}
+
+RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride_b, int64_t rows_t,
+                            const void* dft, int64_t dft_stride_b, int64_t rows_d, int32_t V,
+                            float c, void* ws) {
+  RowStatsArgs r;
+  r.set0.base = static_cast<const uint8_t*>(tgt);
+  r.set0.stride_bytes = tgt_stride_b;
+  r.set0.rows = static_cast<int32_t>(rows_t);
+  r.set1.base = static_cast<const uint8_t*>(dft);
+  r.set1.stride_bytes = dft_stride_b;
+  r.set1.rows = static_cast<int32_t>(rows_d);
+  r.V = V;
+  r.S = pl.S;
+  r.seg_elems = pl.seg_elems;
+  r.c = c;
+  r.partials = reinterpret_cast<Partial*>(static_cast<uint8_t*>(ws) + pl.off_part);
+  return r;
+}
+
+DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride_b, const void* dft,
+                   int64_t dft_stride_b, int32_t V, float c, void* ws, int32_t out_cols,
+                   int32_t* out_tokens, float* out_logprob, float* out_mu) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  DrawArgs d;
+  d.tgt = static_cast<const uint8_t*>(tgt);
+  d.tgt_stride = tgt_stride_b;
+  d.dft = static_cast<const uint8_t*>(dft);
+  d.dft_stride = dft_stride_b;
+  d.V = V;
+  d.P = pl.P;
+  d.chunk_elems = pl.chunk_elems;
+  d.c = c;
+  d.draws = reinterpret_cast<const DrawDesc*>(w + pl.off_draw);
+  d.excl = reinterpret_cast<const int32_t*>(w + pl.off_excl);
+  d.excl_stride = pl.excl_stride;
+  d.part = reinterpret_cast<float2*>(w + pl.off_k3part);
+  d.counters = reinterpret_cast<uint32_t*>(w + pl.off_k3cnt);
+  d.out_cols = out_cols;
+  d.out_tokens = out_tokens;
+  d.out_logprob = out_logprob;
+  d.out_mu = out_mu;
+  return d;
+}
+
+bool outputs_aligned(const void* a, const void* b, const void* c, const void* d, const void* e) {
+  return aligned(a, 4) && aligned(b, 4) && aligned(c, 4) && aligned(d, 4) && aligned(e, 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t spec_verify_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
+
+const char* spec_verify_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK: success";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: a pointer, size, stride or parameter is invalid";
+    case SV_ERR_UNSUPPORTED_DTYPE: return "SV_ERR_UNSUPPORTED_DTYPE: dtype must be SV_F32 or SV_BF16";
+    case SV_ERR_WORKSPACE_TOO_SMALL: return "SV_ERR_WORKSPACE_TOO_SMALL: workspace_bytes is below the required size";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA launch failed";
+    case SV_ERR_NOT_SUPPORTED: return "SV_ERR_NOT_SUPPORTED: valid request not implemented by this build";
+    default: return "unknown sv_status";
+  }
+}
+
+size_t spec_verify_greedy_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype) {
+  Plan pl;
+  if (B < 0 || K < 0 || !make_plan(static_cast<int64_t>(B) * (K + 1), 0, B, V, elem_size(dtype), false, 0, &pl))
+    return 0;
+  return pl.total;
+}
+
+size_t spec_verify_sample_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype,
+                                         int32_t has_draft_logits) {
+  Plan pl;
+  const int64_t rd = has_draft_logits ? static_cast<int64_t>(B) * K : 0;
+  if (B < 0 || K < 0 ||
+      !make_plan(static_cast<int64_t>(B) * (K + 1), rd, B, V, elem_size(dtype), true, 1, &pl))
+    return 0;
+  return pl.total;
+}
+
+size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V, int32_t dtype) {
+  Plan pl;
+  if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES ||
+      !make_plan(static_cast<int64_t>(B) * N, 0, B, V, elem_size(dtype), true, N, &pl))
+    return 0;
+  return pl.total;
+}
+
+sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t row_stride,
+                             const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                             int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
+                             float* out_mu, int32_t* out_status, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || K < 0 || V < 1 || row_stride < V) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target_logits || (K > 0 && !draft_tokens) || !out_tokens || !out_num_accepted || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (!aligned(target_logits, es) || !aligned(workspace, 16) || !aligned(draft_tokens, 4) ||
+      !outputs_aligned(out_tokens, out_num_accepted, out_logprob, out_mu, out_status))
+    return SV_ERR_INVALID_ARG;
+  Plan pl;
+  const int64_t rows = static_cast<int64_t>(B) * (K + 1);
+  if (!make_plan(rows, 0, B, V, es, false, 0, &pl)) return SV_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float c = kLog2e;
+  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride * es, rows, nullptr, 0, 0, V, c, workspace);
+  cudaError_t e = es == 2 ? launch_row_stats<2>(r, rows * pl.S, st) : launch_row_stats<4>(r, rows * pl.S, st);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  ChainArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tgt = static_cast<const uint8_t*>(target_logits);
+  a.tgt_stride = row_stride * es;
+  a.drafts = draft_tokens;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.S = pl.S;
+  a.part_t = r.partials;
+  a.c = c;
+  a.greedy = 1;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_logprob = out_logprob;
+  a.out_mu = out_mu;
+  a.out_status = out_status;
+  e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
+              : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t row_stride,
+                             const void* draft_logits, int64_t draft_row_stride,
+                             const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                             float temperature, const float* uniforms, sv_rule_params rule,
+                             int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
+                             float* out_mu, int32_t* out_status, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || K < 0 || V < 1 || row_stride < V) return SV_ERR_INVALID_ARG;
+  if (draft_logits && draft_row_stride < V) return SV_ERR_INVALID_ARG;
+  if (!valid_temperature(temperature)) return SV_ERR_INVALID_ARG;
+  const sv_status rs = check_rule(rule);
+  if (rs != SV_OK) return rs;
+  if (draft_logits && rule.rule != SV_RULE_EXACT) return SV_ERR_NOT_SUPPORTED;
+  if (B == 0) return SV_OK;
+  if (!target_logits || (K > 0 && !draft_tokens) || !uniforms || !out_tokens || !out_num_accepted ||
+      !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)) ||
+      !aligned(workspace, 16) || !aligned(draft_tokens, 4) || !aligned(uniforms, 4) ||
+      !outputs_aligned(out_tokens, out_num_accepted, out_logprob, out_mu, out_status))
+    return SV_ERR_INVALID_ARG;
+  Plan pl;
+  const int64_t rows_t = static_cast<int64_t>(B) * (K + 1);
+  const int64_t rows_d = draft_logits ? static_cast<int64_t>(B) * K : 0;
+  if (!make_plan(rows_t, rows_d, B, V, es, true, 1, &pl)) return SV_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float c = kLog2e / temperature;
+  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride * es, rows_t, draft_logits,
+                                        draft_row_stride * es, rows_d, V, c, workspace);
+  const int64_t ctas = (rows_t + rows_d) * pl.S;
+  cudaError_t e = es == 2 ? launch_row_stats<2>(r, ctas, st) : launch_row_stats<4>(r, ctas, st);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  ChainArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tgt = static_cast<const uint8_t*>(target_logits);
+  a.tgt_stride = row_stride * es;
+  a.dft = static_cast<const uint8_t*>(draft_logits);
+  a.dft_stride = draft_logits ? draft_row_stride * es : 0;
+  a.drafts = draft_tokens;
+  a.uniforms = uniforms;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.S = pl.S;
+  a.part_t = r.partials;
+  a.part_d = r.partials + rows_t * pl.S;
+  a.c = c;
+  a.greedy = 0;
+  a.rule = rule_args(rule);
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_logprob = out_logprob;
+  a.out_mu = out_mu;
+  a.out_status = out_status;
+  a.draws = reinterpret_cast<DrawDesc*>(w + pl.off_draw);
+  a.excl = reinterpret_cast<int32_t*>(w + pl.off_excl);
+  a.excl_stride = pl.excl_stride;
+  a.draw_counters = reinterpret_cast<uint32_t*>(w + pl.off_k3cnt);
+  e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
+              : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  const DrawArgs d = draw_args(pl, target_logits, row_stride * es, draft_logits,
+                               draft_logits ? draft_row_stride * es : 0, V, c, workspace, K + 1,
+                               out_tokens, out_logprob, out_mu);
+  const int grid3 = B * pl.P;
+  e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
+              : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row_stride,
+                           const int32_t* node_tokens, const int32_t* parents, int32_t B,
+                           int32_t N, int32_t V, int32_t max_depth, float temperature,
+                           const float* uniforms, sv_rule_params rule, int32_t* out_tokens,
+                           int32_t* out_nodes, int32_t* out_num_accepted, float* out_logprob,
+                           float* out_mu, int32_t* out_status, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || row_stride < V || max_depth < 0 ||
+      max_depth > INT32_MAX - 1)
+    return SV_ERR_INVALID_ARG;
+  const bool greedy = temperature == 0.f;
+  if (!greedy && !valid_temperature(temperature)) return SV_ERR_INVALID_ARG;
+  if (!greedy) {
+    const sv_status rs = check_rule(rule);
+    if (rs != SV_OK) return rs;
+  }
+  if (B == 0) return SV_OK;
+  if (!target_logits || !node_tokens || !parents || (!greedy && !uniforms) || !out_tokens ||
+      !out_nodes || !out_num_accepted || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (!aligned(target_logits, es) || !aligned(workspace, 16) || !aligned(node_tokens, 4) ||
+      !aligned(parents, 4) || !aligned(uniforms, 4) || !aligned(out_nodes, 4) ||
+      !outputs_aligned(out_tokens, out_num_accepted, out_logprob, out_mu, out_status))
+    return SV_ERR_INVALID_ARG;
+  Plan pl;
+  const int64_t rows = static_cast<int64_t>(B) * N;
+  if (!make_plan(rows, 0, B, V, es, true, N, &pl)) return SV_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float c = greedy ? kLog2e : kLog2e / temperature;
+  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride * es, rows, nullptr, 0, 0, V, c, workspace);
+  cudaError_t e = es == 2 ? launch_row_stats<2>(r, rows * pl.S, st) : launch_row_stats<4>(r, rows * pl.S, st);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  TreeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tgt = static_cast<const uint8_t*>(target_logits);
+  a.tgt_stride = row_stride * es;
+  a.tokens = node_tokens;
+  a.parents = parents;
+  a.uniforms = uniforms;
+  a.B = B;
+  a.N = N;
+  a.V = V;
+  a.S = pl.S;
+  a.max_depth = max_depth;
+  a.part = r.partials;
+  a.c = c;
+  a.greedy = greedy ? 1 : 0;
+  a.rule = rule_args(rule);
+  a.out_tokens = out_tokens;
+  a.out_nodes = out_nodes;
+  a.out_num = out_num_accepted;
+  a.out_logprob = out_logprob;
+  a.out_mu = out_mu;
+  a.out_status = out_status;
+  a.draws = reinterpret_cast<DrawDesc*>(w + pl.off_draw);
+  a.excl = reinterpret_cast<int32_t*>(w + pl.off_excl);
+  a.excl_stride = pl.excl_stride;
+  a.draw_counters = reinterpret_cast<uint32_t*>(w + pl.off_k3cnt);
+  e = es == 2 ? launch(tree_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
+              : launch(tree_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  if (greedy) return SV_OK;
+  const DrawArgs d = draw_args(pl, target_logits, row_stride * es, nullptr, 0, V, c, workspace,
+                               max_depth + 1, out_tokens, out_logprob, out_mu);
+  const int grid3 = B * pl.P;
+  e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
+              : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // extern "C"

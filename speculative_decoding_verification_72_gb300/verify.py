@@ -1,0 +1,259 @@
+"""Thin ctypes binding of libspecverify (include/spec_verify.h).
+
+Argument marshalling only: every step of verification runs in the library's
+CUDA kernels. Tensors are torch CUDA tensors; outputs and the workspace are
+allocated here with torch (device memory plumbing) and the call is enqueued
+on the current torch stream of the input's device. There is no CPU fallback:
+a missing library or a CPU tensor raises SpecVerifyError.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+SV_OK = 0
+SV_F32 = 0
+SV_BF16 = 1
+
+RULE_EXACT = 0
+RULE_RELAXED = 1
+RULE_POWER = 2
+
+STATUS_BAD_TOKEN = 1
+STATUS_BAD_PARENT = 2
+STATUS_NONFINITE_ROW = 4
+STATUS_ZERO_MASS = 8
+STATUS_DEPTH_EXCEEDED = 16
+STATUS_TIMEOUT = 32
+
+_LIB = None
+_LOCK = threading.Lock()
+_WS = {}
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+class RuleParams(ctypes.Structure):
+    _fields_ = [("rule", ctypes.c_int32), ("tau", ctypes.c_float),
+                ("top_k", ctypes.c_int32), ("alpha", ctypes.c_float)]
+
+
+def library_path():
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libspecverify.so")
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+_SIGS = {
+    "spec_verify_abi_version": (_I32, []),
+    "spec_verify_status_string": (ctypes.c_char_p, [_I32]),
+    "spec_verify_greedy_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "spec_verify_sample_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "spec_verify_tree_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "spec_verify_greedy": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
+                                  _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_sample": (_I32, [_P, _I32, _I64, _P, _I64, _P, _I32, _I32, _I32,
+                                  _F, _P, RuleParams,
+                                  _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_tree": (_I32, [_P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32,
+                                _F, _P, RuleParams,
+                                _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+}
+
+
+def load_library(path=None):
+    """Load libspecverify.so (built in-tree by __graft_entry__.build())."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None and path is None:
+            return _LIB
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise SpecVerifyError(
+                f"libspecverify.so is not built at {p}; run __graft_entry__.build() first")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _LIB = lib
+        return lib
+
+
+def _check(rc):
+    if rc != SV_OK:
+        msg = load_library().spec_verify_status_string(rc).decode()
+        raise SpecVerifyError(f"libspecverify returned {rc}: {msg}")
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise SpecVerifyError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _rows_view(t, name):
+    """(tensor, row_stride) for a [B, R, V] logits tensor whose rows are evenly
+    strided (unit stride along V); otherwise a contiguous copy."""
+    if t.dim() != 3:
+        raise SpecVerifyError(f"{name} must be [B, rows, V]")
+    if not t.is_cuda:
+        raise SpecVerifyError(f"{name} must be a CUDA tensor")
+    B, R, V = t.shape
+    if t.stride(2) != 1 and V > 1:
+        t = t.contiguous()
+    if R > 1:
+        rs, ok = t.stride(1), (B == 1 or t.stride(0) == R * t.stride(1))
+    elif B > 1:
+        rs, ok = t.stride(0), True
+    else:
+        rs, ok = V, True
+    if not ok or rs < V:
+        t = t.contiguous()
+        rs = V
+    return t, rs
+
+
+def _i32(t, name, shape, device):
+    if not isinstance(t, torch.Tensor):
+        t = torch.as_tensor(t)
+    if tuple(t.shape) != tuple(shape):
+        raise SpecVerifyError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.to(device=device, dtype=torch.int32).contiguous()
+
+
+def _f32(t, name, shape, device):
+    if not isinstance(t, torch.Tensor):
+        t = torch.as_tensor(t)
+    if tuple(t.shape) != tuple(shape):
+        raise SpecVerifyError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.to(device=device, dtype=torch.float32).contiguous()
+
+
+def _workspace(nbytes, device, stream):
+    key = (device.index, stream)
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+        _WS[key] = ws
+    return ws
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _outputs(B, cols, device, want_nodes=False):
+    out = dict(
+        tokens=torch.empty((B, cols), dtype=torch.int32, device=device),
+        num_accepted=torch.empty((B,), dtype=torch.int32, device=device),
+        logprob=torch.empty((B, cols), dtype=torch.float32, device=device),
+        mu=torch.empty((B, cols), dtype=torch.float32, device=device),
+        status=torch.empty((B,), dtype=torch.int32, device=device),
+    )
+    if want_nodes:
+        out["nodes"] = torch.empty((B, cols), dtype=torch.int32, device=device)
+    return out
+
+
+def _rule(rule, tau, top_k, alpha):
+    return RuleParams(int(rule), float(tau), int(top_k), float(alpha))
+
+
+def spec_verify_greedy(target_logits, draft_tokens, workspace=None):
+    """Greedy chain verification. target_logits [B, K+1, V] (bf16 / fp32,
+    CUDA), draft_tokens [B, K]. Returns a dict of CUDA tensors: tokens,
+    num_accepted, logprob, mu, status."""
+    lib = load_library()
+    x, stride = _rows_view(target_logits, "target_logits")
+    B, R, V = x.shape
+    K = R - 1
+    dev = x.device
+    d = _i32(draft_tokens, "draft_tokens", (B, K), dev)
+    out = _outputs(B, R, dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    need = lib.spec_verify_greedy_workspace_size(B, K, V, _dtype_code(x))
+    if need == 0 and B > 0:
+        raise SpecVerifyError("invalid sizes")
+    ws = workspace if workspace is not None else _workspace(need, dev, stream)
+    rc = lib.spec_verify_greedy(_ptr(x), _dtype_code(x), stride, _ptr(d), B, K, V,
+                                _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
+                                _ptr(ws), ws.numel(), ctypes.c_void_p(stream))
+    _check(rc)
+    return out
+
+
+def spec_verify_sample(target_logits, draft_tokens, uniforms, draft_logits=None,
+                       temperature=1.0, rule=RULE_EXACT, tau=0.0, top_k=0, alpha=1.0,
+                       workspace=None):
+    """Stochastic chain verification (see include/spec_verify.h)."""
+    lib = load_library()
+    x, stride = _rows_view(target_logits, "target_logits")
+    B, R, V = x.shape
+    K = R - 1
+    dev = x.device
+    y, dstride = (None, 0)
+    if draft_logits is not None:
+        if draft_logits.dtype != x.dtype:
+            raise SpecVerifyError("draft_logits must have the target's dtype")
+        y, dstride = _rows_view(draft_logits, "draft_logits")
+        if tuple(y.shape) != (B, K, V):
+            raise SpecVerifyError(f"draft_logits must be {(B, K, V)}")
+    d = _i32(draft_tokens, "draft_tokens", (B, K), dev)
+    u = _f32(uniforms, "uniforms", (B, R), dev)
+    out = _outputs(B, R, dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    need = lib.spec_verify_sample_workspace_size(B, K, V, _dtype_code(x), int(y is not None))
+    ws = workspace if workspace is not None else _workspace(need, dev, stream)
+    rc = lib.spec_verify_sample(_ptr(x), _dtype_code(x), stride, _ptr(y), dstride, _ptr(d),
+                                B, K, V, float(temperature), _ptr(u),
+                                _rule(rule, tau, top_k, alpha),
+                                _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
+                                _ptr(ws), ws.numel(), ctypes.c_void_p(stream))
+    _check(rc)
+    return out
+
+
+def spec_verify_tree(target_logits, node_tokens, parents, max_depth, temperature=0.0,
+                     uniforms=None, rule=RULE_EXACT, tau=0.0, top_k=0, alpha=1.0,
+                     workspace=None):
+    """Tree verification (see include/spec_verify.h). temperature 0 = greedy."""
+    lib = load_library()
+    x, stride = _rows_view(target_logits, "target_logits")
+    B, N, V = x.shape
+    dev = x.device
+    tok = _i32(node_tokens, "node_tokens", (B, N), dev)
+    par = _i32(parents, "parents", (B, N), dev)
+    u = None
+    if float(temperature) != 0.0:
+        u = _f32(uniforms, "uniforms", (B, N), dev)
+    W = int(max_depth) + 1
+    out = _outputs(B, W, dev, want_nodes=True)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    need = lib.spec_verify_tree_workspace_size(B, N, V, _dtype_code(x))
+    if need == 0 and B > 0:
+        raise SpecVerifyError("invalid sizes")
+    ws = workspace if workspace is not None else _workspace(need, dev, stream)
+    rc = lib.spec_verify_tree(_ptr(x), _dtype_code(x), stride, _ptr(tok), _ptr(par), B, N, V,
+                              int(max_depth), float(temperature), _ptr(u),
+                              _rule(rule, tau, top_k, alpha),
+                              _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["num_accepted"]),
+                              _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
+                              _ptr(ws), ws.numel(), ctypes.c_void_p(stream))
+    _check(rc)
+    return out

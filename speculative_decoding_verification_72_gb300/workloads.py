@@ -67,6 +67,8 @@ def _normal_logits(B, R, V, std, dtype, device, g, chunk_rows=4096):
 
 
 def _other_ids(argmax, V, g, device):
+    if V == 1:
+        return torch.zeros_like(argmax)
     r = torch.randint(0, V - 1, argmax.shape, generator=g, device=device, dtype=torch.int64)
     return r + (r >= argmax).to(torch.int64)
 

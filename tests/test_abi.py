@@ -1,0 +1,145 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/spec_verify.h declares, and rejects invalid arguments on the host
+with the documented codes before launching anything."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_72_gb300 as sv
+from speculative_decoding_verification_72_gb300 import verify as V
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED_DTYPE = 0, 1, 2
+SV_ERR_WORKSPACE_TOO_SMALL, SV_ERR_NOT_SUPPORTED = 3, 5
+FAKE = 0x10000          # 64 KB-aligned stand-in for a device pointer; never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(sv.library_path()):
+        from speculative_decoding_verification_72_gb300 import build
+        build.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_verify_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("spec_verify_greedy", "spec_verify_sample", "spec_verify_tree",
+              "spec_verify_status_string", "spec_verify_abi_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in V._SIGS, f"binding lacks a signature for {name}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.spec_verify_abi_version() == 1
+    for code in range(6):
+        s = lib.spec_verify_status_string(code).decode()
+        assert s and "unknown" not in s
+    assert "unknown" in lib.spec_verify_status_string(99).decode()
+
+
+def test_workspace_sizes(lib):
+    g = lib.spec_verify_greedy_workspace_size(32, 5, 128256, 1)
+    assert g >= 32 * 6 * 16 and g % 256 == 0
+    assert lib.spec_verify_sample_workspace_size(64, 4, 151936, 0, 1) > \
+        lib.spec_verify_sample_workspace_size(64, 4, 151936, 0, 0)
+    assert lib.spec_verify_tree_workspace_size(32, 64, 128256, 1) > 0
+    assert lib.spec_verify_greedy_workspace_size(4, 5, 0, 1) == 0      # V < 1
+    assert lib.spec_verify_greedy_workspace_size(4, 5, 100, 7) == 0    # dtype
+    assert lib.spec_verify_tree_workspace_size(4, 2000, 100, 1) == 0   # N too large
+    assert lib.spec_verify_greedy_workspace_size(0, 5, 100, 1) > 0
+
+
+def _greedy(lib, **kw):
+    a = dict(x=FAKE, dtype=1, stride=100, d=FAKE, B=2, K=3, V=100,
+             tok=FAKE, num=FAKE, lp=FAKE, mu=FAKE, st=FAKE, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify_greedy(P(a["x"]), a["dtype"], a["stride"], P(a["d"]), a["B"], a["K"],
+                                  a["V"], P(a["tok"]), P(a["num"]), P(a["lp"]), P(a["mu"]),
+                                  P(a["st"]), P(a["ws"]), a["wsb"], P(0))
+
+
+def test_greedy_host_validation(lib):
+    assert _greedy(lib, dtype=3) == SV_ERR_UNSUPPORTED_DTYPE
+    assert _greedy(lib, V=0) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, K=-1) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, stride=99) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, x=0) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, d=0) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, tok=0) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, ws=0) == SV_ERR_INVALID_ARG
+    assert _greedy(lib, x=FAKE + 1) == SV_ERR_INVALID_ARG          # misaligned bf16
+    assert _greedy(lib, ws=FAKE + 8) == SV_ERR_INVALID_ARG         # workspace not 16-byte aligned
+    assert _greedy(lib, wsb=16) == SV_ERR_WORKSPACE_TOO_SMALL
+    assert _greedy(lib, B=0, x=0, d=0, tok=0, num=0, ws=0) == SV_OK  # nothing to do
+
+
+def _sample(lib, rule=(0, 0.0, 0, 1.0), T=1.0, draft=FAKE, **kw):
+    a = dict(x=FAKE, dtype=0, stride=100, d=FAKE, B=2, K=3, V=100, u=FAKE, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify_sample(P(a["x"]), a["dtype"], a["stride"], P(draft), 100, P(a["d"]),
+                                  a["B"], a["K"], a["V"], T, P(a["u"]), V.RuleParams(*rule),
+                                  P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                  P(a["ws"]), a["wsb"], P(0))
+
+
+def test_sample_host_validation(lib):
+    assert _sample(lib, T=0.0) == SV_ERR_INVALID_ARG
+    assert _sample(lib, T=float("nan")) == SV_ERR_INVALID_ARG
+    assert _sample(lib, T=float("inf")) == SV_ERR_INVALID_ARG
+    assert _sample(lib, u=0) == SV_ERR_INVALID_ARG
+    assert _sample(lib, rule=(7, 0.0, 0, 1.0)) == SV_ERR_INVALID_ARG
+    assert _sample(lib, rule=(2, 0.0, 0, 0.0), draft=0) == SV_ERR_INVALID_ARG     # alpha <= 0
+    assert _sample(lib, rule=(1, float("nan"), 0, 1.0), draft=0) == SV_ERR_INVALID_ARG
+    assert _sample(lib, rule=(1, 0.1, 99, 1.0), draft=0) == SV_ERR_INVALID_ARG    # top_k > max
+    assert _sample(lib, rule=(1, 0.1, 2, 1.0), draft=0) == SV_ERR_NOT_SUPPORTED
+    assert _sample(lib, rule=(2, 0.0, 0, 0.3)) == SV_ERR_NOT_SUPPORTED            # power with q
+    assert _sample(lib, wsb=64) == SV_ERR_WORKSPACE_TOO_SMALL
+
+
+def _tree(lib, T=0.0, **kw):
+    a = dict(x=FAKE, dtype=1, stride=100, tok=FAKE, par=FAKE, B=2, N=8, V=100, depth=5,
+             u=FAKE, nodes=FAKE, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify_tree(P(a["x"]), a["dtype"], a["stride"], P(a["tok"]), P(a["par"]),
+                                a["B"], a["N"], a["V"], a["depth"], T, P(a["u"]),
+                                V.RuleParams(0, 0.0, 0, 1.0),
+                                P(FAKE), P(a["nodes"]), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                P(a["ws"]), a["wsb"], P(0))
+
+
+def test_tree_host_validation(lib):
+    assert _tree(lib, N=0) == SV_ERR_INVALID_ARG
+    assert _tree(lib, N=1025) == SV_ERR_INVALID_ARG
+    assert _tree(lib, depth=-1) == SV_ERR_INVALID_ARG
+    assert _tree(lib, par=0) == SV_ERR_INVALID_ARG
+    assert _tree(lib, nodes=0) == SV_ERR_INVALID_ARG
+    assert _tree(lib, T=0.5, u=0) == SV_ERR_INVALID_ARG
+    assert _tree(lib, T=-1.0) == SV_ERR_INVALID_ARG
+    assert _tree(lib, wsb=32) == SV_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros((1, 2, 8))
+    with pytest.raises(sv.SpecVerifyError):
+        sv.spec_verify_greedy(x, torch.zeros((1, 1), dtype=torch.int32))
