@@ -1,0 +1,523 @@
+#!/usr/bin/env python3
+"""Throughput of batched speculative-decoding verification on GB300.
+
+Metric: verified logit rows/s (B*(K+1) target rows per step for a chain,
+B*N for a tree) and the achieved HBM bandwidth on the algorithmic bytes
+(every input logit row read once, plus the small index/uniform arrays and
+the outputs).
+
+A step is one verification call (all of its kernels) over one batch of
+seeded synthetic inputs. Inputs are resident in HBM before timing. Steps cycle
+through a pool of input sets whose total size exceeds 4x the L2 cache, so no
+step reads inputs another step left in L2. Steps are replayed from CUDA graphs
+(one call = the row-statistics kernel plus the decide kernel, and the draw
+kernel for stochastic rules) and timed with CUDA events on the launching
+stream, bracketed by a barrier and a device synchronize.
+
+  python bench.py                      # default workload, 1 GPU
+  python bench.py --config qwen_sample --steps 2000 --warmup 20
+  python bench.py --impl reference     # the float64 CPU oracle as the reference arm
+  torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas (weak scaling)
+
+One JSON line is printed by rank 0.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+CONFIGS = {
+    "llama_greedy": dict(kind="greedy", B=32, K=5, V=128256, dtype="bf16", p_match=0.8, seed=7201,
+                         workload="greedy chain verify: Llama-3 vocab V=128256, bf16 logits N(0,3^2), "
+                                  "K=5 drafts (6 rows/request), B=32, drafts = row argmax w.p. 0.8"),
+    "llama_greedy_b8": dict(kind="greedy", B=8, K=5, V=128256, dtype="bf16", p_match=0.8, seed=7201,
+                            workload="greedy chain verify: V=128256 bf16, K=5, B=8"),
+    "llama_greedy_b1": dict(kind="greedy", B=1, K=5, V=128256, dtype="bf16", p_match=0.8, seed=7201,
+                            workload="greedy chain verify: V=128256 bf16, K=5, B=1"),
+    "qwen_sample": dict(kind="sample", B=64, K=4, V=151936, dtype="fp32", seed=7202,
+                        workload="stochastic chain verify (exact rule): Qwen vocab V=151936, fp32 target "
+                                 "logits N(0,3^2), draft logits = target + N(0,1), T=1, B=64, K=4"),
+    "eagle_tree_greedy": dict(kind="tree", B=32, N=64, V=128256, dtype="bf16", T=0.0, rule=0, seed=7203,
+                              workload="EAGLE-3 tree verify (greedy): depth 5 / topk 4 pruned to 64 nodes, "
+                                       "V=128256 bf16, B=32"),
+    "eagle_tree_power": dict(kind="tree", B=32, N=64, V=128256, dtype="bf16", T=1.0, rule=2, alpha=0.3,
+                             seed=7203, workload="EAGLE-3 tree verify (power rule alpha=0.3, T=1), "
+                                                 "64 nodes, V=128256 bf16, B=32"),
+    "eagle_tree_relaxed": dict(kind="tree", B=32, N=64, V=128256, dtype="bf16", T=1.0, rule=1, tau=0.1,
+                               seed=7203, workload="EAGLE-3 tree verify (relaxed rule tau=0.1, T=1), "
+                                                   "64 nodes, V=128256 bf16, B=32"),
+    "long_chain": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
+                       workload="long-chain greedy verify: GPT-2 vocab V=50257 bf16, B=8, K+1=4096 rows "
+                                "per request, drafts = argmax w.p. 0.95"),
+}
+DEFAULT_CONFIG = "llama_greedy"
+KERNELS_PER_CALL = {"greedy": 2, "sample": 3, "tree": 2}
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------ host helpers
+
+def rank_seed(base, rank):
+    """Each rank verifies its own requests (weak scaling): a distinct seed."""
+    return int(base) + 1000003 * int(rank)
+
+
+def aggregate(elapsed_ms_max, rows_per_step, steps, world):
+    """Whole-job rows/s from the slowest rank's timed region."""
+    return world * rows_per_step * steps / (elapsed_ms_max / 1e3)
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_72_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(config_name):
+    """DRAM bytes per call from the committed ncu capture, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic_by_workload.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(config_name)
+        if e and e.get("source_hash") == source_hash():
+            return float(e["dram_bytes_per_call"])
+    except Exception:
+        pass
+    return None
+
+
+def algorithmic_bytes(cfg):
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    B, V = cfg["B"], cfg["V"]
+    if cfg["kind"] == "tree":
+        N = cfg["N"]
+        W = 6
+        rows = B * N
+        logits = rows * V * es
+        small = B * N * 4 * 2 + (B * N * 4 if cfg.get("T", 0) else 0)
+        outs = B * W * (4 + 4 + 4 + 4) + B * 8
+        return rows, logits + small + outs
+    K = cfg["K"]
+    rows = B * (K + 1)
+    logits = rows * V * es
+    if cfg["kind"] == "sample":
+        logits += B * K * V * es
+    small = B * K * 4 + (B * (K + 1) * 4 if cfg["kind"] == "sample" else 0)
+    outs = B * (K + 1) * 12 + B * 8
+    return rows, logits + small + outs
+
+
+# ------------------------------------------------------------ clock sampler
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank_gpu{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return None
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                    except ValueError:
+                        continue
+        except OSError:
+            return None
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in used])),
+                "sm_max_mhz": float(max(r[2] for r in used)),
+                "reasons": reasons, "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------ workloads
+
+def make_inputs(cfg, seed, device):
+    import torch
+    from speculative_decoding_verification_72_gb300 import workloads as W
+    dt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    if cfg["kind"] == "greedy":
+        return W.greedy_chain(B=cfg["B"], K=cfg["K"], V=cfg["V"], dtype=dt, p_match=cfg["p_match"],
+                              seed=seed, device=device)
+    if cfg["kind"] == "sample":
+        return W.stochastic_chain(B=cfg["B"], K=cfg["K"], V=cfg["V"], dtype=dt, seed=seed, device=device)
+    return W.eagle_tree(B=cfg["B"], V=cfg["V"], n_nodes=cfg["N"], dtype=dt, seed=seed, device=device)
+
+
+def call(cfg, x, out=None, ws=None):
+    import speculative_decoding_verification_72_gb300 as sv
+    if cfg["kind"] == "greedy":
+        return sv.spec_verify_greedy(x.target, x.draft_tokens, workspace=ws, out=out)
+    if cfg["kind"] == "sample":
+        return sv.spec_verify_sample(x.target, x.draft_tokens, x.uniforms, draft_logits=x.draft_logits,
+                                     workspace=ws, out=out)
+    return sv.spec_verify_tree(x.target, x.node_tokens, x.parents, x.max_depth,
+                               temperature=cfg.get("T", 0.0), uniforms=x.uniforms,
+                               rule=cfg.get("rule", 0), tau=cfg.get("tau", 0.0),
+                               alpha=cfg.get("alpha", 1.0), workspace=ws, out=out)
+
+
+def input_bytes(x):
+    n = 0
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents"):
+        t = getattr(x, k, None)
+        if t is not None:
+            n += t.numel() * t.element_size()
+    return n
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_rows_per_s(cfg, x_host, budget_s, max_requests=None):
+    """The float64 oracle, as it stands, on whole requests of one input set
+    until budget_s elapses (at least one request). Returns (rows/s, requests)."""
+    from oracle import spec_oracle as O
+    B = cfg["B"]
+    done_rows, t_used, r = 0, 0.0, 0
+    while (t_used < budget_s or r == 0) and r < B and (max_requests is None or r < max_requests):
+        sl = slice(r, r + 1)
+        t0 = time.perf_counter()
+        if cfg["kind"] == "greedy":
+            O.verify_greedy(x_host["target"][sl], x_host["draft_tokens"][sl])
+            rows = cfg["K"] + 1
+        elif cfg["kind"] == "sample":
+            O.verify_sample(x_host["target"][sl], x_host["draft_logits"][sl], x_host["draft_tokens"][sl],
+                            1.0, x_host["uniforms"][sl])
+            rows = cfg["K"] + 1
+        else:
+            O.verify_tree(x_host["target"][sl], x_host["node_tokens"][sl], x_host["parents"][sl], 5,
+                          cfg.get("T", 0.0), x_host["uniforms"][sl], rule=cfg.get("rule", 0),
+                          tau=cfg.get("tau", 0.0), alpha=cfg.get("alpha", 1.0))
+            rows = cfg["N"]
+        t_used += time.perf_counter() - t0
+        done_rows += rows
+        r += 1
+    return done_rows / t_used, r
+
+
+def host_copy(x):
+    d = {}
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents"):
+        t = getattr(x, k, None)
+        if t is None:
+            continue
+        if t.is_floating_point():
+            d[k] = t.float().cpu().numpy().astype(np.float64)
+        else:
+            d[k] = t.cpu().numpy()
+    return d
+
+
+def run_reference(args, cfg, name):
+    """Reference arm: the float64 CPU oracle timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    steps = args.steps if args.steps is not None else 20
+    warmup = args.warmup if args.warmup is not None else 3
+    x = host_copy(make_inputs(cfg, cfg["seed"], "cpu"))
+    # size one step's sample so the whole run stays within about two minutes
+    t_req = oracle_rows_per_s(cfg, x, 0.0, max_requests=1)
+    rows_req = (cfg["K"] + 1) if cfg["kind"] != "tree" else cfg["N"]
+    per_req_s = rows_req / t_req[0]
+    reqs_per_step = max(1, min(cfg["B"], int(120.0 / max(steps + warmup, 1) / per_req_s)))
+    from oracle import spec_oracle as O  # noqa: F401
+    for _ in range(warmup):
+        oracle_rows_per_s(cfg, x, 0.0, max_requests=1)
+    total_rows, total_t = 0, 0.0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        rps, r = oracle_rows_per_s(cfg, x, 1e9, max_requests=reqs_per_step)
+        total_t += time.perf_counter() - t0
+        total_rows += r * rows_req
+    value = total_rows / total_t
+    line = {
+        "impl": "reference", "metric": "verified logit rows/s", "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
+        "ms_per_step": 1e3 * total_t / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["workload"], "name": name},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{reqs_per_step} request(s) of {cfg['B']} per step, float64 NumPy "
+                                   f"oracle, one thread"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------ GPU arm
+
+def run_gpu(args, cfg, name):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import speculative_decoding_verification_72_gb300 as sv
+    sv.load_library()
+    steps = args.steps if args.steps is not None else 100000
+    warmup = max(3, args.warmup if args.warmup is not None else 200)
+
+    rows, alg_bytes = algorithmic_bytes(cfg)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20) or (126 << 20)
+    first = make_inputs(cfg, rank_seed(cfg["seed"], rank), dev)
+    set_bytes = input_bytes(first)
+    nsets = max(2, min(64, math.ceil(4 * l2 / set_bytes)))
+    pool = [first] + [make_inputs(cfg, rank_seed(cfg["seed"] + 17 * i, rank), dev) for i in range(1, nsets)]
+    out = call(cfg, pool[0])
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    need = _workspace_need(cfg)
+    if ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    per_graph = nsets * max(1, math.ceil(32 / nsets))
+    graphs = {}
+
+    def graph_of(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for i in range(n):               # warm the capture stream
+                    call(cfg, pool[i % nsets], out=out, ws=ws)
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        call(cfg, pool[i % nsets], out=out, ws=ws)
+            torch.cuda.synchronize()
+            graphs[n] = g
+        return graphs[n]
+
+    full, rem = divmod(steps, per_graph)
+    g_full = graph_of(per_graph) if full else None
+    g_rem = graph_of(rem) if rem else None
+    g_warm = graph_of(per_graph)
+    for _ in range(max(1, math.ceil(warmup / per_graph))):
+        g_warm.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed = e0.elapsed_time(e1)
+    time.sleep(0.3)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    value = aggregate(elapsed, rows, steps, world)
+    step_s = elapsed / 1e3 / steps
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / step_s / 1e9
+
+    e2e = _e2e(cfg, pool[0], dev, steps, out, ws)
+    if world > 1:
+        t = torch.tensor([e2e["value"]], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MIN)
+        e2e["value"] = float(t.item()) * world
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xh = host_copy(pool[0])
+        rps, nreq = oracle_rows_per_s(cfg, xh, args.cpu_budget)
+        cpu = {"value": rps, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{nreq} of {cfg['B']} requests of one input set (~{args.cpu_budget:.0f} s), "
+                         f"float64 NumPy oracle, one thread"}
+
+    line = {
+        "metric": "verified logit rows/s", "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": elapsed / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes from the pages, no dataset or weights)",
+        "config": {"workload": cfg["workload"], "name": name, "B": cfg["B"],
+                   "rows_per_step": rows, "algorithmic_bytes_per_step": alg_bytes,
+                   "l2_policy": f"rotating pool of {nsets} input sets, {nsets * set_bytes / 1e6:.0f} MB "
+                                f"> 4x L2 ({l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graphs of {per_graph} calls, events on the launch stream",
+                   "parallelism": f"{world} independent replica(s)"},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "one verify call: row_stats_kernel (all logit bytes) + decide kernel"
+                               + (" + draw kernel" if _launches_per_call(cfg) == 3 else ""),
+                     "traffic": recorded_traffic(name)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": steps * _launches_per_call(cfg),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _launches_per_call(cfg):
+    return KERNELS_PER_CALL[cfg["kind"]] + (1 if cfg["kind"] == "tree" and cfg.get("T") else 0)
+
+
+def _workspace_need(cfg):
+    import speculative_decoding_verification_72_gb300 as sv
+    lib = sv.load_library()
+    dt = 1 if cfg["dtype"] == "bf16" else 0
+    if cfg["kind"] == "greedy":
+        return lib.spec_verify_greedy_workspace_size(cfg["B"], cfg["K"], cfg["V"], dt)
+    if cfg["kind"] == "sample":
+        return lib.spec_verify_sample_workspace_size(cfg["B"], cfg["K"], cfg["V"], dt, 1)
+    return lib.spec_verify_tree_workspace_size(cfg["B"], cfg["N"], cfg["V"], dt)
+
+
+def _e2e(cfg, x, dev, steps, out, ws):
+    """Same metric through the public API with host buffers: every step copies
+    that step's inputs from pinned host memory and reads the results back."""
+    import torch
+    names = [k for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents")
+             if getattr(x, k, None) is not None]
+    host = {k: getattr(x, k).cpu().pin_memory() for k in names}
+    devb = {k: torch.empty_like(getattr(x, k)) for k in names}
+    outh = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outh.values())
+    n = max(3, min(steps, 300))
+
+    class Inp:
+        pass
+
+    inp = Inp()
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents"):
+        setattr(inp, k, devb.get(k))
+    inp.max_depth = getattr(x, "max_depth", None)
+
+    def one():
+        for k in names:
+            devb[k].copy_(host[k], non_blocking=True)
+        res = call(cfg, inp, out=out, ws=ws)
+        for k in outh:
+            outh[k].copy_(res[k], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    rows, _ = algorithmic_bytes(cfg)
+    return {"value": rows / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg, args.config)
+    return run_gpu(args, cfg, args.config)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -152,11 +152,30 @@ def _workspace(nbytes, device, stream):
     return ws
 
 
+def _ws(workspace, need, dev, stream):
+    if workspace is None:
+        return _workspace(need, dev, stream)
+    if workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
+        raise SpecVerifyError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    return workspace
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _outputs(B, cols, device, want_nodes=False):
+def _outputs(B, cols, device, want_nodes=False, out=None):
+    """Fresh output tensors, or the caller's (checked) when `out` is given."""
+    if out is not None:
+        need = {"tokens": (B, cols), "num_accepted": (B,), "logprob": (B, cols),
+                "mu": (B, cols), "status": (B,)}
+        if want_nodes:
+            need["nodes"] = (B, cols)
+        for k, shp in need.items():
+            t = out.get(k)
+            if t is None or tuple(t.shape) != shp or not t.is_contiguous() or t.device != device:
+                raise SpecVerifyError(f"out[{k!r}] must be a contiguous {shp} tensor on {device}")
+        return out
     out = dict(
         tokens=torch.empty((B, cols), dtype=torch.int32, device=device),
         num_accepted=torch.empty((B,), dtype=torch.int32, device=device),
@@ -173,33 +192,35 @@ def _rule(rule, tau, top_k, alpha):
     return RuleParams(int(rule), float(tau), int(top_k), float(alpha))
 
 
-def spec_verify_greedy(target_logits, draft_tokens, workspace=None):
+def spec_verify_greedy(target_logits, draft_tokens, workspace=None, out=None):
     """Greedy chain verification. target_logits [B, K+1, V] (bf16 / fp32,
     CUDA), draft_tokens [B, K]. Returns a dict of CUDA tensors: tokens,
-    num_accepted, logprob, mu, status."""
+    num_accepted, logprob, mu, status (the caller's `out` dict if given;
+    with `out` and `workspace` given the call allocates nothing and can be
+    captured in a CUDA graph)."""
     lib = load_library()
     x, stride = _rows_view(target_logits, "target_logits")
     B, R, V = x.shape
     K = R - 1
     dev = x.device
     d = _i32(draft_tokens, "draft_tokens", (B, K), dev)
-    out = _outputs(B, R, dev)
+    out = _outputs(B, R, dev, out=out)
     stream = torch.cuda.current_stream(dev).cuda_stream
     need = lib.spec_verify_greedy_workspace_size(B, K, V, _dtype_code(x))
     if need == 0 and B > 0:
         raise SpecVerifyError("invalid sizes")
-    ws = workspace if workspace is not None else _workspace(need, dev, stream)
+    ws = _ws(workspace, need, dev, stream)
     rc = lib.spec_verify_greedy(_ptr(x), _dtype_code(x), stride, _ptr(d), B, K, V,
                                 _ptr(out["tokens"]), _ptr(out["num_accepted"]),
                                 _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
-                                _ptr(ws), ws.numel(), ctypes.c_void_p(stream))
+                                _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out
 
 
 def spec_verify_sample(target_logits, draft_tokens, uniforms, draft_logits=None,
                        temperature=1.0, rule=RULE_EXACT, tau=0.0, top_k=0, alpha=1.0,
-                       workspace=None):
+                       workspace=None, out=None):
     """Stochastic chain verification (see include/spec_verify.h)."""
     lib = load_library()
     x, stride = _rows_view(target_logits, "target_logits")
@@ -215,23 +236,23 @@ def spec_verify_sample(target_logits, draft_tokens, uniforms, draft_logits=None,
             raise SpecVerifyError(f"draft_logits must be {(B, K, V)}")
     d = _i32(draft_tokens, "draft_tokens", (B, K), dev)
     u = _f32(uniforms, "uniforms", (B, R), dev)
-    out = _outputs(B, R, dev)
+    out = _outputs(B, R, dev, out=out)
     stream = torch.cuda.current_stream(dev).cuda_stream
     need = lib.spec_verify_sample_workspace_size(B, K, V, _dtype_code(x), int(y is not None))
-    ws = workspace if workspace is not None else _workspace(need, dev, stream)
+    ws = _ws(workspace, need, dev, stream)
     rc = lib.spec_verify_sample(_ptr(x), _dtype_code(x), stride, _ptr(y), dstride, _ptr(d),
                                 B, K, V, float(temperature), _ptr(u),
                                 _rule(rule, tau, top_k, alpha),
                                 _ptr(out["tokens"]), _ptr(out["num_accepted"]),
                                 _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
-                                _ptr(ws), ws.numel(), ctypes.c_void_p(stream))
+                                _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out
 
 
 def spec_verify_tree(target_logits, node_tokens, parents, max_depth, temperature=0.0,
                      uniforms=None, rule=RULE_EXACT, tau=0.0, top_k=0, alpha=1.0,
-                     workspace=None):
+                     workspace=None, out=None):
     """Tree verification (see include/spec_verify.h). temperature 0 = greedy."""
     lib = load_library()
     x, stride = _rows_view(target_logits, "target_logits")
@@ -243,17 +264,17 @@ def spec_verify_tree(target_logits, node_tokens, parents, max_depth, temperature
     if float(temperature) != 0.0:
         u = _f32(uniforms, "uniforms", (B, N), dev)
     W = int(max_depth) + 1
-    out = _outputs(B, W, dev, want_nodes=True)
+    out = _outputs(B, W, dev, want_nodes=True, out=out)
     stream = torch.cuda.current_stream(dev).cuda_stream
     need = lib.spec_verify_tree_workspace_size(B, N, V, _dtype_code(x))
     if need == 0 and B > 0:
         raise SpecVerifyError("invalid sizes")
-    ws = workspace if workspace is not None else _workspace(need, dev, stream)
+    ws = _ws(workspace, need, dev, stream)
     rc = lib.spec_verify_tree(_ptr(x), _dtype_code(x), stride, _ptr(tok), _ptr(par), B, N, V,
                               int(max_depth), float(temperature), _ptr(u),
                               _rule(rule, tau, top_k, alpha),
                               _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["num_accepted"]),
                               _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
-                              _ptr(ws), ws.numel(), ctypes.c_void_p(stream))
+                              _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out
