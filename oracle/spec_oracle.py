@@ -71,9 +71,9 @@ RULE_EXACT = 0
 RULE_RELAXED = 1
 RULE_POWER = 2
 
-# A decision whose margin is below this is a near tie: the GPU may take the
-# other branch through fp32 rounding (|u - a| < 1e-5 or a CDF boundary within
-# 1e-5 * S of u * S).
+# An accept test with |u - a| < 1e-5 (or |p - tau| < 1e-5) is a near tie: an
+# fp32 implementation may take the other branch there. For the final draw the
+# same band around u * S gives the range of tokens that rounding can select.
 NEAR_TIE = 1e-5
 
 
@@ -132,21 +132,27 @@ def induced_from_dists(p, q):
     return accepted + rejection_mass * res
 
 
-def inverse_cdf(w, u):
+def inverse_cdf(w, u, band=NEAR_TIE):
     """Smallest j with C_j > u * S (C the inclusive prefix sum of w in index
-    order, S = C[-1]); falls back to the last positive index. Also returns the
-    relative distance from u * S to the chosen cell's nearer boundary."""
-    c = np.cumsum(np.asarray(w, dtype=np.float64))
+    order, S = C[-1]); falls back to the last positive index.
+
+    Also returns the relative distance from u * S to the chosen cell's nearer
+    boundary, and the index range [j_lo, j_hi] of the cells that meet the
+    band u * S +- band * S: a draw computed with a slightly different rounding
+    of the prefix sums lands in that range."""
+    w = np.asarray(w, dtype=np.float64)
+    c = np.cumsum(w)
     s = c[-1]
     thr = u * s
-    hits = np.nonzero(c > thr)[0]
-    if hits.size:
-        j = int(hits[0])
-    else:
-        j = int(np.nonzero(w > 0)[0][-1])
+
+    def first_above(t):
+        hits = np.nonzero(c > t)[0]
+        return int(hits[0]) if hits.size else int(np.nonzero(w > 0)[0][-1])
+
+    j = first_above(thr)
     lo = c[j - 1] if j > 0 else 0.0
     margin = min(abs(thr - lo), abs(c[j] - thr)) / s
-    return j, margin
+    return j, margin, first_above(thr - band * s), first_above(thr + band * s)
 
 
 def _acceptance_vs_rest(rule, p_t, rest, rank, tau, top_k, alpha):
@@ -191,7 +197,8 @@ def _empty_outputs(B, width):
                 logprob=np.zeros((B, width), dtype=np.float64),
                 mu=np.zeros((B, width), dtype=np.float64),
                 status=np.zeros(B, dtype=np.int64),
-                tie_pos=np.full(B, -1, dtype=np.int64))
+                tie_pos=np.full(B, -1, dtype=np.int64),
+                draw_band=np.full((B, 2), -1, dtype=np.int64))
 
 
 # ------------------------------------------------------------- greedy chain
@@ -243,8 +250,9 @@ def verify_sample(target_logits, draft_logits, draft_tokens, temperature,
 
     target_logits [B, K+1, V]; draft_logits [B, K, V] or None (deterministic
     drafts, q = one-hot); draft_tokens [B, K]; uniforms [B, K+1] in [0, 1).
-    Returns tokens / logprob / mu [B, K+1], num_accepted [B], status [B] and
-    tie_pos [B] (first emitted position decided by a near tie, else -1).
+    Returns tokens / logprob / mu [B, K+1], num_accepted [B], status [B],
+    tie_pos [B] (first position whose accept test was a near tie, else -1)
+    and draw_band [B, 2] (tokens the final draw may take under rounding).
     """
     x = np.asarray(target_logits, dtype=np.float64)
     y = None if draft_logits is None else np.asarray(draft_logits, dtype=np.float64)
@@ -327,9 +335,8 @@ def verify_sample(target_logits, draft_logits, draft_tokens, temperature,
             final_w = target_probs(x[b, K], T)
             final_mu = None
             final_scale = 1.0
-        j, cdf_margin = inverse_cdf(final_w, u[b, K])
-        if cdf_margin < NEAR_TIE and tie < 0:
-            tie = n
+        j, _, j_lo, j_hi = inverse_cdf(final_w, u[b, K])
+        out["draw_band"][b] = (j_lo, j_hi)
         p_row = target_probs(x[b, n], T)
         out["tokens"][b, n] = j
         out["logprob"][b, n] = np.log(p_row[j])
@@ -462,9 +469,8 @@ def verify_tree(target_logits, node_tokens, parents, max_depth, temperature,
                 w[rejected] = 0.0
             if not w.sum() > 0.0:
                 w = p.copy()
-            j, cdf_margin = inverse_cdf(w, u[b, 0])
-            if cdf_margin < NEAR_TIE and tie < 0:
-                tie = depth
+            j, _, j_lo, j_hi = inverse_cdf(w, u[b, 0])
+            out["draw_band"][b] = (j_lo, j_hi)
             out["tokens"][b, depth] = j
             out["logprob"][b, depth] = np.log(p[j])
             out["mu"][b, depth] = prod * w[j] / w.sum()

@@ -2,10 +2,12 @@
 
 Rules (fixed by the verification contract):
   * greedy outputs (tokens, num_accepted, nodes, status) are bit-exact;
-  * stochastic outputs are exact except from the first position the oracle
-    marks as a near tie (|u - a| < 1e-5, |p - tau| < 1e-5, or u*S within
-    1e-5*S of a CDF boundary); such requests are compared up to that
-    position and counted;
+  * stochastic outputs are exact except from the first position whose accept
+    test the oracle marks as a near tie (|u - a| < 1e-5 or |p - tau| < 1e-5);
+    such requests are compared up to that position and counted;
+  * the round's final draw (residual / bonus) must equal the oracle's token,
+    or, when u*S lies within 1e-5*S of a CDF boundary, be one of the tokens
+    whose cells meet that band (oracle draw_band); those are counted too;
   * log-probs and mu agree to 1e-4 absolute.
 """
 
@@ -38,12 +40,22 @@ def compare(got, ref, stochastic=False, keys_exact=("tokens",), check_status=Tru
     st_g = host(got["status"]).astype(np.int64)
     nodes_g = host(got["nodes"]).astype(np.int64) if ("nodes" in got and "nodes" in ref) else None
     exempt = 0
+    tok_g = tok_g.copy()
+    lp_g, mu_g = lp_g.copy(), mu_g.copy()
     for b in range(B):
         tie = int(ref["tie_pos"][b]) if stochastic else -1
         cut = W if tie < 0 else tie
         if tie >= 0:
             exempt += 1
         msg = f"request {b} (tie_pos {tie})"
+        if stochastic and tie < 0:
+            pos = int(ref["num_accepted"][b])
+            lo, hi = (int(v) for v in ref["draw_band"][b])
+            if tok_g[b, pos] != tok_r[b, pos] and lo <= tok_g[b, pos] <= hi and lo < hi:
+                # a boundary draw: valid, compared as the oracle's token from here on
+                exempt += 1
+                tok_g[b, pos] = tok_r[b, pos]
+                lp_g[b, pos], mu_g[b, pos] = lp_r[b, pos], mu_r[b, pos]
         assert np.array_equal(tok_g[b, :cut], tok_r[b, :cut]), \
             f"{msg}: tokens {tok_g[b, :cut]} vs oracle {tok_r[b, :cut]}"
         assert np.allclose(lp_g[b, :cut], lp_r[b, :cut], atol=ATOL, rtol=0), \

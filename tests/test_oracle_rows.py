@@ -132,7 +132,7 @@ def test_inverse_cdf_has_law_w_over_sum():
             w[-1] = 0.5
         counts = np.zeros(V)
         for u in us:
-            j, _ = O.inverse_cdf(w, u)
+            j = O.inverse_cdf(w, u)[0]
             counts[j] += 1
         assert np.all(np.abs(counts / M - w / w.sum()) <= 1.0 / M + 1e-12)
         assert counts[w == 0].sum() == 0
@@ -143,6 +143,12 @@ def test_inverse_cdf_edges_and_margin():
     assert O.inverse_cdf(w, 0.0)[0] == 1          # u = 0: first positive index
     assert O.inverse_cdf(w, 0.2499)[0] == 1
     assert O.inverse_cdf(w, 0.25)[0] == 3         # boundary goes to the next cell
-    j, margin = O.inverse_cdf(w, 0.5)
-    assert j == 3 and abs(margin - 0.25) < 1e-15
+    j, margin, lo, hi = O.inverse_cdf(w, 0.5)
+    assert j == 3 and abs(margin - 0.25) < 1e-15 and lo == hi == 3
     assert O.inverse_cdf(np.array([0.0, 2.0]), 1 - 2 ** -53)[0] == 1
+    # the band: cells within 1e-5 * S of u * S
+    w = np.array([0.5, 1e-6, 1e-6, 0.5 - 2e-6])
+    j, margin, lo, hi = O.inverse_cdf(w, 0.5 + 0.5e-6)
+    assert j == 1 and lo == 0 and hi == 3 and margin < 1e-5
+    j, margin, lo, hi = O.inverse_cdf(w, 0.25)
+    assert j == lo == hi == 0
