@@ -1,25 +1,31 @@
 // K2: per-request decisions, one CTA per request, launched as a programmatic
-// dependent of K1 (griddepcontrol.wait before reading K1's partials).
+// dependent of K1. Everything that depends only on the call's inputs (draft
+// tokens, uniforms, the draft tokens' logits, tree links and child lists) is
+// read before griddepcontrol.wait, overlapping K1's tail; only K1's row
+// statistics are read after it. (K2 can only launch once every K1 CTA has
+// passed its own wait on the kernel before the call, so those inputs are
+// complete.)
 //
 // chain_decide_kernel
-//   Greedy (mini-sglang PR #134, verify.py): row i's argmax is merged from its
-//   segment partials; n = first i < K whose draft is out of range or differs
-//   from that argmax; tokens d_0..d_{n-1}, then argmax(row n).
+//   Greedy (mini-sglang PR #134, verify.py): n = first i < K whose draft is
+//   out of range or differs from argmax(row i); tokens d_0..d_{n-1}, then
+//   argmax(row n).
 //   Stochastic (spec-decode README, "How it works"; nanospec README rules):
-//   per draft i, a_i = min(1, p(d_i)/q(d_i)) (exact, power ^alpha) or
-//   [p(d_i) >= tau] (relaxed); accepted iff u_i < a_i; n = first rejection.
-//   The row n draw (residual or bonus) is described for K3.
-//   Rows are taken NT at a time; the first rejection is a block-wide min, so
-//   long chains (K+1 = 4096) stop after the block that holds it.
+//   per draft i, a_i = min(1, p(d_i)/q(d_i)) (exact; power ^alpha) or
+//   [p(d_i) >= tau] (relaxed), computed in the log2 domain from the row
+//   log-sum-exps; accepted iff u_i < a_i; n = first rejection. Row n's draw
+//   (residual or bonus) is described for K3.
+//   Rows are taken kK2Threads at a time and the first rejection is a block
+//   min, so long chains (K+1 = 4096) stop after the block that holds it.
 //
 // tree_decide_kernel
-//   All N rows' statistics and every node's gathered logit (node token in its
-//   parent's row) are loaded into shared memory in parallel; one thread then
-//   walks from the root over children in increasing index (nanospec README,
-//   tree configuration), with rest / branch probabilities in double.
+//   All N rows' statistics and every node's gathered logit (its token in its
+//   parent's row) are staged in shared memory; one thread then walks from the
+//   root over children in increasing index (nanospec README, tree
+//   configuration), with rest / branch probabilities in double.
 #pragma once
 
-#include "sv_common.cuh"
+#include "row_stats.cuh"
 
 namespace sv {
 
@@ -40,9 +46,10 @@ struct ChainArgs {
   int64_t dft_stride;    // bytes
   const int32_t* drafts; // [B, K]
   const float* uniforms; // [B, K+1] (stochastic)
-  int32_t B, K, V, S;
-  const Partial* part_t; // [B*(K+1)*S]
-  const Partial* part_d; // [B*K*S]
+  int32_t B, K, V;
+  const Partial* part;   // K1 partials; target rows 0..B*(K+1)-1, then draft rows
+  int64_t T;             // K1's flattened element count
+  int32_t G;             // K1's CTA count
   float c;               // log2(e) / T (greedy: T = 1)
   int32_t greedy;
   RuleArgs rule;
@@ -57,15 +64,52 @@ struct ChainArgs {
   uint32_t* draw_counters;  // [B], zeroed here for K3's tickets
 };
 
+// Inputs of one chain position, readable before K1 completes.
+struct ChainIn {
+  int tok;
+  bool bad;
+  float u;   // uniform of the accept test (stochastic)
+  float x;   // target logit of the draft token (stochastic)
+  float y;   // draft logit of the draft token (stochastic, with draft logits)
+};
+
+template <int ES>
+__device__ __forceinline__ ChainIn load_chain_in(const ChainArgs& a, int b, int i) {
+  ChainIn in;
+  in.tok = -1;
+  in.bad = false;
+  in.u = 0.f;
+  in.x = -INFINITY;
+  in.y = -INFINITY;
+  const int R = a.K + 1;
+  if (i < a.K) {
+    in.tok = a.drafts[static_cast<int64_t>(b) * a.K + i];
+    in.bad = in.tok < 0 || in.tok >= a.V;
+    if (!a.greedy) {
+      in.u = a.uniforms[static_cast<int64_t>(b) * R + i];
+      if (!in.bad) {
+        in.x = Elem<ES>::load(a.tgt + (static_cast<int64_t>(b) * R + i) * a.tgt_stride, in.tok);
+        if (a.dft) in.y = Elem<ES>::load(a.dft + (static_cast<int64_t>(b) * a.K + i) * a.dft_stride, in.tok);
+      }
+    }
+  }
+  return in;
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArgs a) {
-  grid_dep_wait();
   __shared__ int s_first;
   __shared__ int s_status;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int K = a.K, R = a.K + 1;
   const float c = a.c;
+  const ChainIn pre = load_chain_in<ES>(a, b, tid < R ? tid : R);
+  const float u_final = a.greedy ? 0.f : a.uniforms[static_cast<int64_t>(b) * R + K];
+
+  grid_dep_wait();
+  grid_dep_launch();
+
   if (tid == 0) {
     s_status = 0;
     if (a.draw_counters) a.draw_counters[b] = 0;
@@ -79,36 +123,30 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     const int i = base + tid;
     const bool active = i < R;
     float m = -INFINITY, s = 0.f, lp2row = 0.f, lq2row = 0.f, lp2 = 0.f, acc = 0.f;
-    int idx = INT_MAX, err = 0, tok = -1, st = 0;
-    bool bad = false, zero = false, rej = false;
+    int idx = INT_MAX, err = 0, st = 0;
+    bool zero = false, rej = false;
+    const ChainIn in = (base == 0) ? pre : load_chain_in<ES>(a, b, active ? i : R);
     if (active) {
       const int64_t trow = static_cast<int64_t>(b) * R + i;
-      merge_partial_row(a.part_t + trow * a.S, a.S, c, m, s, idx, err);
+      merge_row(a.part, trow, a.V, a.T, a.G, c, m, s, idx, err);
       lp2row = m * c + log2f(s);
       if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= 4;   // NONFINITE_ROW
       if (err) st |= 32;                                                     // TIMEOUT
       if (i < K) {
-        tok = a.drafts[static_cast<int64_t>(b) * K + i];
-        bad = tok < 0 || tok >= a.V;
         if (a.greedy) {
-          rej = bad || tok != idx;
+          rej = in.bad || in.tok != idx;
         } else {
-          float lq2 = 0.f;
-          if (!bad) {
-            const float x = Elem<ES>::load(a.tgt + trow * a.tgt_stride, tok);
-            lp2 = x * c - lp2row;  // log2 p(t)
-          }
+          if (!in.bad) lp2 = in.x * c - lp2row;   // log2 p(t)
           if (a.dft) {
-            const int64_t drow = static_cast<int64_t>(b) * K + i;
+            const int64_t drow = static_cast<int64_t>(a.B) * R + static_cast<int64_t>(b) * K + i;
             float md, sd;
             int id, ed;
-            merge_partial_row(a.part_d + drow * a.S, a.S, c, md, sd, id, ed);
+            merge_row(a.part, drow, a.V, a.T, a.G, c, md, sd, id, ed);
             lq2row = md * c + log2f(sd);
             if (!(fabsf(md) <= FLT_MAX) || !(sd > 0.f && sd <= FLT_MAX)) st |= 4;
             if (ed) st |= 32;
-            if (!bad) {
-              const float y = Elem<ES>::load(a.dft + drow * a.dft_stride, tok);
-              lq2 = y * c - lq2row;
+            if (!in.bad) {
+              const float lq2 = in.y * c - lq2row;
               if (lp2 == -INFINITY && lq2 == -INFINITY) {
                 zero = true;
               } else {
@@ -118,14 +156,13 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
                 else acc = ex2(r2);
               }
             }
-          } else if (!bad) {   // deterministic draft, rest_1 = 1
+          } else if (!in.bad) {   // deterministic draft, rest_1 = 1
             const float r2 = fminf(0.f, lp2);
             if (a.rule.rule == 1) acc = (ex2(lp2) >= a.rule.tau) ? 1.f : 0.f;
             else if (a.rule.rule == 2) acc = ex2(a.rule.alpha * r2);
             else acc = ex2(r2);
           }
-          const float u = a.uniforms[static_cast<int64_t>(b) * R + i];
-          rej = bad || zero || !(u < acc);
+          rej = in.bad || zero || !(in.u < acc);
         }
       }
       if (rej) atomicMin(&s_first, i);
@@ -139,7 +176,7 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
       if (i <= nb) {
         int stat = st;
         if (i == nb && i < K) {
-          if (bad) stat |= 1;
+          if (in.bad) stat |= 1;
           if (zero) stat |= 8;
         }
         if (stat) atomicOr(&s_status, stat);
@@ -147,13 +184,9 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
       if (a.greedy) {
         int out_tok = -1;
         float lp = 0.f, mu = 0.f;
-        if (i < nb) {
-          out_tok = tok;
-          lp = -log2f(s) * kLn2;   // the draft is the argmax, so x[tok] = m
-          mu = 1.f;
-        } else if (i == nb) {
-          out_tok = idx;
-          lp = -log2f(s) * kLn2;
+        if (i <= nb) {
+          out_tok = (i < nb) ? in.tok : idx;
+          lp = -log2f(s) * kLn2;   // emitted tokens are argmaxes, so x[tok] = m
           mu = 1.f;
         }
         a.out_tokens[o] = out_tok;
@@ -161,13 +194,13 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
         if (a.out_mu) a.out_mu[o] = mu;
       } else {
         if (i < nb) {
-          a.out_tokens[o] = tok;
+          a.out_tokens[o] = in.tok;
           if (a.out_logprob) a.out_logprob[o] = lp2 * kLn2;
           if (a.out_mu) a.out_mu[o] = a.dft ? ex2(lp2) : acc;
         } else if (i == nb) {
           DrawDesc d;
           d.pos = i;
-          d.u = a.uniforms[static_cast<int64_t>(b) * R + K];
+          d.u = u_final;
           d.t_row = static_cast<int32_t>(static_cast<int64_t>(b) * R + i);
           d.d_row = static_cast<int32_t>(static_cast<int64_t>(b) * K + i);
           d.lp2 = lp2row;
@@ -182,8 +215,8 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
           } else {
             d.type = kDrawMaskedP;
             d.scale = 1.f - acc;
-            if (!bad) {
-              a.excl[static_cast<int64_t>(b) * a.excl_stride] = tok;
+            if (!in.bad) {
+              a.excl[static_cast<int64_t>(b) * a.excl_stride] = in.tok;
               d.n_excl = 1;
             }
           }
@@ -213,7 +246,6 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     a.out_num[b] = n;
     if (a.out_status) a.out_status[b] = s_status;
   }
-  grid_dep_launch();
 }
 
 struct TreeArgs {
@@ -222,8 +254,10 @@ struct TreeArgs {
   const int32_t* tokens;   // [B, N]
   const int32_t* parents;  // [B, N]
   const float* uniforms;   // [B, N] (stochastic)
-  int32_t B, N, V, S, max_depth;
-  const Partial* part;     // [B*N*S]
+  int32_t B, N, V, max_depth;
+  const Partial* part;     // K1 partials of the B*N rows
+  int64_t T;
+  int32_t G;
   float c;                 // log2(e) / T (greedy: T = 1)
   int32_t greedy;
   RuleArgs rule;
@@ -241,10 +275,10 @@ struct TreeArgs {
 
 template <int ES>
 __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs a) {
-  grid_dep_wait();
   __shared__ float sm_m[kMaxTreeNodes];     // row max
   __shared__ float sm_l2[kMaxTreeNodes];    // row lse, log2 domain
   __shared__ float sm_g[kMaxTreeNodes];     // node token's logit in its parent's row
+  __shared__ float sm_u[kMaxTreeNodes];     // node's uniform
   __shared__ int sm_am[kMaxTreeNodes];      // row argmax
   __shared__ int sm_tok[kMaxTreeNodes];
   __shared__ int sm_par[kMaxTreeNodes];     // -1 for the root and bad links
@@ -257,21 +291,12 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   const int tid = threadIdx.x;
   const int N = a.N, W = a.max_depth + 1;
   const float c = a.c;
-  if (tid == 0) {
-    s_status = 0;
-    if (a.draw_counters) a.draw_counters[b] = 0;
-  }
+
+  // Call inputs: links, tokens, uniforms and the gathered logits.
+  if (tid == 0) s_status = 0;
   __syncthreads();
   for (int n = tid; n < N; n += kK2Threads) {
     const int64_t row = static_cast<int64_t>(b) * N + n;
-    float m, s;
-    int idx, err;
-    merge_partial_row(a.part + row * a.S, a.S, c, m, s, idx, err);
-    sm_m[n] = m;
-    sm_l2[n] = m * c + log2f(s);
-    sm_am[n] = idx;
-    sm_bad[n] = static_cast<unsigned char>(((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? 4 : 0) |
-                                           (err ? 32 : 0));
     const int par = a.parents[row];
     const int tok = a.tokens[row];
     const bool link_ok = (n == 0) ? (par == -1) : (par >= 0 && par < n);
@@ -279,10 +304,11 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
     const int p = (n > 0 && link_ok) ? par : -1;
     sm_par[n] = p;
     sm_tok[n] = tok;
-    float g = -INFINITY;
+    sm_u[n] = a.greedy ? 0.f : a.uniforms[row];
+    float gl = -INFINITY;
     if (p >= 0 && tok >= 0 && tok < a.V)
-      g = Elem<ES>::load(a.tgt + (static_cast<int64_t>(b) * N + p) * a.tgt_stride, tok);
-    sm_g[n] = g;
+      gl = Elem<ES>::load(a.tgt + (static_cast<int64_t>(b) * N + p) * a.tgt_stride, tok);
+    sm_g[n] = gl;
     sm_first[n] = -1;
   }
   __syncthreads();
@@ -294,6 +320,24 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
         sm_first[p] = n;
       }
     }
+  }
+
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (tid == 0 && a.draw_counters) a.draw_counters[b] = 0;
+  for (int n = tid; n < N; n += kK2Threads) {
+    float m, s;
+    int idx, err;
+    merge_row(a.part, static_cast<int64_t>(b) * N + n, a.V, a.T, a.G, c, m, s, idx, err);
+    sm_m[n] = m;
+    sm_l2[n] = m * c + log2f(s);
+    sm_am[n] = idx;
+    sm_bad[n] = static_cast<unsigned char>(((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? 4 : 0) |
+                                           (err ? 32 : 0));
+  }
+  __syncthreads();
+  if (tid == 0) {
     int status = 0;
     int cur = 0, depth = 0;
     const int64_t ob = static_cast<int64_t>(b) * W;
@@ -353,8 +397,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
             rest -= p;
           }
         }
-        const double u = static_cast<double>(a.uniforms[static_cast<int64_t>(b) * N + kid]);
-        if (u < acc) {
+        if (static_cast<double>(sm_u[kid]) < acc) {
           accepted = kid;
           a.out_tokens[ob + depth] = t;
           if (a.out_logprob) a.out_logprob[ob + depth] = lp2 * kLn2;
@@ -374,7 +417,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
       d.t_row = static_cast<int32_t>(static_cast<int64_t>(b) * N + cur);
       d.d_row = 0;
       d.pos = depth;
-      d.u = a.uniforms[static_cast<int64_t>(b) * N];
+      d.u = sm_u[0];
       d.lp2 = sm_l2[cur];
       d.lq2 = 0.f;
       d.scale = static_cast<float>(reach);
@@ -394,7 +437,6 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   }
   __syncthreads();
   if (tid == 0 && a.out_status) a.out_status[b] = s_status;
-  grid_dep_launch();
 }
 
 }  // namespace sv

@@ -105,6 +105,7 @@ __device__ __forceinline__ bool is_excluded(int j, int nex, const int* s_ex, con
 template <int ES>
 __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   grid_dep_wait();
+  grid_dep_launch();
   __shared__ float red[kK3Threads / 32];
   __shared__ float scan_w[kK3Threads / 32];
   __shared__ int s_ex[kK3LocalExcl];

@@ -3,9 +3,11 @@
 // the launchers, and the kernel launches.
 //
 // One call is K1 (row statistics) -> K2 (decide) [-> K3 (draw)] on the
-// caller's stream. K2 and K3 are launched with programmatic stream
-// serialization, so their launch overlaps the tail of the kernel before them;
-// each waits (griddepcontrol.wait) before touching that kernel's results.
+// caller's stream. All three are launched with programmatic stream
+// serialization, so each one's launch overlaps the tail of the kernel before
+// it. K1 waits (griddepcontrol.wait) before reading anything, so the logits
+// may come from the kernel just before the call; K2 and K3 read only the
+// call's own inputs before their wait and the previous kernel's results after.
 
 #include <cmath>
 #include <cstdint>
@@ -31,18 +33,17 @@ int elem_size(int32_t dtype) {
 }
 
 struct Plan {
-  int32_t S = 0;            // K1 segments per row
-  int32_t seg_elems = 0;
+  int64_t rows_total = 0;
+  int64_t T = 0;            // rows_total * V, K1's flattened element count
   int32_t P = 0;            // K3 chunks per row
   int32_t chunk_elems = 0;
   int32_t excl_stride = 0;
-  int64_t rows_total = 0;
   size_t off_part = 0, off_draw = 0, off_excl = 0, off_k3part = 0, off_k3cnt = 0;
   size_t total = 0;
 };
 
 // Split a V-element row into n pieces of at most max_bytes, each a multiple
-// of 64 elements (so every piece starts at the row's 16-byte phase).
+// of 64 elements.
 void split_row(int64_t V, int es, int64_t max_bytes, int32_t* n_out, int32_t* elems_out) {
   int64_t n = (V * es + max_bytes - 1) / max_bytes;
   if (n < 1) n = 1;
@@ -53,20 +54,20 @@ void split_row(int64_t V, int es, int64_t max_bytes, int32_t* n_out, int32_t* el
   *elems_out = static_cast<int32_t>(e);
 }
 
+// Workspace layout; independent of the device (K1's partial array is sized
+// for the largest grid K1 may use, kK1MaxCtas).
 bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, bool draw,
                int64_t excl_stride, Plan* pl) {
   if (V < 1 || es == 0 || B < 0 || rows_t < 0 || rows_d < 0) return false;
-  split_row(V, es, kK1SegBytes, &pl->S, &pl->seg_elems);
   split_row(V, es, kK3ChunkBytes, &pl->P, &pl->chunk_elems);
   pl->rows_total = rows_t + rows_d;
   if (pl->rows_total > INT32_MAX / 2) return false;
-  const int64_t k1_ctas = pl->rows_total * pl->S;
-  if (k1_ctas >= INT32_MAX) return false;
+  pl->T = pl->rows_total * V;
   if (draw && B * pl->P >= INT32_MAX) return false;
   pl->excl_stride = static_cast<int32_t>(excl_stride < 1 ? 1 : excl_stride);
   size_t off = 0;
   pl->off_part = off;
-  off += align_up(static_cast<size_t>(k1_ctas) * sizeof(Partial), kAlign);
+  off += align_up(static_cast<size_t>(pl->rows_total + kK1MaxCtas) * kK1Consumers * sizeof(Partial), kAlign);
   if (draw) {
     pl->off_draw = off;
     off += align_up(static_cast<size_t>(B) * sizeof(DrawDesc), kAlign);
@@ -79,6 +80,24 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
   }
   pl->total = off < kAlign ? kAlign : off;
   return true;
+}
+
+// K1 grid for this device: kK1CtasPerSm per SM, fewer for small problems.
+int k1_grid(int64_t T, int es) {
+  static int sm_count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    sm_count[dev] = n;
+  }
+  int64_t g = static_cast<int64_t>(sm_count[dev]) * kK1CtasPerSm;
+  const int64_t by_size = (T * es + kK1MinBytesPerCta - 1) / kK1MinBytesPerCta;
+  if (by_size < g) g = by_size;
+  if (g > kK1MaxCtas) g = kK1MaxCtas;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -124,23 +143,38 @@ cudaError_t launch(Kern kernel, int grid, int block, size_t smem, cudaStream_t s
 }
 
 template <int ES>
-cudaError_t launch_row_stats(const RowStatsArgs& a, int64_t ctas, cudaStream_t stream) {
-  return launch(row_stats_kernel<ES>, static_cast<int>(ctas), kK1Threads, kK1SegBytes, stream, false, a);
+cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(row_stats_kernel<ES>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kK1SmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return launch(row_stats_kernel<ES>, a.G, kK1Threads, kK1SmemBytes, stream, true, a);
 }
 
-RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride_b, int64_t rows_t,
-                            const void* dft, int64_t dft_stride_b, int64_t rows_d, int32_t V,
+RowSet row_set(const void* base, int64_t stride_elems, int64_t rows, int64_t V, int es) {
+  RowSet r;
+  r.base = static_cast<const uint8_t*>(base);
+  r.stride_bytes = stride_elems * es;
+  r.rows = static_cast<int32_t>(rows);
+  r.safe_lo = reinterpret_cast<uintptr_t>(base);
+  r.safe_hi = rows > 0 ? r.safe_lo + static_cast<uintptr_t>(((rows - 1) * stride_elems + V) * es) : r.safe_lo;
+  return r;
+}
+
+RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride, int64_t rows_t,
+                            const void* dft, int64_t dft_stride, int64_t rows_d, int32_t V, int es,
                             float c, void* ws) {
   RowStatsArgs r;
-  r.set0.base = static_cast<const uint8_t*>(tgt);
-  r.set0.stride_bytes = tgt_stride_b;
-  r.set0.rows = static_cast<int32_t>(rows_t);
-  r.set1.base = static_cast<const uint8_t*>(dft);
-  r.set1.stride_bytes = dft_stride_b;
-  r.set1.rows = static_cast<int32_t>(rows_d);
+  r.set0 = row_set(tgt, tgt_stride, rows_t, V, es);
+  r.set1 = row_set(dft, dft_stride, rows_d, V, es);
   r.V = V;
-  r.S = pl.S;
-  r.seg_elems = pl.seg_elems;
+  r.T = pl.T;
+  r.G = k1_grid(pl.T, es);
   r.c = c;
   r.partials = reinterpret_cast<Partial*>(static_cast<uint8_t*>(ws) + pl.off_part);
   return r;
@@ -238,8 +272,8 @@ sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t r
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = kLog2e;
-  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride * es, rows, nullptr, 0, 0, V, c, workspace);
-  cudaError_t e = es == 2 ? launch_row_stats<2>(r, rows * pl.S, st) : launch_row_stats<4>(r, rows * pl.S, st);
+  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride, rows, nullptr, 0, 0, V, es, c, workspace);
+  cudaError_t e = es == 2 ? launch_row_stats<2>(r, st) : launch_row_stats<4>(r, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   ChainArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -249,8 +283,9 @@ sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t r
   a.B = B;
   a.K = K;
   a.V = V;
-  a.S = pl.S;
-  a.part_t = r.partials;
+  a.part = r.partials;
+  a.T = r.T;
+  a.G = r.G;
   a.c = c;
   a.greedy = 1;
   a.out_tokens = out_tokens;
@@ -293,10 +328,9 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = kLog2e / temperature;
-  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride * es, rows_t, draft_logits,
-                                        draft_row_stride * es, rows_d, V, c, workspace);
-  const int64_t ctas = (rows_t + rows_d) * pl.S;
-  cudaError_t e = es == 2 ? launch_row_stats<2>(r, ctas, st) : launch_row_stats<4>(r, ctas, st);
+  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride, rows_t, draft_logits,
+                                        draft_row_stride, rows_d, V, es, c, workspace);
+  cudaError_t e = es == 2 ? launch_row_stats<2>(r, st) : launch_row_stats<4>(r, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   ChainArgs a;
@@ -310,9 +344,9 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   a.B = B;
   a.K = K;
   a.V = V;
-  a.S = pl.S;
-  a.part_t = r.partials;
-  a.part_d = r.partials + rows_t * pl.S;
+  a.part = r.partials;
+  a.T = r.T;
+  a.G = r.G;
   a.c = c;
   a.greedy = 0;
   a.rule = rule_args(rule);
@@ -369,8 +403,8 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = greedy ? kLog2e : kLog2e / temperature;
-  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride * es, rows, nullptr, 0, 0, V, c, workspace);
-  cudaError_t e = es == 2 ? launch_row_stats<2>(r, rows * pl.S, st) : launch_row_stats<4>(r, rows * pl.S, st);
+  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride, rows, nullptr, 0, 0, V, es, c, workspace);
+  cudaError_t e = es == 2 ? launch_row_stats<2>(r, st) : launch_row_stats<4>(r, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   TreeArgs a;
@@ -383,9 +417,10 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
   a.B = B;
   a.N = N;
   a.V = V;
-  a.S = pl.S;
   a.max_depth = max_depth;
   a.part = r.partials;
+  a.T = r.T;
+  a.G = r.G;
   a.c = c;
   a.greedy = greedy ? 1 : 0;
   a.rule = rule_args(rule);

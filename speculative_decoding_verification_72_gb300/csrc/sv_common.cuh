@@ -75,6 +75,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -117,6 +121,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------ programmatic dependent launch
@@ -185,31 +194,6 @@ __device__ __forceinline__ void merge_stats(float& m, float& s, int& i, float m2
   } else if (m2 != -INFINITY) {
     s += s2 * ex2((m2 - m) * c);
   }
-}
-
-__device__ __forceinline__ void merge_partial_row(const Partial* __restrict__ p, int S, float c,
-                                                  float& m, float& s, int& idx, int& err) {
-  m = -INFINITY;
-  s = 0.f;
-  idx = INT_MAX;
-  err = 0;
-  int k = 0;
-  for (; k + 4 <= S; k += 4) {
-    Partial v[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) v[t] = p[k + t];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      merge_stats(m, s, idx, v[t].m, v[t].s, v[t].idx, c);
-      err |= v[t].err;
-    }
-  }
-  for (; k < S; ++k) {
-    const Partial v = p[k];
-    merge_stats(m, s, idx, v.m, v.s, v.idx, c);
-    err |= v.err;
-  }
-  if (m == -INFINITY) idx = 0;   // every element is -inf: the lowest index attains the max
 }
 
 }  // namespace sv
