@@ -6,10 +6,10 @@
 // flattened element space of T = rows * V elements; CTA g owns the elements
 // [T g / G, T (g+1) / G), so every CTA streams the same number of bytes
 // whatever the row count. Warp 0 is the producer: one lane walks the CTA's
-// row pieces and issues 1-D bulk copies (TMA) of up to 16 KB into a 6-stage
+// row pieces and issues 1-D bulk copies (TMA) of up to 28 KB into a 3-stage
 // shared-memory ring, arming each stage's "full" mbarrier with the byte count
 // and reusing a stage once all consumer warps have released it on its
-// "empty" mbarrier. Warps 1..8 consume: each thread folds its group of 16-byte
+// "empty" mbarrier. Warps 1..7 consume: each thread folds its 16-byte
 // vectors of each stage into a running (max, sum 2^((x - max) c)) and
 // remembers the group holding its first maximum. At the end of every row
 // piece the consumers resolve the exact argmax, reduce (shuffles, then a
@@ -30,18 +30,24 @@
 
 namespace sv {
 
-constexpr int kK1Consumers = 8;                       // consumer warps
+constexpr int kK1Consumers = 7;                       // consumer warps
 constexpr int kK1Threads = 32 * (kK1Consumers + 1);   // + one producer warp
 constexpr int kK1ConsumerThreads = 32 * kK1Consumers;
-constexpr int kK1StageBytes = 16384;
-constexpr int kK1Stages = 6;
-constexpr int kK1SmemBytes = kK1StageBytes * kK1Stages;
 constexpr int kK1CtasPerSm = 2;
+// Each of an SM's four schedulers holds a quarter of the 64K registers and
+// its share of the resident warps: with 2 CTAs of 8 warps every scheduler
+// gets 4 warps, which leaves 128 registers per thread.
+constexpr int kK1WarpsPerScheduler = (kK1CtasPerSm * (kK1Consumers + 1) + 3) / 4;
+constexpr int kK1MaxRegs = (16384 / (kK1WarpsPerScheduler * 32)) / 8 * 8;
+// Vectors one consumer thread folds per stage, in halves of kGroupVecs.
+constexpr int kStageVecs = 8;
+constexpr int kGroupVecs = 4;
+constexpr int kK1StageBytes = kK1ConsumerThreads * kStageVecs * 16;   // 28 KB
+constexpr int kK1Stages = 3;
+constexpr int kK1SmemBytes = kK1StageBytes * kK1Stages;
 constexpr int kK1MaxCtas = 4096;                      // bound used to size the workspace
 constexpr int kK1MinBytesPerCta = 16384;
-// Vectors one consumer thread folds per stage.
-constexpr int kGroupVecs = kK1StageBytes / 16 / kK1ConsumerThreads;
-static_assert(kGroupVecs == 4, "fold_group assumes four vectors per thread and stage");
+static_assert(kStageVecs == 2 * kGroupVecs, "a stage is folded as two groups per thread");
 
 struct RowSet {
   const uint8_t* base;   // first row
@@ -123,11 +129,12 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }
 
 // Where a thread's running maximum first appeared: a scalar element (base == 0,
-// exact index j) or a stage group (re-read at the end of the piece).
+// exact index j) or one of its groups (re-read at the end of the piece).
 struct GroupCand {
   uintptr_t base;   // global address of the stage's first copied byte, or 0
   int jbase;        // row index of the stage's first element
   int nvec;         // vectors in the stage
+  int k0;           // the group's first vector slot k (vector ct + k * kK1ConsumerThreads)
   int j;            // exact index of a scalar candidate
 };
 
@@ -145,80 +152,172 @@ __device__ __forceinline__ void fold_scalar(float x, int j, float c, float& m, f
   if (x > -INFINITY) s += ex2(fmaf(x, c, -mc));
 }
 
-// Fold one thread's unpacked group of a stage into (m, s): at most one
-// rescale per group; the argmax keeps only the group where the maximum first
-// rose (groups arrive in increasing index order, so a strict '>' keeps the
-// lowest index).
-template <int N>
-__device__ __forceinline__ void fold_values(const float (&f)[kGroupVecs][N], int jbase, int nvec,
-                                            uintptr_t gbase, float c, float& m, float& mc, float& s,
-                                            GroupCand& cand) {
-  float gm[kGroupVecs];
+// A group is 16 32-bit words (kGroupVecs vectors): 16 fp32 elements, or 32
+// bf16 elements packed two per word (low half first).
+constexpr int kGroupWords = kGroupVecs * 4;
+
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+template <int ES>
+__device__ __forceinline__ float group_max(const uint32_t (&w)[kGroupWords]) {
+  if constexpr (ES == 2) {
+    uint32_t a[8];
 #pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k) {
-    if constexpr (N == 8)
-      gm[k] = fmaxf(max3f(f[k][0], f[k][1], f[k][2]),
-                    max3f(max3f(f[k][3], f[k][4], f[k][5]), f[k][6], f[k][7]));
-    else
-      gm[k] = max3f(f[k][0], f[k][1], fmaxf(f[k][2], f[k][3]));
+    for (int i = 0; i < 8; ++i) a[i] = max_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = max_bf16x2(a[2 * i], a[2 * i + 1]);
+    a[0] = max_bf16x2(a[0], a[1]);
+    a[2] = max_bf16x2(a[2], a[3]);
+    a[0] = max_bf16x2(a[0], a[2]);
+    return fmaxf(__uint_as_float(a[0] << 16), __uint_as_float(a[0] & 0xffff0000u));
+  } else {
+    float t[6];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+      t[i] = max3f(__uint_as_float(w[3 * i]), __uint_as_float(w[3 * i + 1]), __uint_as_float(w[3 * i + 2]));
+    t[5] = __uint_as_float(w[15]);
+    return fmaxf(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]));
   }
-  const float gmax = fmaxf(max3f(gm[0], gm[1], gm[2]), gm[3]);
+}
+
+// sum over the group of 2^(x c - mc), with packed fp32x2 FMA / add.
+template <int ES>
+__device__ __forceinline__ float group_sum(const uint32_t (&w)[kGroupWords], float c, float mc) {
+  const float2 c2 = make_float2(c, c);
+  const float2 nmc2 = make_float2(-mc, -mc);
+  float2 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+  constexpr int kPairs = ES == 2 ? kGroupWords : kGroupWords / 2;
+#pragma unroll
+  for (int k = 0; k < kPairs; ++k) {
+    float2 x;
+    if constexpr (ES == 2) {
+      x = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+    } else {
+      x = make_float2(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1]));
+    }
+    const float2 t = __ffma2_rn(x, c2, nmc2);
+    acc[k & 3] = __fadd2_rn(acc[k & 3], make_float2(ex2(t.x), ex2(t.y)));
+  }
+  const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 a = __fadd2_rn(a01, a23);
+  return a.x + a.y;
+}
+
+// Fold one group into (m, s). After a piece's first group the exponentials
+// use the running maximum from before the group, so they do not wait on the
+// group's own maximum; when the maximum rises the running sum is rescaled
+// once (and the group re-summed against the new maximum only if it rose by so
+// much that the old reference could overflow). The argmax keeps only the
+// group where the maximum first rose: groups arrive in increasing index
+// order, so a strict '>' keeps the lowest index.
+template <int ES>
+__device__ __forceinline__ void fold_words(const uint32_t (&w)[kGroupWords], int jbase, int nvec,
+                                           int k0, uintptr_t gbase, float c, float& m, float& mc,
+                                           float& s, GroupCand& cand) {
+  if (m == -INFINITY) {
+    const float gmax = group_max<ES>(w);
+    if (gmax > -INFINITY) {
+      mc = gmax * c;
+      s = group_sum<ES>(w, c, mc);
+      m = gmax;
+      cand.base = gbase;
+      cand.jbase = jbase;
+      cand.nvec = nvec;
+      cand.k0 = k0;
+    }
+    return;
+  }
+  const float gsum = group_sum<ES>(w, c, mc);
+  const float gmax = group_max<ES>(w);
   if (gmax > m) {
-    s = (m == -INFINITY) ? 0.f : s * ex2((m - gmax) * c);
+    const float d = (m - gmax) * c;
+    if (d > -100.f && gsum <= FLT_MAX) {
+      s = (s + gsum) * ex2(d);
+    } else {
+      s = s * ex2(d) + group_sum<ES>(w, c, gmax * c);
+    }
     m = gmax;
     mc = gmax * c;
     cand.base = gbase;
     cand.jbase = jbase;
     cand.nvec = nvec;
-  }
-  if (gmax > -INFINITY) {
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < kGroupVecs; ++k) {
-#pragma unroll
-      for (int e = 0; e < N; e += 2) {
-        acc0 += ex2(fmaf(f[k][e], c, -mc));
-        acc1 += ex2(fmaf(f[k][e + 1], c, -mc));
-      }
-    }
-    s += acc0 + acc1;
+    cand.k0 = k0;
+  } else {
+    s += gsum;
   }
 }
 
-// A full interior stage: four vectors per thread, no masking.
+// A full interior stage: kStageVecs vectors per thread, folded as two groups,
+// no masking.
 template <int ES>
 __device__ __forceinline__ void fold_stage_full(const uint4* sv4, int ct, int jbase, uintptr_t gbase,
                                                 float c, float& m, float& mc, float& s, GroupCand& cand) {
-  constexpr int N = Elem<ES>::kVec;
-  float f[kGroupVecs][N];
 #pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k) Elem<ES>::unpack(sv4[ct + k * kK1ConsumerThreads], f[k]);
-  fold_values<N>(f, jbase, kGroupVecs * kK1ConsumerThreads, gbase, c, m, mc, s, cand);
+  for (int h = 0; h < kStageVecs / kGroupVecs; ++h) {
+    uint32_t w[kGroupWords];
+#pragma unroll
+    for (int k = 0; k < kGroupVecs; ++k) {
+      const uint4 v = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
+      w[4 * k] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+    fold_words<ES>(w, jbase, kStageVecs * kK1ConsumerThreads, h * kGroupVecs, gbase, c, m, mc, s, cand);
+  }
 }
 
-// A short stage, or one holding bytes outside the piece: guarded loads and
-// masking. Kept out of line so the full-stage path stays free of them.
+// A stage with fewer than kStageVecs vectors per thread, or whose first or
+// last vector holds bytes outside the piece (the 16-byte hull adds at most
+// 15 bytes at each end, so only vector 0 of the first stage and vector
+// nvec - 1 of the last can). Missing vectors read as -inf; only those two
+// vectors are masked element by element.
 template <int ES>
-__device__ __noinline__ void fold_stage_edge(const uint4* sv4, int nvec, int ct, int jbase, int j0,
-                                             int j1, uintptr_t gbase, float c, float& m, float& mc,
-                                             float& s, GroupCand& cand) {
+__device__ __forceinline__ void fold_stage_edge(const uint4* sv4, int nvec, int ct, int jbase, int j0,
+                                                int j1, int mask_lo_v, int mask_hi_v, uintptr_t gbase,
+                                                float c, float& m, float& mc, float& s, GroupCand& cand) {
   constexpr int N = Elem<ES>::kVec;
-  float f[kGroupVecs][N];
+  // -inf in every element of a word
+  constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k) {
-    const int v = ct + k * kK1ConsumerThreads;
-    if (v < nvec) {
-      Elem<ES>::unpack(sv4[v], f[k]);
-    } else {
+  for (int h = 0; h < kStageVecs / kGroupVecs; ++h) {
+    uint32_t w[kGroupWords];
 #pragma unroll
-      for (int e = 0; e < N; ++e) f[k][e] = -INFINITY;
+    for (int k = 0; k < kGroupVecs; ++k) {
+      const int v = ct + (h * kGroupVecs + k) * kK1ConsumerThreads;
+      uint4 q = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
+      if (v < nvec) q = sv4[v];
+      if (v == mask_lo_v || v == mask_hi_v) {
+        uint32_t word[4] = {q.x, q.y, q.z, q.w};
+        const int jv = jbase + v * N;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          if (jv + e < j0 || jv + e >= j1) {
+            if constexpr (ES == 2) {
+              const int wi = e >> 1;
+              word[wi] = (e & 1) ? ((word[wi] & 0x0000ffffu) | 0xff800000u)
+                                 : ((word[wi] & 0xffff0000u) | 0x0000ff80u);
+            } else {
+              word[e] = kNegInfWord;
+            }
+          }
+        }
+        q = make_uint4(word[0], word[1], word[2], word[3]);
+      }
+      w[4 * k] = q.x;
+      w[4 * k + 1] = q.y;
+      w[4 * k + 2] = q.z;
+      w[4 * k + 3] = q.w;
     }
-    const int jv = jbase + v * N;
-#pragma unroll
-    for (int e = 0; e < N; ++e)
-      if (jv + e < j0 || jv + e >= j1) f[k][e] = -INFINITY;
+    fold_words<ES>(w, jbase, nvec, h * kGroupVecs, gbase, c, m, mc, s, cand);
   }
-  fold_values<N>(f, jbase, nvec, gbase, c, m, mc, s, cand);
 }
 
 // Lowest index in [j0, j1) of the remembered candidate holding the value m,
@@ -230,7 +329,7 @@ __device__ __forceinline__ int resolve_cand(const GroupCand& cand, int ct, float
   constexpr int N = Elem<ES>::kVec;
 #pragma unroll
   for (int k = 0; k < kGroupVecs; ++k) {
-    const int v = ct + k * kK1ConsumerThreads;
+    const int v = ct + (cand.k0 + k) * kK1ConsumerThreads;
     if (v < cand.nvec) {
       const uint4 w = __ldg(reinterpret_cast<const uint4*>(cand.base) + v);
       float f[N];
@@ -245,7 +344,7 @@ __device__ __forceinline__ int resolve_cand(const GroupCand& cand, int ct, float
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kK1Threads, kK1CtasPerSm) row_stats_kernel(const RowStatsArgs a) {
+__global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full_bar[kK1Stages];
   __shared__ __align__(8) uint64_t empty_bar[kK1Stages];
@@ -277,14 +376,14 @@ __global__ void __launch_bounds__(kK1Threads, kK1CtasPerSm) row_stats_kernel(con
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int st = 0;
+      int st = 0, slot = 0;
+      uint32_t phase = 0;   // parity of the current use of `slot`
       bool ok = true;
       for (int64_t e = E0; e < E1 && ok;) {
         const Piece p = make_piece<ES>(a, e, E1);
         for (int s = 0; s < p.nst; ++s, ++st) {
-          const int slot = st % kK1Stages;
-          const int use = st / kK1Stages;
-          if (use > 0 && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), (use - 1) & 1)) {
+          // the slot's previous use (parity phase ^ 1) must have been released
+          if (st >= kK1Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) {
             ok = false;
             break;
           }
@@ -295,6 +394,10 @@ __global__ void __launch_bounds__(kK1Threads, kK1CtasPerSm) row_stats_kernel(con
           mbar_arrive_expect_tx(fb, bytes);
           bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off),
                    bytes, fb);
+          if (++slot == kK1Stages) {
+            slot = 0;
+            phase ^= 1;
+          }
         }
         e = static_cast<int64_t>(p.row) * a.V + p.j1;
       }
@@ -310,7 +413,8 @@ __global__ void __launch_bounds__(kK1Threads, kK1CtasPerSm) row_stats_kernel(con
   const int ct = tid - 32;
   const int cw = warp - 1;
   const float c = a.c;
-  int st = 0, npiece = 0;
+  int slot = 0, npiece = 0;
+  uint32_t phase = 0;
   bool ok = true;
   for (int64_t e = E0; e < E1; ++npiece) {
     const Piece p = make_piece<ES>(a, e, E1);
@@ -319,29 +423,42 @@ __global__ void __launch_bounds__(kK1Threads, kK1CtasPerSm) row_stats_kernel(con
     cand.base = 0;
     cand.jbase = 0;
     cand.nvec = 0;
+    cand.k0 = 0;
     cand.j = INT_MAX;
     for (int j = p.j0 + ct; j < p.head_end; j += kK1ConsumerThreads)
       fold_scalar(Elem<ES>::load(p.rowp, j), j, c, m, mc, s, cand);
-    for (int sg = 0; sg < p.nst; ++sg, ++st) {
-      if (!ok) continue;
-      const int slot = st % kK1Stages;
-      if (!mbar_wait_bounded(smem_u32(&full_bar[slot]), (st / kK1Stages) & 1)) {
-        ok = false;   // stop consuming (and releasing); the producer times out too
-        continue;
+    // Per-piece constants; the stage loop only steps them.
+    const int last = p.nst - 1;
+    const bool first_edge = p.cp_lo < p.lo;
+    const bool last_hull = p.cp_hi > p.hi;
+    const bool last_edge = last_hull || ((p.cp_hi - p.cp_lo) % kK1StageBytes) != 0;
+    const int last_nvec = static_cast<int>((p.cp_hi - p.cp_lo - static_cast<uintptr_t>(last) * kK1StageBytes) / 16u);
+    // row index of a stage's first element (the first may precede j0 by up to 7)
+    int jbase = p.j0 - static_cast<int>((p.lo - p.cp_lo) / ES);
+    uintptr_t gaddr = p.cp_lo;
+    for (int sg = 0; sg < p.nst; ++sg) {
+      if (ok) {
+        if (!mbar_wait_bounded(smem_u32(&full_bar[slot]), phase)) {
+          ok = false;   // stop consuming (and releasing); the producer times out too
+        } else {
+          const uint4* sv4 = reinterpret_cast<const uint4*>(ring + slot * kK1StageBytes);
+          if ((sg == 0 && first_edge) || (sg == last && last_edge)) {
+            const int nvec = sg == last ? last_nvec : kStageVecs * kK1ConsumerThreads;
+            fold_stage_edge<ES>(sv4, nvec, ct, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,
+                                (sg == last && last_hull) ? nvec - 1 : -1, gaddr, c, m, mc, s, cand);
+          }
+          else
+            fold_stage_full<ES>(sv4, ct, jbase, gaddr, c, m, mc, s, cand);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+        }
       }
-      const uint32_t off = static_cast<uint32_t>(sg) * kK1StageBytes;
-      const int nvec = static_cast<int>(min(static_cast<uintptr_t>(kK1StageBytes), p.cp_hi - p.cp_lo - off) / 16u);
-      // row index of the stage's first element (may precede j0 by up to 7)
-      const int jbase = p.j0 + static_cast<int>((static_cast<int64_t>(p.cp_lo + off) -
-                                                 static_cast<int64_t>(p.lo)) / ES);
-      const bool edge = (sg == 0 && p.cp_lo < p.lo) || (sg == p.nst - 1 && p.cp_hi > p.hi);
-      const uint4* sv4 = reinterpret_cast<const uint4*>(ring + slot * kK1StageBytes);
-      if (!edge && nvec == kGroupVecs * kK1ConsumerThreads)
-        fold_stage_full<ES>(sv4, ct, jbase, p.cp_lo + off, c, m, mc, s, cand);
-      else
-        fold_stage_edge<ES>(sv4, nvec, ct, jbase, p.j0, p.j1, p.cp_lo + off, c, m, mc, s, cand);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+      jbase += kK1StageBytes / ES;
+      gaddr += kK1StageBytes;
+      if (++slot == kK1Stages) {
+        slot = 0;
+        phase ^= 1;
+      }
     }
     for (int j = p.tail_begin + ct; j < p.j1; j += kK1ConsumerThreads)
       fold_scalar(Elem<ES>::load(p.rowp, j), j, c, m, mc, s, cand);

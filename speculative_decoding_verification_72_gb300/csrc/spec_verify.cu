@@ -148,8 +148,12 @@ cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(row_stats_kernel<ES>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kK1SmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(row_stats_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kK1SmemBytes);
+    if (e != cudaSuccess) return e;
+    // The largest shared-memory carveout, so kK1CtasPerSm rings fit on one SM.
+    e = cudaFuncSetAttribute(row_stats_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
