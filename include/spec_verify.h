@@ -190,6 +190,33 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
                            float* out_logprob, float* out_mu, int32_t* out_status,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of the library's static scratch array used by
+ * spec_verify_greedy_static (one array per GPU that loads the library). */
+#define SV_STATIC_SCRATCH_BYTES (2u << 20)
+
+/* Greedy chain verification that allocates nothing and takes no workspace.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that hold only their input and output buffers and cannot allocate device
+ * memory themselves -- plugin hosts that hand a custom op fixed buffers,
+ * serving loops that forbid allocation after start-up (an allocation can
+ * synchronise the device or fail under memory pressure), or code running
+ * while another component owns the allocator.
+ * Arguments, outputs and results are exactly those of spec_verify_greedy; the
+ * scratch is a file-scope static device array of SV_STATIC_SCRATCH_BYTES,
+ * which holds B*(K+1) <= 126976 rows. Larger requests return
+ * SV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address once; make that first call before any stream
+ * capture. Every call shares the one array per device, and it keeps the last
+ * call's contents: nothing in it has to start at zero (each call writes all it
+ * reads), but two calls whose work overlaps on the GPU (different streams, or
+ * concurrent host threads) race on it and must be serialised by the caller. */
+sv_status spec_verify_greedy_static(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                    const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                    int32_t* out_tokens, int32_t* out_num_accepted,
+                                    float* out_logprob, float* out_mu, int32_t* out_status,
+                                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

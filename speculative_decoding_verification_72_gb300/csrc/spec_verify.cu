@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "spec_verify.h"
 #include "decide.cuh"
@@ -448,6 +449,44 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// ------------------------------------------------- no-allocation variant
+//
+// Scratch for spec_verify_greedy_static: a file-scope device array, so a
+// caller that cannot allocate device memory still gets the workspace the
+// greedy kernels need. Every GPU that loads the library holds one copy until
+// the process exits. Host code must not pass g_static_scratch itself to a
+// kernel (in host code that name is a host-side stand-in, not a device
+// address); the device address is looked up once per device below.
+static __device__ __align__(256) unsigned char g_static_scratch[SV_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_dev[64] = {nullptr};
+}  // namespace
+
+sv_status spec_verify_greedy_static(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                    const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                    int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
+                                    float* out_mu, int32_t* out_status, void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (g_static_scratch_dev[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return SV_ERR_CUDA;
+      g_static_scratch_dev[dev] = p;
+    }
+    scratch = g_static_scratch_dev[dev];
+  }
+  // The greedy path's own size check turns a request that needs more than
+  // the static array into SV_ERR_WORKSPACE_TOO_SMALL before any launch.
+  return spec_verify_greedy(target_logits, dtype, row_stride, draft_tokens, B, K, V, out_tokens,
+                            out_num_accepted, out_logprob, out_mu, out_status, scratch,
+                            SV_STATIC_SCRATCH_BYTES, stream);
 }
 
 }  // extern "C"

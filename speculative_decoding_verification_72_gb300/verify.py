@@ -68,6 +68,8 @@ _SIGS = {
     "spec_verify_tree": (_I32, [_P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32,
                                 _F, _P, RuleParams,
                                 _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_greedy_static": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
+                                         _P, _P, _P, _P, _P, _P]),
 }
 
 
