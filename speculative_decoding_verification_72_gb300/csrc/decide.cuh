@@ -387,14 +387,17 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
           if (!dup) {
             counted = true;
             lp2 = sm_g[kid] * c - sm_l2[cur];
-            const double p = static_cast<double>(ex2(lp2));
+            const float p = ex2(lp2);
             if (a.rule.rule == 1) {
-              acc = (p >= static_cast<double>(a.rule.tau)) ? 1.0 : 0.0;
+              acc = (p >= a.rule.tau) ? 1.0 : 0.0;
             } else {
-              const double ratio = rest <= 0.0 ? 1.0 : fmin(1.0, p / rest);
-              acc = (a.rule.rule == 2) ? pow(ratio, static_cast<double>(a.rule.alpha)) : ratio;
+              // rest is kept in double (it cancels when the rejected mass is
+              // close to 1); the ratio itself needs only fp32
+              const float ratio = rest <= 0.0 ? 1.f : fminf(1.f, p / static_cast<float>(rest));
+              acc = (a.rule.rule == 2) ? static_cast<double>(exp2f(a.rule.alpha * log2f(ratio)))
+                                       : static_cast<double>(ratio);
             }
-            rest -= p;
+            rest -= static_cast<double>(p);
           }
         }
         if (static_cast<double>(sm_u[kid]) < acc) {

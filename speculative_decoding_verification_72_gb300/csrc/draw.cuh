@@ -4,13 +4,15 @@
 // nanospec README's tree and deterministic-draft rules draw from p with the
 // rejected tokens removed).
 //
-// Grid = B x P CTAs; CTA (b, c) sums the weights w_j of vocabulary chunk c of
-// request b's row (and, for the zero-mass fallback, sum p_j) and takes a ticket.
-// The last CTA of request b forms the ordered prefix over the P chunk sums in
-// double, finds the chunk where u * S falls, re-reads that chunk (just read,
-// so L2-resident) with contiguous per-thread ranges, and resolves the
-// smallest j whose inclusive prefix sum exceeds u * S with a block scan.
-// Per-element weights are recomputed by the same code in both passes.
+// Grid = B x P CTAs; CTA (b, c) sums the weights w_j of vocabulary chunk c
+// (kK3ChunkElems elements) of request b's row (and, for the zero-mass
+// fallback, sum p_j) with coalesced element-strided loads, and takes a
+// ticket. The last CTA of request b forms the ordered prefix over the P chunk
+// sums in double, finds the chunk where u * S falls, recomputes that chunk's
+// weights (just read, so L2-resident) into shared memory, and resolves the
+// smallest j whose inclusive prefix sum exceeds u * S with a block scan over
+// contiguous shared-memory segments. Per-element weights are recomputed by the
+// same code in both passes.
 #pragma once
 
 #include "sv_common.cuh"
@@ -18,7 +20,9 @@
 namespace sv {
 
 constexpr int kK3Threads = 256;
-constexpr int kK3ChunkBytes = 32768;
+constexpr int kK3PerThread = 16;                          // elements per thread per chunk
+constexpr int kK3ChunkElems = kK3Threads * kK3PerThread;  // 4096
+constexpr int kK3SegStride = kK3PerThread + 1;           // padded shared-memory segment
 constexpr int kK3LocalExcl = 64;
 
 struct DrawArgs {
@@ -108,6 +112,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   grid_dep_launch();
   __shared__ float red[kK3Threads / 32];
   __shared__ float scan_w[kK3Threads / 32];
+  __shared__ float seg[kK3Threads * kK3SegStride];
   __shared__ int s_ex[kK3LocalExcl];
   __shared__ int s_nex;
   __shared__ int s_last, s_chunk, s_usep, s_pick, s_lastpos;
@@ -127,17 +132,21 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   row.lp2 = d.lp2;
   row.lq2 = d.lq2;
 
-  // Pass 1: this chunk's weight sums.
+  // Pass 1: this chunk's weight sums (element j = lo + tid + k * kK3Threads).
   const int lo = ch * a.chunk_elems;
   const int hi = min(a.V, lo + a.chunk_elems);
   int nex = gather_excl(d, ex, lo, hi, s_ex, &s_nex);
   float sw = 0.f, sp = 0.f;
-  for (int j = lo + tid; j < hi; j += kK3Threads) {
-    float w, p;
-    row.weight(j, w, p);
-    if (nex && is_excluded(j, nex, s_ex, ex, d.n_excl)) w = 0.f;
-    sw += w;
-    sp += p;
+#pragma unroll
+  for (int k = 0; k < kK3PerThread; ++k) {
+    const int j = lo + tid + k * kK3Threads;
+    if (j < hi) {
+      float w, p;
+      row.weight(j, w, p);
+      if (nex && is_excluded(j, nex, s_ex, ex, d.n_excl)) w = 0.f;
+      sw += w;
+      sp += p;
+    }
   }
   const float tw = block_sum_fixed(sw, red);
   const float tp = block_sum_fixed(sp, red);
@@ -197,25 +206,35 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   }
   __syncthreads();
 
-  // Pass 2: contiguous per-thread ranges over the chosen chunk.
+  // Pass 2: the chosen chunk's weights into shared memory (coalesced), then a
+  // scan over contiguous segments: thread t owns elements [t*16, t*16 + 16).
   const int c2 = s_chunk;
   const int usep = s_usep;
   const float thr = s_thr;
   const int lo2 = c2 * a.chunk_elems;
   const int hi2 = min(a.V, lo2 + a.chunk_elems);
   nex = usep ? 0 : gather_excl(d, ex, lo2, hi2, s_ex, &s_nex);
-  const int per = (hi2 - lo2 + kK3Threads - 1) / kK3Threads;
-  const int my_lo = min(hi2, lo2 + tid * per);
-  const int my_hi = min(hi2, my_lo + per);
+#pragma unroll
+  for (int k = 0; k < kK3PerThread; ++k) {
+    const int i = tid + k * kK3Threads;   // chunk offset
+    const int j = lo2 + i;
+    float w = 0.f;
+    if (j < hi2) {
+      float p;
+      row.weight(j, w, p);
+      if (usep) w = p;
+      else if (nex && is_excluded(j, nex, s_ex, ex, d.n_excl)) w = 0.f;
+    }
+    seg[(i / kK3PerThread) * kK3SegStride + (i % kK3PerThread)] = w;
+  }
+  __syncthreads();
+  const float* mine = seg + tid * kK3SegStride;
   float tsum = 0.f;
   int lastpos = -1;
-  for (int j = my_lo; j < my_hi; ++j) {
-    float w, p;
-    row.weight(j, w, p);
-    if (usep) w = p;
-    else if (nex && is_excluded(j, nex, s_ex, ex, d.n_excl)) w = 0.f;
-    tsum += w;
-    if (w > 0.f) lastpos = j;
+#pragma unroll
+  for (int k = 0; k < kK3PerThread; ++k) {
+    tsum += mine[k];
+    if (mine[k] > 0.f) lastpos = lo2 + tid * kK3PerThread + k;
   }
   // Block exclusive scan of the per-thread sums (thread order = index order).
   const int warp = tid >> 5, lane = tid & 31;
@@ -230,7 +249,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   float wbase = 0.f;
   for (int w = 0; w < warp; ++w) wbase += scan_w[w];
   const float excl_sum = wbase + incl - tsum;
-  if (excl_sum + tsum > thr && my_lo < my_hi) atomicMin(&s_pick, tid);
+  if (excl_sum + tsum > thr && tsum > 0.f) atomicMin(&s_pick, tid);
   if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
   __syncthreads();
   int j_out = -1;
@@ -238,15 +257,12 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
     if (tid == 0) j_out = s_lastpos >= 0 ? s_lastpos : hi2 - 1;
   } else if (tid == s_pick) {
     float part = 0.f;
-    j_out = my_hi - 1;
-    for (int j = my_lo; j < my_hi; ++j) {
-      float w, p;
-      row.weight(j, w, p);
-      if (usep) w = p;
-      else if (nex && is_excluded(j, nex, s_ex, ex, d.n_excl)) w = 0.f;
-      part += w;
-      if (excl_sum + part > thr) {
-        j_out = j;
+    j_out = lastpos;
+#pragma unroll
+    for (int k = 0; k < kK3PerThread; ++k) {
+      part += mine[k];
+      if (excl_sum + part > thr && mine[k] > 0.f) {
+        j_out = lo2 + tid * kK3PerThread + k;
         break;
       }
     }

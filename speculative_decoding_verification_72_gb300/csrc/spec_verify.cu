@@ -43,24 +43,13 @@ struct Plan {
   size_t total = 0;
 };
 
-// Split a V-element row into n pieces of at most max_bytes, each a multiple
-// of 64 elements.
-void split_row(int64_t V, int es, int64_t max_bytes, int32_t* n_out, int32_t* elems_out) {
-  int64_t n = (V * es + max_bytes - 1) / max_bytes;
-  if (n < 1) n = 1;
-  int64_t e = (V + n - 1) / n;
-  e = (e + 63) / 64 * 64;
-  n = (V + e - 1) / e;
-  *n_out = static_cast<int32_t>(n);
-  *elems_out = static_cast<int32_t>(e);
-}
-
 // Workspace layout; independent of the device (K1's partial array is sized
 // for the largest grid K1 may use, kK1MaxCtas).
 bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, bool draw,
                int64_t excl_stride, Plan* pl) {
   if (V < 1 || es == 0 || B < 0 || rows_t < 0 || rows_d < 0) return false;
-  split_row(V, es, kK3ChunkBytes, &pl->P, &pl->chunk_elems);
+  pl->chunk_elems = kK3ChunkElems;
+  pl->P = static_cast<int32_t>((V + kK3ChunkElems - 1) / kK3ChunkElems);
   pl->rows_total = rows_t + rows_d;
   if (pl->rows_total > INT32_MAX / 2) return false;
   pl->T = pl->rows_total * V;
