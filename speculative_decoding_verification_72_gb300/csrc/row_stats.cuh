@@ -12,8 +12,9 @@
 // "empty" mbarrier. Warps 1..7 consume: each thread folds its 16-byte
 // vectors of each stage into a running (max, sum 2^((x - max) c)) and
 // remembers the group holding its first maximum. At the end of every row
-// piece the consumers resolve the exact argmax, reduce (shuffles, then a
-// named barrier across the consumer warps) and write one Partial per
+// piece the consumers resolve the exact argmax from a per-thread shared-memory
+// stash of that group (copied when the maximum rose), reduce (shuffles, then
+// a named barrier across the consumer warps) and write one Partial per
 // (CTA, row piece); the decide kernel merges a row's partials.
 //
 // Copies cover the 16-byte-aligned hull of each row piece when it lies inside
@@ -44,7 +45,10 @@ constexpr int kStageVecs = 8;
 constexpr int kGroupVecs = 4;
 constexpr int kK1StageBytes = kK1ConsumerThreads * kStageVecs * 16;   // 28 KB
 constexpr int kK1Stages = 3;
-constexpr int kK1SmemBytes = kK1StageBytes * kK1Stages;
+constexpr int kK1RingBytes = kK1StageBytes * kK1Stages;
+// Per-thread copy of the half-stage that holds its running maximum (16 words).
+constexpr int kK1StashBytes = kK1ConsumerThreads * kGroupVecs * 16;
+constexpr int kK1SmemBytes = kK1RingBytes + kK1StashBytes;
 constexpr int kK1MaxCtas = 4096;                      // bound used to size the workspace
 constexpr int kK1MinBytesPerCta = 16384;
 static_assert(kStageVecs == 2 * kGroupVecs, "a stage is folded as two groups per thread");
@@ -128,14 +132,14 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
-// Where a thread's running maximum first appeared: a scalar element (base == 0,
-// exact index j) or one of its groups (re-read at the end of the piece).
+// Where a thread's running maximum first appeared: a scalar element
+// (stage -1, exact index j) or one half of one stage of the current row piece,
+// whose 16 words the thread has copied to its shared-memory stash.
 struct GroupCand {
-  uintptr_t base;   // global address of the stage's first copied byte, or 0
-  int jbase;        // row index of the stage's first element
-  int nvec;         // vectors in the stage
-  int k0;           // the group's first vector slot k (vector ct + k * kK1ConsumerThreads)
-  int j;            // exact index of a scalar candidate
+  int stage;   // stage index within the piece, or -1 for a scalar element
+  int half;    // vectors k = 4*half .. 4*half + 3 of the thread's stage share
+  int j;       // exact index of a scalar candidate
+  int jbase;   // row index of the candidate stage's first element
 };
 
 // Scalar fold (ragged edges only); strict '>' since a thread visits its
@@ -146,7 +150,7 @@ __device__ __forceinline__ void fold_scalar(float x, int j, float c, float& m, f
     s = (m == -INFINITY) ? 0.f : s * ex2((m - x) * c);
     m = x;
     mc = x * c;
-    cand.base = 0;
+    cand.stage = -1;
     cand.j = j;
   }
   if (x > -INFINITY) s += ex2(fmaf(x, c, -mc));
@@ -210,89 +214,24 @@ __device__ __forceinline__ float group_sum(const uint32_t (&w)[kGroupWords], flo
   return a.x + a.y;
 }
 
-// Fold one group into (m, s). After a piece's first group the exponentials
-// use the running maximum from before the group, so they do not wait on the
-// group's own maximum; when the maximum rises the running sum is rescaled
-// once (and the group re-summed against the new maximum only if it rose by so
-// much that the old reference could overflow). The argmax keeps only the
-// group where the maximum first rose: groups arrive in increasing index
-// order, so a strict '>' keeps the lowest index.
-template <int ES>
-__device__ __forceinline__ void fold_words(const uint32_t (&w)[kGroupWords], int jbase, int nvec,
-                                           int k0, uintptr_t gbase, float c, float& m, float& mc,
-                                           float& s, GroupCand& cand) {
-  if (m == -INFINITY) {
-    const float gmax = group_max<ES>(w);
-    if (gmax > -INFINITY) {
-      mc = gmax * c;
-      s = group_sum<ES>(w, c, mc);
-      m = gmax;
-      cand.base = gbase;
-      cand.jbase = jbase;
-      cand.nvec = nvec;
-      cand.k0 = k0;
-    }
-    return;
-  }
-  const float gsum = group_sum<ES>(w, c, mc);
-  const float gmax = group_max<ES>(w);
-  if (gmax > m) {
-    const float d = (m - gmax) * c;
-    if (d > -100.f && gsum <= FLT_MAX) {
-      s = (s + gsum) * ex2(d);
-    } else {
-      s = s * ex2(d) + group_sum<ES>(w, c, gmax * c);
-    }
-    m = gmax;
-    mc = gmax * c;
-    cand.base = gbase;
-    cand.jbase = jbase;
-    cand.nvec = nvec;
-    cand.k0 = k0;
-  } else {
-    s += gsum;
-  }
-}
+constexpr int kStageFullVecs = kStageVecs * kK1ConsumerThreads;
 
-// A full interior stage: kStageVecs vectors per thread, folded as two groups,
-// no masking.
-template <int ES>
-__device__ __forceinline__ void fold_stage_full(const uint4* sv4, int ct, int jbase, uintptr_t gbase,
-                                                float c, float& m, float& mc, float& s, GroupCand& cand) {
-#pragma unroll
-  for (int h = 0; h < kStageVecs / kGroupVecs; ++h) {
-    uint32_t w[kGroupWords];
-#pragma unroll
-    for (int k = 0; k < kGroupVecs; ++k) {
-      const uint4 v = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
-      w[4 * k] = v.x;
-      w[4 * k + 1] = v.y;
-      w[4 * k + 2] = v.z;
-      w[4 * k + 3] = v.w;
-    }
-    fold_words<ES>(w, jbase, kStageVecs * kK1ConsumerThreads, h * kGroupVecs, gbase, c, m, mc, s, cand);
-  }
-}
-
-// A stage with fewer than kStageVecs vectors per thread, or whose first or
-// last vector holds bytes outside the piece (the 16-byte hull adds at most
-// 15 bytes at each end, so only vector 0 of the first stage and vector
-// nvec - 1 of the last can). Missing vectors read as -inf; only those two
-// vectors are masked element by element.
-template <int ES>
-__device__ __forceinline__ void fold_stage_edge(const uint4* sv4, int nvec, int ct, int jbase, int j0,
-                                                int j1, int mask_lo_v, int mask_hi_v, uintptr_t gbase,
-                                                float c, float& m, float& mc, float& s, GroupCand& cand) {
+// One half (kGroupVecs vectors, 16 words) of a thread's share of a stage:
+// vectors v = ct + (4*h + k) * kK1ConsumerThreads. With EDGE, vectors past
+// nvec read as -inf and the two vectors that may hold bytes outside the piece
+// (mask_lo_v, mask_hi_v) are masked element by element.
+template <int ES, bool EDGE>
+__device__ __forceinline__ void load_half(const uint4* sv4, int ct, int h, int nvec, int jbase, int j0,
+                                          int j1, int mask_lo_v, int mask_hi_v,
+                                          uint32_t (&w)[kGroupWords]) {
   constexpr int N = Elem<ES>::kVec;
-  // -inf in every element of a word
-  constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;
+  constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;   // -inf in every element
 #pragma unroll
-  for (int h = 0; h < kStageVecs / kGroupVecs; ++h) {
-    uint32_t w[kGroupWords];
-#pragma unroll
-    for (int k = 0; k < kGroupVecs; ++k) {
-      const int v = ct + (h * kGroupVecs + k) * kK1ConsumerThreads;
-      uint4 q = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
+  for (int k = 0; k < kGroupVecs; ++k) {
+    const int v = ct + (h * kGroupVecs + k) * kK1ConsumerThreads;
+    uint4 q;
+    if constexpr (EDGE) {
+      q = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
       if (v < nvec) q = sv4[v];
       if (v == mask_lo_v || v == mask_hi_v) {
         uint32_t word[4] = {q.x, q.y, q.z, q.w};
@@ -311,36 +250,114 @@ __device__ __forceinline__ void fold_stage_edge(const uint4* sv4, int nvec, int 
         }
         q = make_uint4(word[0], word[1], word[2], word[3]);
       }
-      w[4 * k] = q.x;
-      w[4 * k + 1] = q.y;
-      w[4 * k + 2] = q.z;
-      w[4 * k + 3] = q.w;
+    } else {
+      q = sv4[v];
     }
-    fold_words<ES>(w, jbase, nvec, h * kGroupVecs, gbase, c, m, mc, s, cand);
+    w[4 * k] = q.x;
+    w[4 * k + 1] = q.y;
+    w[4 * k + 2] = q.z;
+    w[4 * k + 3] = q.w;
   }
 }
 
-// Lowest index in [j0, j1) of the remembered candidate holding the value m,
-// re-read from global memory (INT_MAX if m is -inf).
-template <int ES>
-__device__ __forceinline__ int resolve_cand(const GroupCand& cand, int ct, float m, int j0, int j1) {
-  if (!(m > -INFINITY)) return INT_MAX;
-  if (cand.base == 0) return cand.j;
-  constexpr int N = Elem<ES>::kVec;
+// Fold one stage (two halves) into (m, s). After the piece's first finite
+// stage the exponentials use the running maximum from before the stage, so
+// they do not wait on the stage's own maximum; the running sum is rescaled
+// once per stage when the maximum rises (both halves re-summed from shared
+// memory against the new maximum only if the rise could overflow). The argmax
+// keeps the half where the maximum first rose: stages and halves arrive in
+// increasing index order, so a strict '>' (and the lower half on a tie) keeps
+// the lowest index.
+// Record half h of this stage as the thread's candidate: its words (as
+// loaded, masked where needed) go to the thread's stash, vector k at
+// stash[k * kK1ConsumerThreads + ct].
+template <int ES, bool EDGE>
+__device__ __forceinline__ void stash_half(const uint4* sv4, uint4* stash, int ct, int h, int nvec,
+                                           int jbase, int j0, int j1, int mask_lo_v, int mask_hi_v,
+                                           int sg, GroupCand& cand) {
+  uint32_t w[kGroupWords];
+  load_half<ES, EDGE>(sv4, ct, h, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
 #pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k) {
-    const int v = ct + (cand.k0 + k) * kK1ConsumerThreads;
-    if (v < cand.nvec) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(cand.base) + v);
-      float f[N];
-      Elem<ES>::unpack(w, f);
-      const int jv = cand.jbase + v * N;
-#pragma unroll
-      for (int e = 0; e < N; ++e)
-        if (f[e] == m && jv + e >= j0 && jv + e < j1) return jv + e;
+  for (int k = 0; k < kGroupVecs; ++k)
+    stash[k * kK1ConsumerThreads + ct] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  cand.stage = sg;
+  cand.half = h;
+  cand.jbase = jbase;
+}
+
+template <int ES, bool EDGE>
+__device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int nvec, int ct, int jbase,
+                                           int j0, int j1, int mask_lo_v, int mask_hi_v, int sg, float c,
+                                           float& m, float& mc, float& s, GroupCand& cand) {
+  uint32_t w[kGroupWords];
+  if (m == -INFINITY) {   // the maximum first, then the sums against it (one stage per piece)
+    load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+    const float ga = group_max<ES>(w);
+    load_half<ES, EDGE>(sv4, ct, 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+    const float gb = group_max<ES>(w);
+    const float gmax = fmaxf(ga, gb);
+    if (gmax > -INFINITY) {
+      mc = gmax * c;
+      s = group_sum<ES>(w, c, mc);
+      load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+      s += group_sum<ES>(w, c, mc);
+      m = gmax;
+      stash_half<ES, EDGE>(sv4, stash, ct, ga >= gb ? 0 : 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, sg,
+                           cand);
     }
+    return;
   }
-  return INT_MAX;
+  load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+  const float sa = group_sum<ES>(w, c, mc);
+  const float ga = group_max<ES>(w);
+  load_half<ES, EDGE>(sv4, ct, 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+  const float sb = group_sum<ES>(w, c, mc);
+  const float gb = group_max<ES>(w);
+  const float gmax = fmaxf(ga, gb);
+  const float gsum = sa + sb;
+  if (gmax > m) {
+    const float d = (m - gmax) * c;
+    if (d > -100.f && gsum <= FLT_MAX) {
+      s = (s + gsum) * ex2(d);
+    } else {
+      const float nmc = gmax * c;
+      float r = group_sum<ES>(w, c, nmc);
+      load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+      r += group_sum<ES>(w, c, nmc);
+      s = s * ex2(d) + r;
+    }
+    m = gmax;
+    mc = gmax * c;
+    stash_half<ES, EDGE>(sv4, stash, ct, ga >= gb ? 0 : 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, sg,
+                         cand);
+  } else if (gmax > -INFINITY) {
+    s += gsum;
+  }
+}
+
+// Lowest index in [j0, j1) of the thread's candidate holding the value m,
+// read back from its stash (all four vectors loaded before the search);
+// INT_MAX if m is -inf.
+template <int ES>
+__device__ __forceinline__ int resolve_cand(const GroupCand& cand, const uint4* stash, int ct, float m,
+                                            int j0, int j1) {
+  if (!(m > -INFINITY)) return INT_MAX;
+  if (cand.stage < 0) return cand.j;
+  constexpr int N = Elem<ES>::kVec;
+  uint4 q[kGroupVecs];
+#pragma unroll
+  for (int k = 0; k < kGroupVecs; ++k) q[k] = stash[k * kK1ConsumerThreads + ct];
+  int best = INT_MAX;
+#pragma unroll
+  for (int k = kGroupVecs - 1; k >= 0; --k) {
+    float f[N];
+    Elem<ES>::unpack(q[k], f);
+    const int jv = cand.jbase + (ct + (cand.half * kGroupVecs + k) * kK1ConsumerThreads) * N;
+#pragma unroll
+    for (int e = N - 1; e >= 0; --e)
+      if (f[e] == m && jv + e >= j0 && jv + e < j1) best = jv + e;
+  }
+  return best;
 }
 
 template <int ES>
@@ -410,6 +427,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   }
 
   // -------------------------------------------------------------- consumers
+  uint4* const stash = reinterpret_cast<uint4*>(ring + kK1RingBytes);
   const int ct = tid - 32;
   const int cw = warp - 1;
   const float c = a.c;
@@ -420,22 +438,22 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
     const Piece p = make_piece<ES>(a, e, E1);
     float m = -INFINITY, mc = -INFINITY, s = 0.f;
     GroupCand cand;
-    cand.base = 0;
-    cand.jbase = 0;
-    cand.nvec = 0;
-    cand.k0 = 0;
+    cand.stage = -1;
+    cand.half = 0;
     cand.j = INT_MAX;
+    cand.jbase = 0;
     for (int j = p.j0 + ct; j < p.head_end; j += kK1ConsumerThreads)
       fold_scalar(Elem<ES>::load(p.rowp, j), j, c, m, mc, s, cand);
     // Per-piece constants; the stage loop only steps them.
     const int last = p.nst - 1;
     const bool first_edge = p.cp_lo < p.lo;
     const bool last_hull = p.cp_hi > p.hi;
-    const bool last_edge = last_hull || ((p.cp_hi - p.cp_lo) % kK1StageBytes) != 0;
-    const int last_nvec = static_cast<int>((p.cp_hi - p.cp_lo - static_cast<uintptr_t>(last) * kK1StageBytes) / 16u);
-    // row index of a stage's first element (the first may precede j0 by up to 7)
-    int jbase = p.j0 - static_cast<int>((p.lo - p.cp_lo) / ES);
-    uintptr_t gaddr = p.cp_lo;
+    const int last_nvec =
+        static_cast<int>((p.cp_hi - p.cp_lo - static_cast<uintptr_t>(last > 0 ? last : 0) * kK1StageBytes) / 16u);
+    const bool last_edge = last_hull || last_nvec != kStageFullVecs;
+    // row index of the piece's first copied element (may precede j0 by up to 7)
+    const int jbase0 = p.j0 - static_cast<int>((p.lo - p.cp_lo) / ES);
+    int jbase = jbase0;
     for (int sg = 0; sg < p.nst; ++sg) {
       if (ok) {
         if (!mbar_wait_bounded(smem_u32(&full_bar[slot]), phase)) {
@@ -443,18 +461,17 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
         } else {
           const uint4* sv4 = reinterpret_cast<const uint4*>(ring + slot * kK1StageBytes);
           if ((sg == 0 && first_edge) || (sg == last && last_edge)) {
-            const int nvec = sg == last ? last_nvec : kStageVecs * kK1ConsumerThreads;
-            fold_stage_edge<ES>(sv4, nvec, ct, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,
-                                (sg == last && last_hull) ? nvec - 1 : -1, gaddr, c, m, mc, s, cand);
+            const int nvec = sg == last ? last_nvec : kStageFullVecs;
+            fold_stage<ES, true>(sv4, stash, nvec, ct, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,
+                                 (sg == last && last_hull) ? nvec - 1 : -1, sg, c, m, mc, s, cand);
+          } else {
+            fold_stage<ES, false>(sv4, stash, kStageFullVecs, ct, jbase, 0, 0, -1, -1, sg, c, m, mc, s, cand);
           }
-          else
-            fold_stage_full<ES>(sv4, ct, jbase, gaddr, c, m, mc, s, cand);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
         }
       }
       jbase += kK1StageBytes / ES;
-      gaddr += kK1StageBytes;
       if (++slot == kK1Stages) {
         slot = 0;
         phase ^= 1;
@@ -468,7 +485,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
     float wm = m;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-    int widx = (m == wm) ? resolve_cand<ES>(cand, ct, m, p.j0, p.j1) : INT_MAX;
+    int widx = (m == wm) ? resolve_cand<ES>(cand, stash, ct, m, p.j0, p.j1) : INT_MAX;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) widx = min(widx, __shfl_xor_sync(0xffffffffu, widx, o));
     float ws = (m == -INFINITY) ? 0.f : s * ex2((m - wm) * c);
