@@ -24,6 +24,13 @@ constexpr int kK3PerThread = 16;                          // elements per thread
 constexpr int kK3ChunkElems = kK3Threads * kK3PerThread;  // 4096
 constexpr int kK3SegStride = kK3PerThread + 1;           // padded shared-memory segment
 constexpr int kK3LocalExcl = 64;
+// Chunk sums staged in shared memory by the last CTA (V up to 1M elements;
+// beyond that the rest are read from global memory).
+constexpr int kK3MaxChunks = 256;
+
+__device__ __forceinline__ float2 chunk_sum(const float2* s_part, const float2* g_part, int k) {
+  return k < kK3MaxChunks ? s_part[k] : __ldcg(&g_part[k]);
+}
 
 struct DrawArgs {
   const uint8_t* tgt;
@@ -118,6 +125,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   __shared__ int s_last, s_chunk, s_usep, s_pick, s_lastpos;
   __shared__ float s_thr;
   __shared__ double s_S;
+  __shared__ float2 s_part[kK3MaxChunks];
 
   const int tid = threadIdx.x;
   const int b = blockIdx.x / a.P;
@@ -160,21 +168,25 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // Last CTA of request b: ordered prefix over the chunk sums (double).
+  // Last CTA of request b: the chunk sums are loaded together into shared
+  // memory (a loop of dependent loads would pay one L2 round trip per
+  // chunk), then thread 0 forms their ordered prefix in double.
+  const float2* pp_g = a.part + static_cast<int64_t>(b) * a.P;
+  for (int k = tid; k < a.P && k < kK3MaxChunks; k += kK3Threads) s_part[k] = __ldcg(&pp_g[k]);
+  __syncthreads();
   if (tid == 0) {
-    const float2* pp = a.part + static_cast<int64_t>(b) * a.P;
     double S = 0.0;
-    for (int k = 0; k < a.P; ++k) S += static_cast<double>(__ldcg(&pp[k]).x);
+    for (int k = 0; k < a.P; ++k) S += static_cast<double>(chunk_sum(s_part, pp_g, k).x);
     int usep = !(S > 0.0);
     if (usep) {
       S = 0.0;
-      for (int k = 0; k < a.P; ++k) S += static_cast<double>(__ldcg(&pp[k]).y);
+      for (int k = 0; k < a.P; ++k) S += static_cast<double>(chunk_sum(s_part, pp_g, k).y);
     }
     const double thr = static_cast<double>(d.u) * S;
     double pre = 0.0;
     int cstar = -1;
     for (int k = 0; k < a.P; ++k) {
-      const float2 v = __ldcg(&pp[k]);
+      const float2 v = chunk_sum(s_part, pp_g, k);
       const double w = usep ? v.y : v.x;
       if (pre + w > thr) {
         cstar = k;
@@ -185,7 +197,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
     if (cstar < 0) {   // rounding left no crossing: last chunk with weight
       double run = 0.0, pre_last = 0.0;
       for (int k = 0; k < a.P; ++k) {
-        const float2 v = __ldcg(&pp[k]);
+        const float2 v = chunk_sum(s_part, pp_g, k);
         const double w = usep ? v.y : v.x;
         if (w > 0.0) {
           cstar = k;
