@@ -81,13 +81,27 @@ def aggregate(elapsed_ms_max, rows_per_step, steps, world):
     return world * rows_per_step * steps / (elapsed_ms_max / 1e3)
 
 
-def source_hash():
+# Sources of the kernels one call of each workload kind launches; the entry
+# point file (launch shapes) is in every set.
+_CALL_SOURCES = {
+    "greedy": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "spec_verify.cu"),
+    "draw": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "draw.cuh", "spec_verify.cu"),
+}
+
+
+def source_hash(cfg=None):
+    """Hash of the kernel sources behind one call of workload `cfg` (all of
+    them when cfg is None). A recorded DRAM capture stays valid only while
+    this hash is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_72_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    if cfg is None:
+        names = [n for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
+    else:
+        names = sorted(_CALL_SOURCES["draw" if _launches_per_call(cfg) == 3 else "greedy"])
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -109,7 +123,7 @@ def recorded_traffic(config_name):
         with open(p) as f:
             d = json.load(f)
         e = d.get(config_name)
-        if e and e.get("source_hash") == source_hash():
+        if e and e.get("source_hash") == source_hash(CONFIGS[config_name]):
             return float(e["dram_bytes_per_call"])
     except Exception:
         pass
