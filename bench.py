@@ -76,6 +76,17 @@ def rank_seed(base, rank):
     return int(base) + 1000003 * int(rank)
 
 
+def reduce_over_ranks(value, op, device, world):
+    """MAX or MIN of a per-rank float over all ranks (identity on one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.MIN)
+    return float(t.item())
+
+
 def aggregate(elapsed_ms_max, rows_per_step, steps, world):
     """Whole-job rows/s from the slowest rank's timed region."""
     return world * rows_per_step * steps / (elapsed_ms_max / 1e3)
@@ -404,10 +415,7 @@ def run_gpu(args, cfg, name):
     time.sleep(0.3)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = reduce_over_ranks(elapsed, "max", dev, world)
 
     value = aggregate(elapsed, rows, steps, world)
     step_s = elapsed / 1e3 / steps
@@ -415,10 +423,8 @@ def run_gpu(args, cfg, name):
     achieved = alg_bytes / step_s / 1e9
 
     e2e = _e2e(cfg, pool[0], dev, steps, out, ws)
-    if world > 1:
-        t = torch.tensor([e2e["value"]], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MIN)
-        e2e["value"] = float(t.item()) * world
+    if world > 1:   # the slowest replica's rate, times the replicas
+        e2e["value"] = reduce_over_ranks(e2e["value"], "min", dev, world) * world
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
