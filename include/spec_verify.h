@@ -66,7 +66,8 @@ typedef int32_t sv_status;
 #define SV_ERR_UNSUPPORTED_DTYPE   2  /* dtype is neither SV_F32 nor SV_BF16 */
 #define SV_ERR_WORKSPACE_TOO_SMALL 3  /* workspace_bytes below the required size */
 #define SV_ERR_CUDA                4  /* a CUDA launch or attribute call failed */
-#define SV_ERR_NOT_SUPPORTED       5  /* valid request this build does not implement */
+#define SV_ERR_NOT_SUPPORTED       5  /* valid request this build does not implement
+                                         (no call of this version returns it) */
 
 /* Logit element types. */
 #define SV_F32  0
@@ -144,8 +145,15 @@ sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t r
  *                  u * (total weight), in ascending vocabulary order.
  * With draft logits: exact acceptance min(1, p/q); p(t) = q(t) = 0 rejects
  * (SV_STATUS_ZERO_MASS); residual normalize(relu(p - q)), or p when that mass
- * is zero; mu = p(token). The relaxed and power rules with draft logits are
- * SV_ERR_NOT_SUPPORTED in this version.
+ * is zero; mu = p(token). The power rule accepts with min(1, p/q)^alpha and
+ * the relaxed rule with [p >= tau or rank < top_k]; the residual is the same,
+ * and mu_j(a) = q_j(a) acc_j(a) + (1 - sum_s q_j(s) acc_j(s)) res_j(a) for
+ * every emitted draft row j (the bonus token after K acceptances keeps
+ * mu = p). These two rules add one more pass over rows 0..n of both logit
+ * arrays for those sums.
+ * Relaxed with top_k > 0 adds a per-row selection of the top_k-th largest
+ * logit (rank(t) < top_k iff x_t is at least that value), reading each tested
+ * row two (bf16) or four (fp32) more times.
  * Without draft logits (deterministic drafts): exact a = p(d), power
  * a = p(d)^alpha, relaxed a = [p(d) >= tau or rank(d) < top_k]; mu = a for
  * an accepted draft; on rejection the draw is from p with d removed and mu is

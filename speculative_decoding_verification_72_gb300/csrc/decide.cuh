@@ -37,7 +37,16 @@ struct RuleArgs {
   float tau;
   int32_t top_k;
   float alpha;
+  // Relaxed rule with top_k > 0: per tested row, the top_k-th largest logit
+  // (topk_threshold_kernel); rank(t) < top_k iff x_t >= it. Else nullptr.
+  const float* thr;
 };
+
+// Relaxed acceptance of a token with log2 p = lp2 and raw logit x, in a row
+// whose rank bound is thr.
+__device__ __forceinline__ bool relaxed_accepts(const RuleArgs& r, float lp2, float x, float thr) {
+  return ex2(lp2) >= r.tau || (r.top_k > 0 && x >= thr);
+}
 
 struct ChainArgs {
   const uint8_t* tgt;
@@ -62,6 +71,7 @@ struct ChainArgs {
   int32_t* excl;         // [B * excl_stride]
   int32_t excl_stride;
   uint32_t* draw_counters;  // [B], zeroed here for K3's tickets
+  uint32_t* mu_counters;    // [B], zeroed here for the mu pass's tickets (or nullptr)
 };
 
 // Inputs of one chain position, readable before K1 completes.
@@ -96,6 +106,11 @@ __device__ __forceinline__ ChainIn load_chain_in(const ChainArgs& a, int b, int 
   return in;
 }
 
+// Rank bound of chain row i (read after the wait: its kernel runs before K2).
+__device__ __forceinline__ float row_thr(const ChainArgs& a, int b, int i) {
+  return a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * a.K + i] : INFINITY;
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArgs a) {
   __shared__ int s_first;
@@ -113,6 +128,7 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
   if (tid == 0) {
     s_status = 0;
     if (a.draw_counters) a.draw_counters[b] = 0;
+    if (a.mu_counters) a.mu_counters[b] = 0;
   }
   int n = -1;
   int base = 0;
@@ -151,14 +167,14 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
                 zero = true;
               } else {
                 const float r2 = fminf(0.f, lp2 - lq2);   // log2 min(1, p/q)
-                if (a.rule.rule == 1) acc = (ex2(lp2) >= a.rule.tau) ? 1.f : 0.f;
+                if (a.rule.rule == 1) acc = relaxed_accepts(a.rule, lp2, in.x, row_thr(a, b, i)) ? 1.f : 0.f;
                 else if (a.rule.rule == 2) acc = ex2(a.rule.alpha * r2);
                 else acc = ex2(r2);
               }
             }
           } else if (!in.bad) {   // deterministic draft, rest_1 = 1
             const float r2 = fminf(0.f, lp2);
-            if (a.rule.rule == 1) acc = (ex2(lp2) >= a.rule.tau) ? 1.f : 0.f;
+            if (a.rule.rule == 1) acc = relaxed_accepts(a.rule, lp2, in.x, row_thr(a, b, i)) ? 1.f : 0.f;
             else if (a.rule.rule == 2) acc = ex2(a.rule.alpha * r2);
             else acc = ex2(r2);
           }
@@ -389,7 +405,8 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
             lp2 = sm_g[kid] * c - sm_l2[cur];
             const float p = ex2(lp2);
             if (a.rule.rule == 1) {
-              acc = (p >= a.rule.tau) ? 1.0 : 0.0;
+              const float thr = a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * N + cur] : INFINITY;
+              acc = relaxed_accepts(a.rule, lp2, sm_g[kid], thr) ? 1.0 : 0.0;
             } else {
               // rest is kept in double (it cancels when the rejected mass is
               // close to 1); the ratio itself needs only fp32

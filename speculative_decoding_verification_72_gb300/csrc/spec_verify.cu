@@ -2,12 +2,15 @@
 // validation, the workspace plan shared by the *_workspace_size functions and
 // the launchers, and the kernel launches.
 //
-// One call is K1 (row statistics) -> K2 (decide) [-> K3 (draw)] on the
-// caller's stream. All three are launched with programmatic stream
-// serialization, so each one's launch overlaps the tail of the kernel before
-// it. K1 waits (griddepcontrol.wait) before reading anything, so the logits
-// may come from the kernel just before the call; K2 and K3 read only the
-// call's own inputs before their wait and the previous kernel's results after.
+// One call is K1 (row statistics) [-> top-k bound] -> K2 (decide) [-> K3
+// (draw) [-> mu pass]] on the caller's stream; the bracketed kernels run only
+// for the rules that need them (rules.cuh). Every kernel is launched with
+// programmatic stream serialization, so its launch overlaps the tail of the
+// kernel before it. K1 waits (griddepcontrol.wait) before reading anything,
+// so the logits may come from the kernel just before the call; the others
+// read only the call's own inputs before their wait and earlier kernels'
+// results after it (the top-k kernel waits first, so a wait on it also
+// covers K1).
 
 #include <cmath>
 #include <cstdint>
@@ -18,6 +21,7 @@
 #include "decide.cuh"
 #include "draw.cuh"
 #include "row_stats.cuh"
+#include "rules.cuh"
 
 namespace {
 
@@ -40,13 +44,16 @@ struct Plan {
   int32_t chunk_elems = 0;
   int32_t excl_stride = 0;
   size_t off_part = 0, off_draw = 0, off_excl = 0, off_k3part = 0, off_k3cnt = 0;
+  size_t off_thr = 0, off_mupart = 0, off_mucnt = 0;
   size_t total = 0;
 };
 
 // Workspace layout; independent of the device (K1's partial array is sized
-// for the largest grid K1 may use, kK1MaxCtas).
+// for the largest grid K1 may use, kK1MaxCtas). Stochastic calls also hold a
+// rank bound per target row and, with draft logits (mu_rows = B * K > 0), the
+// mu pass's chunk sums and tickets, whatever rule the call uses.
 bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, bool draw,
-               int64_t excl_stride, Plan* pl) {
+               int64_t excl_stride, int64_t mu_rows, Plan* pl) {
   if (V < 1 || es == 0 || B < 0 || rows_t < 0 || rows_d < 0) return false;
   pl->chunk_elems = kK3ChunkElems;
   pl->P = static_cast<int32_t>((V + kK3ChunkElems - 1) / kK3ChunkElems);
@@ -54,6 +61,7 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
   if (pl->rows_total > INT32_MAX / 2) return false;
   pl->T = pl->rows_total * V;
   if (draw && B * pl->P >= INT32_MAX) return false;
+  if (mu_rows * pl->P >= INT32_MAX) return false;
   pl->excl_stride = static_cast<int32_t>(excl_stride < 1 ? 1 : excl_stride);
   size_t off = 0;
   pl->off_part = off;
@@ -67,6 +75,14 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
     off += align_up(static_cast<size_t>(B) * pl->P * sizeof(float2), kAlign);
     pl->off_k3cnt = off;
     off += align_up(static_cast<size_t>(B) * sizeof(uint32_t), kAlign);
+    pl->off_thr = off;
+    off += align_up(static_cast<size_t>(rows_t) * sizeof(float), kAlign);
+    if (mu_rows > 0) {
+      pl->off_mupart = off;
+      off += align_up(static_cast<size_t>(mu_rows) * pl->P * sizeof(float2), kAlign);
+      pl->off_mucnt = off;
+      off += align_up(static_cast<size_t>(B) * sizeof(uint32_t), kAlign);
+    }
   }
   pl->total = off < kAlign ? kAlign : off;
   return true;
@@ -101,7 +117,6 @@ sv_status check_rule(const sv_rule_params& r) {
   if (r.rule == SV_RULE_RELAXED) {
     if (std::isnan(r.tau)) return SV_ERR_INVALID_ARG;
     if (r.top_k < 0 || r.top_k > SV_MAX_TOP_K) return SV_ERR_INVALID_ARG;
-    if (r.top_k > 0) return SV_ERR_NOT_SUPPORTED;
   }
   return SV_OK;
 }
@@ -110,8 +125,9 @@ RuleArgs rule_args(const sv_rule_params& r) {
   RuleArgs a;
   a.rule = r.rule;
   a.tau = r.tau;
-  a.top_k = r.top_k;
+  a.top_k = r.rule == SV_RULE_RELAXED ? r.top_k : 0;
   a.alpha = r.rule == SV_RULE_POWER ? r.alpha : 1.f;
+  a.thr = nullptr;
   return a;
 }
 
@@ -148,6 +164,23 @@ cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   return launch(row_stats_kernel<ES>, a.G, kK1Threads, kK1SmemBytes, stream, true, a);
+}
+
+cudaError_t launch_topk(const void* tgt, int64_t stride_b, int32_t rows_per_req, int32_t row_pitch,
+                        int32_t V, int32_t k, const int32_t* parents, float* thr, int64_t grid, int es,
+                        cudaStream_t st) {
+  TopkArgs t;
+  t.tgt = static_cast<const uint8_t*>(tgt);
+  t.tgt_stride = stride_b;
+  t.rows_per_req = rows_per_req;
+  t.row_pitch = row_pitch;
+  t.V = V;
+  t.k = k;
+  t.parents = parents;
+  t.thr = thr;
+  if (grid > INT32_MAX) return cudaErrorInvalidValue;
+  return es == 2 ? launch(topk_threshold_kernel<2>, static_cast<int>(grid), kTkThreads, 0, st, true, t)
+                 : launch(topk_threshold_kernel<4>, static_cast<int>(grid), kTkThreads, 0, st, true, t);
 }
 
 RowSet row_set(const void* base, int64_t stride_elems, int64_t rows, int64_t V, int es) {
@@ -223,7 +256,7 @@ const char* spec_verify_status_string(sv_status s) {
 
 size_t spec_verify_greedy_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype) {
   Plan pl;
-  if (B < 0 || K < 0 || !make_plan(static_cast<int64_t>(B) * (K + 1), 0, B, V, elem_size(dtype), false, 0, &pl))
+  if (B < 0 || K < 0 || !make_plan(static_cast<int64_t>(B) * (K + 1), 0, B, V, elem_size(dtype), false, 0, 0, &pl))
     return 0;
   return pl.total;
 }
@@ -233,7 +266,7 @@ size_t spec_verify_sample_workspace_size(int32_t B, int32_t K, int32_t V, int32_
   Plan pl;
   const int64_t rd = has_draft_logits ? static_cast<int64_t>(B) * K : 0;
   if (B < 0 || K < 0 ||
-      !make_plan(static_cast<int64_t>(B) * (K + 1), rd, B, V, elem_size(dtype), true, 1, &pl))
+      !make_plan(static_cast<int64_t>(B) * (K + 1), rd, B, V, elem_size(dtype), true, 1, rd, &pl))
     return 0;
   return pl.total;
 }
@@ -241,7 +274,7 @@ size_t spec_verify_sample_workspace_size(int32_t B, int32_t K, int32_t V, int32_
 size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V, int32_t dtype) {
   Plan pl;
   if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES ||
-      !make_plan(static_cast<int64_t>(B) * N, 0, B, V, elem_size(dtype), true, N, &pl))
+      !make_plan(static_cast<int64_t>(B) * N, 0, B, V, elem_size(dtype), true, N, 0, &pl))
     return 0;
   return pl.total;
 }
@@ -262,7 +295,7 @@ sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t r
     return SV_ERR_INVALID_ARG;
   Plan pl;
   const int64_t rows = static_cast<int64_t>(B) * (K + 1);
-  if (!make_plan(rows, 0, B, V, es, false, 0, &pl)) return SV_ERR_INVALID_ARG;
+  if (!make_plan(rows, 0, B, V, es, false, 0, 0, &pl)) return SV_ERR_INVALID_ARG;
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = kLog2e;
@@ -306,7 +339,6 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   if (!valid_temperature(temperature)) return SV_ERR_INVALID_ARG;
   const sv_status rs = check_rule(rule);
   if (rs != SV_OK) return rs;
-  if (draft_logits && rule.rule != SV_RULE_EXACT) return SV_ERR_NOT_SUPPORTED;
   if (B == 0) return SV_OK;
   if (!target_logits || (K > 0 && !draft_tokens) || !uniforms || !out_tokens || !out_num_accepted ||
       !workspace)
@@ -318,7 +350,7 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   Plan pl;
   const int64_t rows_t = static_cast<int64_t>(B) * (K + 1);
   const int64_t rows_d = draft_logits ? static_cast<int64_t>(B) * K : 0;
-  if (!make_plan(rows_t, rows_d, B, V, es, true, 1, &pl)) return SV_ERR_INVALID_ARG;
+  if (!make_plan(rows_t, rows_d, B, V, es, true, 1, rows_d, &pl)) return SV_ERR_INVALID_ARG;
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = kLog2e / temperature;
@@ -344,6 +376,14 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   a.c = c;
   a.greedy = 0;
   a.rule = rule_args(rule);
+  if (a.rule.top_k > 0 && K > 0) {
+    float* thr = reinterpret_cast<float*>(w + pl.off_thr);
+    e = launch_topk(target_logits, row_stride * es, K, K + 1, V, a.rule.top_k, nullptr, thr, B * K, es, st);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    a.rule.thr = thr;
+  }
+  const bool mu_pass = draft_logits && a.rule.rule != SV_RULE_EXACT && K > 0;
+  a.mu_counters = mu_pass ? reinterpret_cast<uint32_t*>(w + pl.off_mucnt) : nullptr;
   a.out_tokens = out_tokens;
   a.out_num = out_num_accepted;
   a.out_logprob = out_logprob;
@@ -362,6 +402,32 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   const int grid3 = B * pl.P;
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
+  if (e != cudaSuccess || !mu_pass) return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  MuArgs m;
+  std::memset(&m, 0, sizeof(m));
+  m.tgt = a.tgt;
+  m.tgt_stride = a.tgt_stride;
+  m.dft = a.dft;
+  m.dft_stride = a.dft_stride;
+  m.drafts = draft_tokens;
+  m.B = B;
+  m.K = K;
+  m.V = V;
+  m.P = pl.P;
+  m.chunk_elems = pl.chunk_elems;
+  m.part = r.partials;
+  m.T = r.T;
+  m.G = r.G;
+  m.c = c;
+  m.rule = a.rule;
+  m.num = out_num_accepted;
+  m.tokens = out_tokens;
+  m.out_mu = out_mu;
+  m.mpart = reinterpret_cast<float2*>(w + pl.off_mupart);
+  m.counters = a.mu_counters;
+  const int grid_mu = B * K * pl.P;
+  e = es == 2 ? launch(mu_pass_kernel<2>, grid_mu, kMuThreads, 0, st, true, m)
+              : launch(mu_pass_kernel<4>, grid_mu, kMuThreads, 0, st, true, m);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -393,7 +459,7 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
     return SV_ERR_INVALID_ARG;
   Plan pl;
   const int64_t rows = static_cast<int64_t>(B) * N;
-  if (!make_plan(rows, 0, B, V, es, true, N, &pl)) return SV_ERR_INVALID_ARG;
+  if (!make_plan(rows, 0, B, V, es, true, N, 0, &pl)) return SV_ERR_INVALID_ARG;
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = greedy ? kLog2e : kLog2e / temperature;
@@ -418,6 +484,12 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
   a.c = c;
   a.greedy = greedy ? 1 : 0;
   a.rule = rule_args(rule);
+  if (!greedy && a.rule.top_k > 0) {
+    float* thr = reinterpret_cast<float*>(w + pl.off_thr);
+    e = launch_topk(target_logits, row_stride * es, N, N, V, a.rule.top_k, parents, thr, B * N, es, st);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    a.rule.thr = thr;
+  }
   a.out_tokens = out_tokens;
   a.out_nodes = out_nodes;
   a.out_num = out_num_accepted;

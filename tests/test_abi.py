@@ -110,8 +110,10 @@ def test_sample_host_validation(lib):
     assert _sample(lib, rule=(2, 0.0, 0, 0.0), draft=0) == SV_ERR_INVALID_ARG     # alpha <= 0
     assert _sample(lib, rule=(1, float("nan"), 0, 1.0), draft=0) == SV_ERR_INVALID_ARG
     assert _sample(lib, rule=(1, 0.1, 99, 1.0), draft=0) == SV_ERR_INVALID_ARG    # top_k > max
-    assert _sample(lib, rule=(1, 0.1, 2, 1.0), draft=0) == SV_ERR_NOT_SUPPORTED
-    assert _sample(lib, rule=(2, 0.0, 0, 0.3)) == SV_ERR_NOT_SUPPORTED            # power with q
+    # valid rule combinations pass validation and stop at the workspace check
+    assert _sample(lib, rule=(1, 0.1, 2, 1.0), draft=0, wsb=64) == SV_ERR_WORKSPACE_TOO_SMALL
+    assert _sample(lib, rule=(1, 0.1, 16, 1.0), wsb=64) == SV_ERR_WORKSPACE_TOO_SMALL
+    assert _sample(lib, rule=(2, 0.0, 0, 0.3), wsb=64) == SV_ERR_WORKSPACE_TOO_SMALL  # power with q
     assert _sample(lib, wsb=64) == SV_ERR_WORKSPACE_TOO_SMALL
 
 
