@@ -143,11 +143,12 @@ def _check_mu_frequencies(tokens_at, mus_at, runs):
     assert mass <= 1 + 1e-9
 
 
-@pytest.mark.parametrize("rule,alpha,tau", [(O.RULE_EXACT, 1.0, 0.0),
-                                            (O.RULE_POWER, 0.3, 0.0),
-                                            (O.RULE_RELAXED, 1.0, 0.15)])
-def test_mu_is_emission_probability_with_draft_logits(rule, alpha, tau):
-    rng = np.random.default_rng(5 + rule)
+@pytest.mark.parametrize("rule,alpha,tau,top_k", [(O.RULE_EXACT, 1.0, 0.0, 0),
+                                                  (O.RULE_POWER, 0.3, 0.0, 0),
+                                                  (O.RULE_RELAXED, 1.0, 0.15, 0),
+                                                  (O.RULE_RELAXED, 1.0, 0.3, 2)])
+def test_mu_is_emission_probability_with_draft_logits(rule, alpha, tau, top_k):
+    rng = np.random.default_rng(5 + rule + top_k)
     V, K, runs = 6, 2, 40000
     x = rng.normal(0, 1.5, (K + 1, V))
     y = x[:K] + rng.normal(0, 1.0, (K, V))
@@ -156,7 +157,7 @@ def test_mu_is_emission_probability_with_draft_logits(rule, alpha, tau):
     u = rng.random((runs, K + 1))
     out = O.verify_sample(np.broadcast_to(x, (runs, K + 1, V)),
                           np.broadcast_to(y, (runs, K, V)), d, 1.0, u,
-                          rule=rule, alpha=alpha, tau=tau)
+                          rule=rule, alpha=alpha, tau=tau, top_k=top_k)
     _check_mu_frequencies(out["tokens"][:, 0], out["mu"][:, 0], runs)
     later = out["num_accepted"] >= 1     # rows are context-free here
     _check_mu_frequencies(out["tokens"][later, 1], out["mu"][later, 1], int(later.sum()))
@@ -218,6 +219,19 @@ def test_relaxed_extremes():
     am = np.argmax(x[:, :4], axis=-1)
     tk = O.verify_sample(x, None, am, 1.0, u, rule=O.RULE_RELAXED, tau=2.0, top_k=1)
     assert (tk["num_accepted"] == 4).all() and (tk["mu"][:, :4] == 1.0).all()
+
+
+def test_relaxed_top_k_counts_strictly_greater_logits_with_ties():
+    # one row with repeated values; the draft at each token in turn, tau out of
+    # reach: accepted iff fewer than k logits are strictly above it
+    row = np.array([1.0, 3.0, 2.0, 3.0, 0.5, 2.0, 3.0])
+    greater = [5, 0, 3, 0, 6, 3, 0]   # logits strictly above row[t], counted by hand
+    for k in (1, 3, 4, 6, 7):
+        for t in range(row.size):
+            x = np.stack([row, row])[None]        # K = 1: row 0 tests the draft
+            out = O.verify_sample(x, None, np.array([[t]]), 1.0, np.array([[0.5, 0.5]]),
+                                  rule=O.RULE_RELAXED, tau=2.0, top_k=k)
+            assert int(out["num_accepted"][0]) == (1 if greater[t] < k else 0), (k, t)
 
 
 def test_perfect_draft_emits_k_plus_one():
