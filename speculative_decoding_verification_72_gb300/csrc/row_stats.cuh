@@ -13,9 +13,10 @@
 // vectors of each stage into a running (max, sum 2^((x - max) c)) and
 // remembers the group holding its first maximum. At the end of every row
 // piece the consumers resolve the exact argmax from a per-thread shared-memory
-// stash of that group (copied when the maximum rose), reduce (shuffles, then
-// a named barrier across the consumer warps) and write one Partial per
-// (CTA, row piece); the decide kernel merges a row's partials.
+// stash of that group (copied when the maximum rose) and reduce it within the
+// warp; the last warp to finish the piece merges the warps' results and
+// writes one Partial per (CTA, row piece), so no warp waits for another. The
+// decide kernel merges a row's partials.
 //
 // Copies cover the 16-byte-aligned hull of each row piece when it lies inside
 // the logit buffer, and elements outside the piece are masked in the first
@@ -50,6 +51,12 @@ constexpr int kK1RingBytes = kK1StageBytes * kK1Stages;
 constexpr int kK1StashBytes = kK1ConsumerThreads * kGroupVecs * 16;
 constexpr int kK1SmemBytes = kK1RingBytes + kK1StashBytes;
 constexpr int kK1MaxCtas = 4096;                      // bound used to size the workspace
+// Piece-result slots: warps of a CTA are at most kK1Stages pieces apart when
+// every piece has a copied stage, plus one piece per buffer edge handled by
+// scalar loads alone (two per row set, two row sets).
+constexpr int kK1RedBufs = 8;
+static_assert(kK1RedBufs >= kK1Stages + 5 && (kK1RedBufs & (kK1RedBufs - 1)) == 0, "piece-result ring");
+static_assert(kK1Consumers <= 8, "the piece merge reduces lanes 0..7");
 constexpr int kK1MinBytesPerCta = 16384;
 static_assert(kStageVecs == 2 * kGroupVecs, "a stage is folded as two groups per thread");
 
@@ -95,12 +102,14 @@ struct Piece {
   int tail_begin;           // scalar elements [tail_begin, j1)
 };
 
+// The piece of row `row` that starts at element j0 and ends at the row's end
+// or at flattened element e_end, whichever is first.
 template <int ES>
-__device__ __forceinline__ Piece make_piece(const RowStatsArgs& a, int64_t e, int64_t e_end) {
+__device__ __forceinline__ Piece make_piece(const RowStatsArgs& a, int row, int j0, int64_t e_end) {
   Piece p;
-  p.row = static_cast<int>(e / a.V);
-  p.j0 = static_cast<int>(e - static_cast<int64_t>(p.row) * a.V);
-  p.j1 = static_cast<int>(min(static_cast<int64_t>(a.V), e_end - static_cast<int64_t>(p.row) * a.V));
+  p.row = row;
+  p.j0 = j0;
+  p.j1 = static_cast<int>(min(static_cast<int64_t>(a.V), e_end - static_cast<int64_t>(row) * a.V));
   const bool first = p.row < a.set0.rows;
   const RowSet& rs = first ? a.set0 : a.set1;
   const int lr = first ? p.row : p.row - a.set0.rows;
@@ -365,22 +374,23 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full_bar[kK1Stages];
   __shared__ __align__(8) uint64_t empty_bar[kK1Stages];
-  __shared__ float red_m[2][kK1Consumers];
-  __shared__ float red_s[2][kK1Consumers];
-  __shared__ int red_i[2][kK1Consumers];
-  __shared__ int red_e[2][kK1Consumers];
+  __shared__ Partial red[kK1RedBufs][kK1Consumers];
+  __shared__ int red_cnt[kK1RedBufs];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
   const int64_t E0 = a.T * g / a.G;
   const int64_t E1 = a.T * (g + 1) / a.G;
+  const int row0 = static_cast<int>(E0 / a.V);   // the one division; pieces then step row by row
+  const int j00 = static_cast<int>(E0 - static_cast<int64_t>(row0) * a.V);
 
   // Inputs may come from the kernel before this one, and the partials this
   // kernel writes may still be read by the previous call: wait for it first.
   grid_dep_wait();
   grid_dep_launch();
 
+  if (tid < kK1RedBufs) red_cnt[tid] = 0;
   if (tid == 0) {
     for (int i = 0; i < kK1Stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
@@ -396,8 +406,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
       int st = 0, slot = 0;
       uint32_t phase = 0;   // parity of the current use of `slot`
       bool ok = true;
-      for (int64_t e = E0; e < E1 && ok;) {
-        const Piece p = make_piece<ES>(a, e, E1);
+      for (int row = row0, j0 = j00; E0 < E1 && ok; ++row, j0 = 0) {
+        const Piece p = make_piece<ES>(a, row, j0, E1);
         for (int s = 0; s < p.nst; ++s, ++st) {
           // the slot's previous use (parity phase ^ 1) must have been released
           if (st >= kK1Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) {
@@ -416,7 +426,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
             phase ^= 1;
           }
         }
-        e = static_cast<int64_t>(p.row) * a.V + p.j1;
+        if (static_cast<int64_t>(row) * a.V + p.j1 >= E1) break;
       }
       // The copies still in flight are the last (up to) kK1Stages issued; let
       // them land before the CTA can exit.
@@ -434,8 +444,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   int slot = 0, npiece = 0;
   uint32_t phase = 0;
   bool ok = true;
-  for (int64_t e = E0; e < E1; ++npiece) {
-    const Piece p = make_piece<ES>(a, e, E1);
+  for (int row = row0, j0 = j00; E0 < E1; ++npiece, ++row, j0 = 0) {
+    const Piece p = make_piece<ES>(a, row, j0, E1);
     float m = -INFINITY, mc = -INFINITY, s = 0.f;
     GroupCand cand;
     cand.stage = -1;
@@ -492,31 +502,52 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
 
-    // CTA: the consumer warps' results, double-buffered by piece parity so
-    // one named barrier per piece suffices.
-    const int buf = npiece & 1;
+    // CTA: each warp leaves its result in the piece's slot of a small ring
+    // and counts itself in; the last warp to arrive merges the slot (lanes
+    // 0..7, a fixed shuffle tree, so the result does not depend on which warp
+    // was last) and writes the Partial. No warp waits for another here.
+    const int buf = npiece & (kK1RedBufs - 1);
+    int merger = 0;
     if (lane == 0) {
-      red_m[buf][cw] = wm;
-      red_s[buf][cw] = ws;
-      red_i[buf][cw] = widx;
-      red_e[buf][cw] = ok ? 0 : 1;
+      Partial mine;
+      mine.m = wm;
+      mine.s = ws;
+      mine.idx = widx;
+      mine.err = ok ? 0 : 1;
+      red[buf][cw] = mine;
+      __threadfence_block();
+      merger = atomicAdd(&red_cnt[buf], 1) == kK1Consumers - 1;
     }
-    named_barrier_sync(1, kK1ConsumerThreads);
-    if (cw == 0 && lane == 0) {
-      float rm = red_m[buf][0], rs = red_s[buf][0];
-      int ri = red_i[buf][0], re = red_e[buf][0];
-      for (int w = 1; w < kK1Consumers; ++w) {
-        merge_stats(rm, rs, ri, red_m[buf][w], red_s[buf][w], red_i[buf][w], c);
-        re |= red_e[buf][w];
+    if (__shfl_sync(0xffffffffu, merger, 0)) {
+      __threadfence_block();
+      float rm = -INFINITY, rs = 0.f;
+      int ri = INT_MAX, re = 0;
+      if (lane < kK1Consumers) {
+        const Partial v = red[buf][lane];
+        rm = v.m;
+        rs = v.s;
+        ri = v.idx;
+        re = v.err;
       }
-      Partial out;
-      out.m = rm;
-      out.s = rs;
-      out.idx = ri;
-      out.err = re;
-      a.partials[static_cast<int64_t>(p.row) + g] = out;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, rm, o);
+        const float os = __shfl_xor_sync(0xffffffffu, rs, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ri, o);
+        re |= __shfl_xor_sync(0xffffffffu, re, o);
+        merge_stats(rm, rs, ri, om, os, oi, c);
+      }
+      if (lane == 0) {
+        atomicExch(&red_cnt[buf], 0);
+        Partial out;
+        out.m = rm;
+        out.s = rs;
+        out.idx = ri;
+        out.err = re;
+        a.partials[static_cast<int64_t>(p.row) + g] = out;
+      }
     }
-    e = static_cast<int64_t>(p.row) * a.V + p.j1;
+    if (static_cast<int64_t>(row) * a.V + p.j1 >= E1) break;
   }
 }
 
