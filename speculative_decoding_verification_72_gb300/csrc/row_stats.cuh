@@ -225,43 +225,52 @@ __device__ __forceinline__ float group_sum(const uint32_t (&w)[kGroupWords], flo
 
 constexpr int kStageFullVecs = kStageVecs * kK1ConsumerThreads;
 
-// One half (kGroupVecs vectors, 16 words) of a thread's share of a stage:
-// vectors v = ct + (4*h + k) * kK1ConsumerThreads. With EDGE, vectors past
-// nvec read as -inf and the two vectors that may hold bytes outside the piece
-// (mask_lo_v, mask_hi_v) are masked element by element.
-template <int ES, bool EDGE>
-__device__ __forceinline__ void load_half(const uint4* sv4, int ct, int h, int nvec, int jbase, int j0,
-                                          int j1, int mask_lo_v, int mask_hi_v,
-                                          uint32_t (&w)[kGroupWords]) {
+// Edge stages (the first and last of a piece whose copy hull reaches past the
+// piece, or a short last stage) are masked in place before the fold: each
+// thread rewrites only its own vectors v = ct + k * kK1ConsumerThreads, so no
+// other thread is involved. Vectors past nvec (not written by the copy) become
+// all -inf, and the vectors that may hold elements outside [j0, j1)
+// (mask_lo_v, mask_hi_v) get -inf in those elements. The fold then has a
+// single code path for every stage.
+template <int ES>
+__device__ __forceinline__ void mask_stage(uint4* sv4, int ct, int nvec, int jbase, int j0, int j1,
+                                           int mask_lo_v, int mask_hi_v) {
   constexpr int N = Elem<ES>::kVec;
   constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;   // -inf in every element
 #pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k) {
-    const int v = ct + (h * kGroupVecs + k) * kK1ConsumerThreads;
-    uint4 q;
-    if constexpr (EDGE) {
-      q = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
-      if (v < nvec) q = sv4[v];
-      if (v == mask_lo_v || v == mask_hi_v) {
-        uint32_t word[4] = {q.x, q.y, q.z, q.w};
-        const int jv = jbase + v * N;
+  for (int k = 0; k < kStageVecs; ++k) {
+    const int v = ct + k * kK1ConsumerThreads;
+    if (v >= nvec) {
+      sv4[v] = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
+    } else if (v == mask_lo_v || v == mask_hi_v) {
+      const uint4 q = sv4[v];
+      uint32_t word[4] = {q.x, q.y, q.z, q.w};
+      const int jv = jbase + v * N;
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-          if (jv + e < j0 || jv + e >= j1) {
-            if constexpr (ES == 2) {
-              const int wi = e >> 1;
-              word[wi] = (e & 1) ? ((word[wi] & 0x0000ffffu) | 0xff800000u)
-                                 : ((word[wi] & 0xffff0000u) | 0x0000ff80u);
-            } else {
-              word[e] = kNegInfWord;
-            }
+      for (int e = 0; e < N; ++e) {
+        if (jv + e < j0 || jv + e >= j1) {
+          if constexpr (ES == 2) {
+            const int wi = e >> 1;
+            word[wi] = (e & 1) ? ((word[wi] & 0x0000ffffu) | 0xff800000u)
+                               : ((word[wi] & 0xffff0000u) | 0x0000ff80u);
+          } else {
+            word[e] = kNegInfWord;
           }
         }
-        q = make_uint4(word[0], word[1], word[2], word[3]);
       }
-    } else {
-      q = sv4[v];
+      sv4[v] = make_uint4(word[0], word[1], word[2], word[3]);
     }
+  }
+  // These generic-proxy writes precede the next bulk copy into the slot.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One half (kGroupVecs vectors, 16 words) of a thread's share of a stage:
+// vectors v = ct + (4*h + k) * kK1ConsumerThreads.
+__device__ __forceinline__ void load_half(const uint4* sv4, int ct, int h, uint32_t (&w)[kGroupWords]) {
+#pragma unroll
+  for (int k = 0; k < kGroupVecs; ++k) {
+    const uint4 q = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
     w[4 * k] = q.x;
     w[4 * k + 1] = q.y;
     w[4 * k + 2] = q.z;
@@ -269,76 +278,56 @@ __device__ __forceinline__ void load_half(const uint4* sv4, int ct, int h, int n
   }
 }
 
-// Fold one stage (two halves) into (m, s). After the piece's first finite
-// stage the exponentials use the running maximum from before the stage, so
-// they do not wait on the stage's own maximum; the running sum is rescaled
-// once per stage when the maximum rises (both halves re-summed from shared
-// memory against the new maximum only if the rise could overflow). The argmax
-// keeps the half where the maximum first rose: stages and halves arrive in
-// increasing index order, so a strict '>' (and the lower half on a tie) keeps
-// the lowest index.
-// Record half h of this stage as the thread's candidate: its words (as
-// loaded, masked where needed) go to the thread's stash, vector k at
-// stash[k * kK1ConsumerThreads + ct].
-template <int ES, bool EDGE>
-__device__ __forceinline__ void stash_half(const uint4* sv4, uint4* stash, int ct, int h, int nvec,
-                                           int jbase, int j0, int j1, int mask_lo_v, int mask_hi_v,
-                                           int sg, GroupCand& cand) {
-  uint32_t w[kGroupWords];
-  load_half<ES, EDGE>(sv4, ct, h, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+// Record half h of this stage as the thread's candidate: its 16 words go to
+// the thread's stash, vector k at stash[k * kK1ConsumerThreads + ct].
+__device__ __forceinline__ void stash_half(const uint4* sv4, uint4* stash, int ct, int h, int jbase, int sg,
+                                           GroupCand& cand) {
 #pragma unroll
   for (int k = 0; k < kGroupVecs; ++k)
-    stash[k * kK1ConsumerThreads + ct] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    stash[k * kK1ConsumerThreads + ct] = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
   cand.stage = sg;
   cand.half = h;
   cand.jbase = jbase;
 }
 
-template <int ES, bool EDGE>
-__device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int nvec, int ct, int jbase,
-                                           int j0, int j1, int mask_lo_v, int mask_hi_v, int sg, float c,
-                                           float& m, float& mc, float& s, GroupCand& cand) {
+// Fold one stage (two halves) into (m, s). s is the sum of 2^(x c - mc) over
+// the elements folded so far; mc = m c once m is finite, and before that the
+// reference the piece started with (the previous piece's maximum, so the
+// first stage needs no second pass in the common case). The exponentials use
+// mc from before the stage, so they do not wait on the stage's own maximum.
+// When the maximum rises, the sum is moved to the new reference once; the
+// halves are re-summed against the new maximum from shared memory only if the
+// stage sum overflowed or the new maximum sat more than 2^20 below the old
+// reference (where flushed small terms could matter). The argmax keeps the
+// half where the maximum first rose: stages and halves arrive in increasing
+// index order, so a strict '>' (and the lower half on a tie) keeps the
+// lowest index.
+template <int ES>
+__device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int ct, int jbase, int sg,
+                                           float c, float& m, float& mc, float& s, GroupCand& cand) {
   uint32_t w[kGroupWords];
-  if (m == -INFINITY) {   // the maximum first, then the sums against it (one stage per piece)
-    load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
-    const float ga = group_max<ES>(w);
-    load_half<ES, EDGE>(sv4, ct, 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
-    const float gb = group_max<ES>(w);
-    const float gmax = fmaxf(ga, gb);
-    if (gmax > -INFINITY) {
-      mc = gmax * c;
-      s = group_sum<ES>(w, c, mc);
-      load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
-      s += group_sum<ES>(w, c, mc);
-      m = gmax;
-      stash_half<ES, EDGE>(sv4, stash, ct, ga >= gb ? 0 : 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, sg,
-                           cand);
-    }
-    return;
-  }
-  load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+  load_half(sv4, ct, 0, w);
   const float sa = group_sum<ES>(w, c, mc);
   const float ga = group_max<ES>(w);
-  load_half<ES, EDGE>(sv4, ct, 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+  load_half(sv4, ct, 1, w);
   const float sb = group_sum<ES>(w, c, mc);
   const float gb = group_max<ES>(w);
   const float gmax = fmaxf(ga, gb);
   const float gsum = sa + sb;
   if (gmax > m) {
-    const float d = (m - gmax) * c;
-    if (d > -100.f && gsum <= FLT_MAX) {
+    const float nmc = gmax * c;
+    const float d = mc - nmc;
+    if (gsum <= FLT_MAX && d <= 20.f) {
       s = (s + gsum) * ex2(d);
     } else {
-      const float nmc = gmax * c;
       float r = group_sum<ES>(w, c, nmc);
-      load_half<ES, EDGE>(sv4, ct, 0, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, w);
+      load_half(sv4, ct, 0, w);
       r += group_sum<ES>(w, c, nmc);
-      s = s * ex2(d) + r;
+      s = (m == -INFINITY ? 0.f : s * ex2(d)) + r;
     }
     m = gmax;
-    mc = gmax * c;
-    stash_half<ES, EDGE>(sv4, stash, ct, ga >= gb ? 0 : 1, nvec, jbase, j0, j1, mask_lo_v, mask_hi_v, sg,
-                         cand);
+    mc = nmc;
+    stash_half(sv4, stash, ct, ga >= gb ? 0 : 1, jbase, sg, cand);
   } else if (gmax > -INFINITY) {
     s += gsum;
   }
@@ -444,9 +433,10 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   int slot = 0, npiece = 0;
   uint32_t phase = 0;
   bool ok = true;
+  float ref = 0.f;   // exponent reference a piece starts from (log2 domain)
   for (int row = row0, j0 = j00; E0 < E1; ++npiece, ++row, j0 = 0) {
     const Piece p = make_piece<ES>(a, row, j0, E1);
-    float m = -INFINITY, mc = -INFINITY, s = 0.f;
+    float m = -INFINITY, mc = ref, s = 0.f;
     GroupCand cand;
     cand.stage = -1;
     cand.half = 0;
@@ -469,14 +459,13 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
         if (!mbar_wait_bounded(smem_u32(&full_bar[slot]), phase)) {
           ok = false;   // stop consuming (and releasing); the producer times out too
         } else {
-          const uint4* sv4 = reinterpret_cast<const uint4*>(ring + slot * kK1StageBytes);
+          uint4* sv4 = reinterpret_cast<uint4*>(ring + slot * kK1StageBytes);
           if ((sg == 0 && first_edge) || (sg == last && last_edge)) {
             const int nvec = sg == last ? last_nvec : kStageFullVecs;
-            fold_stage<ES, true>(sv4, stash, nvec, ct, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,
-                                 (sg == last && last_hull) ? nvec - 1 : -1, sg, c, m, mc, s, cand);
-          } else {
-            fold_stage<ES, false>(sv4, stash, kStageFullVecs, ct, jbase, 0, 0, -1, -1, sg, c, m, mc, s, cand);
+            mask_stage<ES>(sv4, ct, nvec, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,
+                           (sg == last && last_hull) ? nvec - 1 : -1);
           }
+          fold_stage<ES>(sv4, stash, ct, jbase, sg, c, m, mc, s, cand);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
         }
@@ -489,6 +478,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
     }
     for (int j = p.tail_begin + ct; j < p.j1; j += kK1ConsumerThreads)
       fold_scalar(Elem<ES>::load(p.rowp, j), j, c, m, mc, s, cand);
+    if (m > -INFINITY) ref = mc;
 
     // Warp: max, the lowest index among lanes holding it, and the sum
     // rescaled to the warp max (fixed shuffle order).
