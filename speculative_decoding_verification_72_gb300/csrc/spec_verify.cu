@@ -88,17 +88,22 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
   return true;
 }
 
-// K1 grid for this device: kK1CtasPerSm per SM, fewer for small problems.
-int k1_grid(int64_t T, int es) {
-  static int sm_count[64] = {0};
+// SM count of the current device (looked up once per device).
+int sm_count() {
+  static int count[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (sm_count[dev] == 0) {
+  if (count[dev] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    sm_count[dev] = n;
+    count[dev] = n;
   }
-  int64_t g = static_cast<int64_t>(sm_count[dev]) * kK1CtasPerSm;
+  return count[dev];
+}
+
+// K1 grid for this device: kK1CtasPerSm per SM, fewer for small problems.
+int k1_grid(int64_t T, int es) {
+  int64_t g = static_cast<int64_t>(sm_count()) * kK1CtasPerSm;
   const int64_t by_size = (T * es + kK1MinBytesPerCta - 1) / kK1MinBytesPerCta;
   if (by_size < g) g = by_size;
   if (g > kK1MaxCtas) g = kK1MaxCtas;
@@ -207,7 +212,7 @@ RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride,
   return r;
 }
 
-DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride_b, const void* dft,
+DrawArgs draw_args(const Plan& pl, int es, const void* tgt, int64_t tgt_stride_b, const void* dft,
                    int64_t dft_stride_b, int32_t V, float c, void* ws, int32_t out_cols,
                    int32_t* out_tokens, float* out_logprob, float* out_mu) {
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -219,6 +224,8 @@ DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride_b, const 
   d.V = V;
   d.P = pl.P;
   d.chunk_elems = pl.chunk_elems;
+  const int cpc = es == 2 ? kK3Cpc<2> : kK3Cpc<4>;
+  d.Q = (pl.P + cpc - 1) / cpc;
   d.c = c;
   d.draws = reinterpret_cast<const DrawDesc*>(w + pl.off_draw);
   d.excl = reinterpret_cast<const int32_t*>(w + pl.off_excl);
@@ -396,10 +403,10 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
               : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  const DrawArgs d = draw_args(pl, target_logits, row_stride * es, draft_logits,
+  const DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, draft_logits,
                                draft_logits ? draft_row_stride * es : 0, V, c, workspace, K + 1,
                                out_tokens, out_logprob, out_mu);
-  const int grid3 = B * pl.P;
+  const int grid3 = B * d.Q;
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
   if (e != cudaSuccess || !mu_pass) return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
@@ -504,9 +511,9 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
               : launch(tree_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   if (greedy) return SV_OK;
-  const DrawArgs d = draw_args(pl, target_logits, row_stride * es, nullptr, 0, V, c, workspace,
+  const DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, nullptr, 0, V, c, workspace,
                                max_depth + 1, out_tokens, out_logprob, out_mu);
-  const int grid3 = B * pl.P;
+  const int grid3 = B * d.Q;
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
