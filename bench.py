@@ -60,6 +60,10 @@ CONFIGS = {
     "eagle_tree_relaxed": dict(kind="tree", B=32, N=64, V=128256, dtype="bf16", T=1.0, rule=1, tau=0.1,
                                seed=7203, workload="EAGLE-3 tree verify (relaxed rule tau=0.1, T=1), "
                                                    "64 nodes, V=128256 bf16, B=32"),
+    "llama_greedy_finish": dict(kind="greedy", B=32, K=5, V=128256, dtype="bf16", p_match=0.8, seed=7201,
+                                finish=True,
+                                workload="greedy chain verify with the finish step: V=128256 bf16, K=5, B=32, "
+                                         "a 2-id stop set, per-request max_new in [1, 6], running counters"),
     "long_chain": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
                        workload="long-chain greedy verify: GPT-2 vocab V=50257 bf16, B=8, K+1=4096 rows "
                                 "per request, drafts = argmax w.p. 0.95"),
@@ -95,8 +99,9 @@ def aggregate(elapsed_ms_max, rows_per_step, steps, world):
 # Sources of the kernels one call of each workload kind launches; the entry
 # point file (launch shapes) is in every set.
 _CALL_SOURCES = {
-    "greedy": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "spec_verify.cu"),
-    "draw": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "draw.cuh", "spec_verify.cu"),
+    "greedy": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "spec_verify.cu"),
+    "draw": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "draw.cuh", "rules.cuh",
+             "spec_verify.cu"),
 }
 
 
@@ -225,8 +230,15 @@ def make_inputs(cfg, seed, device):
     from speculative_decoding_verification_72_gb300 import workloads as W
     dt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
     if cfg["kind"] == "greedy":
-        return W.greedy_chain(B=cfg["B"], K=cfg["K"], V=cfg["V"], dtype=dt, p_match=cfg["p_match"],
-                              seed=seed, device=device)
+        x = W.greedy_chain(B=cfg["B"], K=cfg["K"], V=cfg["V"], dtype=dt, p_match=cfg["p_match"],
+                           seed=seed, device=device)
+        if cfg.get("finish"):   # device-resident finish inputs, so a captured call copies nothing
+            g = torch.Generator(device="cpu").manual_seed(seed)
+            x.stop_ids = torch.randint(0, cfg["V"], (2,), generator=g).to(device=device, dtype=torch.int32)
+            x.max_new = torch.randint(1, cfg["K"] + 2, (cfg["B"],), generator=g).to(device=device,
+                                                                                 dtype=torch.int32)
+            x.counters = torch.zeros((cfg["B"], 4), dtype=torch.int64, device=device)
+        return x
     if cfg["kind"] == "sample":
         return W.stochastic_chain(B=cfg["B"], K=cfg["K"], V=cfg["V"], dtype=dt, seed=seed, device=device)
     return W.eagle_tree(B=cfg["B"], V=cfg["V"], n_nodes=cfg["N"], dtype=dt, seed=seed, device=device)
@@ -235,6 +247,9 @@ def make_inputs(cfg, seed, device):
 def call(cfg, x, out=None, ws=None):
     import speculative_decoding_verification_72_gb300 as sv
     if cfg["kind"] == "greedy":
+        if cfg.get("finish"):
+            return sv.spec_verify_greedy(x.target, x.draft_tokens, workspace=ws, out=out, stop_ids=x.stop_ids,
+                                         max_new=x.max_new, counters=x.counters)
         return sv.spec_verify_greedy(x.target, x.draft_tokens, workspace=ws, out=out)
     if cfg["kind"] == "sample":
         return sv.spec_verify_sample(x.target, x.draft_tokens, x.uniforms, draft_logits=x.draft_logits,
@@ -483,7 +498,8 @@ def _e2e(cfg, x, dev, steps, out, ws):
     """Same metric through the public API with host buffers: every step copies
     that step's inputs from pinned host memory and reads the results back."""
     import torch
-    names = [k for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents")
+    names = [k for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents",
+                         "stop_ids", "max_new")
              if getattr(x, k, None) is not None]
     host = {k: getattr(x, k).cpu().pin_memory() for k in names}
     devb = {k: torch.empty_like(getattr(x, k)) for k in names}
@@ -496,9 +512,11 @@ def _e2e(cfg, x, dev, steps, out, ws):
         pass
 
     inp = Inp()
-    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents"):
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents",
+              "stop_ids", "max_new"):
         setattr(inp, k, devb.get(k))
     inp.max_depth = getattr(x, "max_depth", None)
+    inp.counters = getattr(x, "counters", None)   # running totals stay on the device
 
     def one():
         for k in names:

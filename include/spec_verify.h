@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 1
+#define SPEC_VERIFY_ABI_VERSION 2
 
 /* Return codes. */
 typedef int32_t sv_status;
@@ -85,6 +85,8 @@ typedef int32_t sv_status;
 #define SV_STATUS_ZERO_MASS      8   /* a draft token with p(t) = q(t) = 0 (rejected) */
 #define SV_STATUS_DEPTH_EXCEEDED 16  /* the walk reached max_depth at a node with children */
 #define SV_STATUS_TIMEOUT        32  /* a bounded wait in a kernel gave up */
+#define SV_STATUS_STOPPED        64  /* finish step: a stop token ended the request */
+#define SV_STATUS_CAPPED         128 /* finish step: max_new removed emitted tokens */
 
 /* Rule parameters. tau: relaxed threshold on p. top_k: relaxed rank bound
  * (0 disables it; rank = number of logits strictly greater, so top_k = 1
@@ -96,6 +98,29 @@ typedef struct sv_rule_params {
   int32_t top_k;
   float alpha;
 } sv_rule_params;
+
+/* Optional finish step of the *_ex entry points (mini-sglang PR #134: Known
+ * limitations, multi-token stop sets, and engine.py's accept_length /
+ * accept_rate counters; spec-decode README CLI: tokens per target pass and
+ * acceptance rate). A call emits tokens[0..n]; the request stops at the first
+ * emitted token in stop_ids (that token is kept); max_new[b] (clamped at 0)
+ * caps the tokens kept; positions kept..n are cleared (token -1, log-prob 0,
+ * mu 0, tree node -1) and out_len[b] = kept. num_accepted still reports the
+ * rule's n. counters[b] (int64, 4 per request, running totals owned by the
+ * caller) gain (1 round, drafts offered = K or max_depth, n, kept): tokens
+ * per pass = counters[3] / counters[0], acceptance rate = counters[2] /
+ * counters[1]. All pointers are device memory; stop_ids may be NULL when
+ * n_stop = 0, max_new and counters may be NULL; out_len is required. The
+ * step runs inside the call's last kernel; two calls on the same counters
+ * must not overlap on the GPU. */
+#define SV_MAX_STOP_IDS 16
+typedef struct sv_finish_params {
+  const int32_t* stop_ids;   /* [n_stop] token ids */
+  int32_t n_stop;            /* 0 .. SV_MAX_STOP_IDS */
+  const int32_t* max_new;    /* [B] tokens each request may still emit, or NULL */
+  int32_t* out_len;          /* [B] tokens kept */
+  int64_t* counters;         /* [B, 4] running totals, or NULL */
+} sv_finish_params;
 
 /* Largest top_k the relaxed rule supports. */
 #define SV_MAX_TOP_K 16
@@ -197,6 +222,33 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
                            int32_t* out_tokens, int32_t* out_nodes, int32_t* out_num_accepted,
                            float* out_logprob, float* out_mu, int32_t* out_status,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* The three entry points above with the finish step (sv_finish_params);
+ * finish = NULL behaves exactly like the plain call. Invalid finish
+ * parameters (out_len NULL, n_stop outside 0..SV_MAX_STOP_IDS, stop_ids NULL
+ * with n_stop > 0, misaligned pointers) return SV_ERR_INVALID_ARG. */
+sv_status spec_verify_greedy_ex(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                int32_t* out_tokens, int32_t* out_num_accepted,
+                                float* out_logprob, float* out_mu, int32_t* out_status,
+                                const sv_finish_params* finish,
+                                void* workspace, size_t workspace_bytes, void* stream);
+sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                const void* draft_logits, int64_t draft_row_stride,
+                                const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                float temperature, const float* uniforms, sv_rule_params rule,
+                                int32_t* out_tokens, int32_t* out_num_accepted,
+                                float* out_logprob, float* out_mu, int32_t* out_status,
+                                const sv_finish_params* finish,
+                                void* workspace, size_t workspace_bytes, void* stream);
+sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t row_stride,
+                              const int32_t* node_tokens, const int32_t* parents,
+                              int32_t B, int32_t N, int32_t V, int32_t max_depth,
+                              float temperature, const float* uniforms, sv_rule_params rule,
+                              int32_t* out_tokens, int32_t* out_nodes, int32_t* out_num_accepted,
+                              float* out_logprob, float* out_mu, int32_t* out_status,
+                              const sv_finish_params* finish,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of the library's static scratch array used by
  * spec_verify_greedy_static (one array per GPU that loads the library). */

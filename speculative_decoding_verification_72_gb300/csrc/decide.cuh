@@ -25,6 +25,7 @@
 //   configuration), with rest / branch probabilities in double.
 #pragma once
 
+#include "finish.cuh"
 #include "row_stats.cuh"
 
 namespace sv {
@@ -72,6 +73,7 @@ struct ChainArgs {
   int32_t excl_stride;
   uint32_t* draw_counters;  // [B], zeroed here for K3's tickets
   uint32_t* mu_counters;    // [B], zeroed here for the mu pass's tickets (or nullptr)
+  FinishArgs fin;           // stop / cap / counters (greedy: applied here)
 };
 
 // Inputs of one chain position, readable before K1 completes.
@@ -115,6 +117,7 @@ template <int ES>
 __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArgs a) {
   __shared__ int s_first;
   __shared__ int s_status;
+  __shared__ int s_fin;
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int K = a.K, R = a.K + 1;
@@ -262,6 +265,10 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     a.out_num[b] = n;
     if (a.out_status) a.out_status[b] = s_status;
   }
+  if (a.greedy && a.fin.out_len) {   // greedy: this kernel ends the call
+    __syncthreads();
+    finish_request(a.fin, b, n, R, a.out_tokens, a.out_logprob, a.out_mu, nullptr, a.out_status, &s_fin);
+  }
 }
 
 struct TreeArgs {
@@ -287,6 +294,7 @@ struct TreeArgs {
   int32_t* excl;
   int32_t excl_stride;
   uint32_t* draw_counters;
+  FinishArgs fin;          // stop / cap / counters (greedy walk: applied here)
 };
 
 template <int ES>
@@ -302,6 +310,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   __shared__ int sm_next[kMaxTreeNodes];    // next sibling
   __shared__ unsigned char sm_bad[kMaxTreeNodes];  // row not finite / timed out
   __shared__ int s_status;
+  __shared__ int s_n, s_fin;
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -447,6 +456,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
       break;
     }
     a.out_num[b] = depth;
+    s_n = depth;
     for (int j = depth + 1; j < W; ++j) {
       a.out_tokens[ob + j] = -1;
       a.out_nodes[ob + j] = -1;
@@ -457,6 +467,10 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   }
   __syncthreads();
   if (tid == 0 && a.out_status) a.out_status[b] = s_status;
+  if (a.greedy && a.fin.out_len) {   // greedy walk: this kernel ends the call
+    __syncthreads();
+    finish_request(a.fin, b, s_n, W, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes, a.out_status, &s_fin);
+  }
 }
 
 }  // namespace sv

@@ -18,6 +18,7 @@
 // same code in both passes.
 #pragma once
 
+#include "finish.cuh"
 #include "sv_common.cuh"
 
 namespace sv {
@@ -57,6 +58,10 @@ struct DrawArgs {
   int32_t* out_tokens;
   float* out_logprob;
   float* out_mu;
+  int32_t* out_nodes;    // tree calls, else nullptr
+  int32_t* out_status;
+  FinishArgs fin;        // applied by the last CTA of a request when fin_here
+  int32_t fin_here;
 };
 
 template <int ES>
@@ -316,6 +321,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   __shared__ float s_thr;
   __shared__ double s_S;
   __shared__ float2 s_part[kK3MaxChunks];
+  __shared__ int s_fin;
 
   const int tid = threadIdx.x;
   const int b = blockIdx.x / a.Q;
@@ -493,6 +499,11 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
       if (d.type == kDrawMaskedP) mu = static_cast<float>(static_cast<double>(d.scale) * p / s_S);
       a.out_mu[o] = mu;
     }
+  }
+  if (a.fin_here) {   // no mu pass follows: this kernel ends the call
+    __syncthreads();
+    finish_request(a.fin, b, d.pos, a.out_cols, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes, a.out_status,
+                   &s_fin);
   }
 }
 

@@ -183,6 +183,10 @@ struct MuArgs {
   const int32_t* num;      // n per request (decide kernel)
   const int32_t* tokens;   // [B, K+1]: the draw at position n (draw kernel)
   float* out_mu;           // [B, K+1]
+  int32_t* out_tokens;     // [B, K+1] (the same array as tokens; cleared by the finish step)
+  float* out_logprob;
+  int32_t* out_status;
+  FinishArgs fin;          // stop / cap / counters, applied by the last CTA of a request
   float2* mpart;           // [B * K * P]: (sum q acc, sum relu(p - q))
   uint32_t* counters;      // [B], zeroed by the decide kernel of the same call
 };
@@ -211,7 +215,7 @@ template <int ES>
 __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
   __shared__ float red[kMuThreads / 32];
   __shared__ float s_lp2, s_lq2;
-  __shared__ int s_last;
+  __shared__ int s_last, s_fin;
   grid_dep_wait();
   grid_dep_launch();
   const int tid = threadIdx.x;
@@ -277,6 +281,10 @@ __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
     if (a.out_mu) a.out_mu[o] = static_cast<float>(mu);
   }
   if (tid == 0) a.counters[b] = 0u;
+  if (a.fin.out_len) {   // this kernel ends the call
+    __syncthreads();
+    finish_request(a.fin, b, n, a.K + 1, a.out_tokens, a.out_logprob, a.out_mu, nullptr, a.out_status, &s_fin);
+  }
 }
 
 }  // namespace sv

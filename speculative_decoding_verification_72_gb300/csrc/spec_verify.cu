@@ -236,7 +236,27 @@ DrawArgs draw_args(const Plan& pl, int es, const void* tgt, int64_t tgt_stride_b
   d.out_tokens = out_tokens;
   d.out_logprob = out_logprob;
   d.out_mu = out_mu;
+  d.out_nodes = nullptr;
+  d.out_status = nullptr;
+  std::memset(&d.fin, 0, sizeof(d.fin));
+  d.fin_here = 0;
   return d;
+}
+
+// Finish-step arguments of a call (disabled when fin is null).
+sv_status finish_args(const sv_finish_params* fin, int32_t offered, FinishArgs* f) {
+  std::memset(f, 0, sizeof(*f));
+  if (!fin) return SV_OK;
+  if (!fin->out_len || !aligned(fin->out_len, 4)) return SV_ERR_INVALID_ARG;
+  if (fin->n_stop < 0 || fin->n_stop > SV_MAX_STOP_IDS || (fin->n_stop > 0 && !fin->stop_ids)) return SV_ERR_INVALID_ARG;
+  if (!aligned(fin->stop_ids, 4) || !aligned(fin->max_new, 4) || !aligned(fin->counters, 8)) return SV_ERR_INVALID_ARG;
+  f->stop_ids = fin->stop_ids;
+  f->n_stop = fin->n_stop;
+  f->max_new = fin->max_new;
+  f->out_len = fin->out_len;
+  f->counters = reinterpret_cast<long long*>(fin->counters);
+  f->offered = offered;
+  return SV_OK;
 }
 
 bool outputs_aligned(const void* a, const void* b, const void* c, const void* d, const void* e) {
@@ -291,9 +311,21 @@ sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t r
                              int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
                              float* out_mu, int32_t* out_status, void* workspace,
                              size_t workspace_bytes, void* stream) {
+  return spec_verify_greedy_ex(target_logits, dtype, row_stride, draft_tokens, B, K, V, out_tokens,
+                               out_num_accepted, out_logprob, out_mu, out_status, nullptr, workspace,
+                               workspace_bytes, stream);
+}
+
+sv_status spec_verify_greedy_ex(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
+                                float* out_mu, int32_t* out_status, const sv_finish_params* finish,
+                                void* workspace, size_t workspace_bytes, void* stream) {
   const int es = elem_size(dtype);
   if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
   if (B < 0 || K < 0 || V < 1 || row_stride < V) return SV_ERR_INVALID_ARG;
+  FinishArgs fa;
+  if (finish_args(finish, K, &fa) != SV_OK) return SV_ERR_INVALID_ARG;
   if (B == 0) return SV_OK;
   if (!target_logits || (K > 0 && !draft_tokens) || !out_tokens || !out_num_accepted || !workspace)
     return SV_ERR_INVALID_ARG;
@@ -322,6 +354,7 @@ sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t r
   a.G = r.G;
   a.c = c;
   a.greedy = 1;
+  a.fin = fa;
   a.out_tokens = out_tokens;
   a.out_num = out_num_accepted;
   a.out_logprob = out_logprob;
@@ -339,8 +372,23 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
                              int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
                              float* out_mu, int32_t* out_status, void* workspace,
                              size_t workspace_bytes, void* stream) {
+  return spec_verify_sample_ex(target_logits, dtype, row_stride, draft_logits, draft_row_stride,
+                               draft_tokens, B, K, V, temperature, uniforms, rule, out_tokens,
+                               out_num_accepted, out_logprob, out_mu, out_status, nullptr, workspace,
+                               workspace_bytes, stream);
+}
+
+sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                const void* draft_logits, int64_t draft_row_stride,
+                                const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                float temperature, const float* uniforms, sv_rule_params rule,
+                                int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
+                                float* out_mu, int32_t* out_status, const sv_finish_params* finish,
+                                void* workspace, size_t workspace_bytes, void* stream) {
   const int es = elem_size(dtype);
   if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  FinishArgs fa;
+  if (finish_args(finish, K, &fa) != SV_OK) return SV_ERR_INVALID_ARG;
   if (B < 0 || K < 0 || V < 1 || row_stride < V) return SV_ERR_INVALID_ARG;
   if (draft_logits && draft_row_stride < V) return SV_ERR_INVALID_ARG;
   if (!valid_temperature(temperature)) return SV_ERR_INVALID_ARG;
@@ -403,9 +451,12 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
               : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  const DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, draft_logits,
-                               draft_logits ? draft_row_stride * es : 0, V, c, workspace, K + 1,
-                               out_tokens, out_logprob, out_mu);
+  DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, draft_logits,
+                         draft_logits ? draft_row_stride * es : 0, V, c, workspace, K + 1,
+                         out_tokens, out_logprob, out_mu);
+  d.out_status = out_status;
+  d.fin = fa;
+  d.fin_here = (fa.out_len && !mu_pass) ? 1 : 0;
   const int grid3 = B * d.Q;
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
@@ -430,6 +481,10 @@ sv_status spec_verify_sample(const void* target_logits, int32_t dtype, int64_t r
   m.num = out_num_accepted;
   m.tokens = out_tokens;
   m.out_mu = out_mu;
+  m.out_tokens = out_tokens;
+  m.out_logprob = out_logprob;
+  m.out_status = out_status;
+  m.fin = fa;
   m.mpart = reinterpret_cast<float2*>(w + pl.off_mupart);
   m.counters = a.mu_counters;
   const int grid_mu = B * K * pl.P;
@@ -445,8 +500,22 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
                            int32_t* out_nodes, int32_t* out_num_accepted, float* out_logprob,
                            float* out_mu, int32_t* out_status, void* workspace,
                            size_t workspace_bytes, void* stream) {
+  return spec_verify_tree_ex(target_logits, dtype, row_stride, node_tokens, parents, B, N, V, max_depth,
+                             temperature, uniforms, rule, out_tokens, out_nodes, out_num_accepted,
+                             out_logprob, out_mu, out_status, nullptr, workspace, workspace_bytes, stream);
+}
+
+sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t row_stride,
+                              const int32_t* node_tokens, const int32_t* parents, int32_t B,
+                              int32_t N, int32_t V, int32_t max_depth, float temperature,
+                              const float* uniforms, sv_rule_params rule, int32_t* out_tokens,
+                              int32_t* out_nodes, int32_t* out_num_accepted, float* out_logprob,
+                              float* out_mu, int32_t* out_status, const sv_finish_params* finish,
+                              void* workspace, size_t workspace_bytes, void* stream) {
   const int es = elem_size(dtype);
   if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  FinishArgs fa;
+  if (finish_args(finish, max_depth, &fa) != SV_OK) return SV_ERR_INVALID_ARG;
   if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || row_stride < V || max_depth < 0 ||
       max_depth > INT32_MAX - 1)
     return SV_ERR_INVALID_ARG;
@@ -490,6 +559,7 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
   a.G = r.G;
   a.c = c;
   a.greedy = greedy ? 1 : 0;
+  a.fin = fa;
   a.rule = rule_args(rule);
   if (!greedy && a.rule.top_k > 0) {
     float* thr = reinterpret_cast<float*>(w + pl.off_thr);
@@ -511,8 +581,12 @@ sv_status spec_verify_tree(const void* target_logits, int32_t dtype, int64_t row
               : launch(tree_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   if (greedy) return SV_OK;
-  const DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, nullptr, 0, V, c, workspace,
-                               max_depth + 1, out_tokens, out_logprob, out_mu);
+  DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, nullptr, 0, V, c, workspace,
+                         max_depth + 1, out_tokens, out_logprob, out_mu);
+  d.out_nodes = out_nodes;
+  d.out_status = out_status;
+  d.fin = fa;
+  d.fin_here = fa.out_len ? 1 : 0;
   const int grid3 = B * d.Q;
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);

@@ -44,6 +44,12 @@ class RuleParams(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("alpha", ctypes.c_float)]
 
 
+class FinishParams(ctypes.Structure):
+    _fields_ = [("stop_ids", ctypes.c_void_p), ("n_stop", ctypes.c_int32),
+                ("max_new", ctypes.c_void_p), ("out_len", ctypes.c_void_p),
+                ("counters", ctypes.c_void_p)]
+
+
 def library_path():
     return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libspecverify.so")
 
@@ -70,6 +76,14 @@ _SIGS = {
                                 _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_greedy_static": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                          _P, _P, _P, _P, _P, _P]),
+    "spec_verify_greedy_ex": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
+                                     _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_sample_ex": (_I32, [_P, _I32, _I64, _P, _I64, _P, _I32, _I32, _I32,
+                                     _F, _P, RuleParams,
+                                     _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_verify_tree_ex": (_I32, [_P, _I32, _I64, _P, _P, _I32, _I32, _I32, _I32,
+                                   _F, _P, RuleParams,
+                                   _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
 }
 
 
@@ -130,8 +144,12 @@ def _rows_view(t, name):
 
 
 def _i32(t, name, shape, device):
+    """int32 contiguous copy on `device`; shape None = any 1-D length."""
     if not isinstance(t, torch.Tensor):
-        t = torch.as_tensor(t)
+        t = torch.as_tensor(t, dtype=torch.int64)
+    if shape is None:
+        shape = (t.numel(),)
+        t = t.reshape(-1)
     if tuple(t.shape) != tuple(shape):
         raise SpecVerifyError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t.to(device=device, dtype=torch.int32).contiguous()
@@ -194,12 +212,34 @@ def _rule(rule, tau, top_k, alpha):
     return RuleParams(int(rule), float(tau), int(top_k), float(alpha))
 
 
-def spec_verify_greedy(target_logits, draft_tokens, workspace=None, out=None):
+def _finish(B, dev, out, stop_ids, max_new, counters):
+    """(FinishParams pointer, tensors kept alive) when a finish option is
+    given, else (None, None). Adds out["out_len"]."""
+    if stop_ids is None and max_new is None and counters is None:
+        return None, None
+    stop = _i32(stop_ids if stop_ids is not None else [], "stop_ids", None, dev)
+    cap = _i32(max_new, "max_new", (B,), dev) if max_new is not None else None
+    if counters is not None:
+        if (not isinstance(counters, torch.Tensor) or counters.dtype != torch.int64 or
+                tuple(counters.shape) != (B, 4) or not counters.is_contiguous() or counters.device != dev):
+            raise SpecVerifyError(f"counters must be a contiguous int64 ({B}, 4) tensor on {dev}")
+    if out.get("out_len") is None:
+        out["out_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
+    fp = FinishParams(_ptr(stop) if stop.numel() else None, int(stop.numel()),
+                      _ptr(cap) if cap is not None else None, _ptr(out["out_len"]),
+                      _ptr(counters) if counters is not None else None)
+    return ctypes.byref(fp), (fp, stop, cap)
+
+
+def spec_verify_greedy(target_logits, draft_tokens, workspace=None, out=None,
+                       stop_ids=None, max_new=None, counters=None):
     """Greedy chain verification. target_logits [B, K+1, V] (bf16 / fp32,
     CUDA), draft_tokens [B, K]. Returns a dict of CUDA tensors: tokens,
     num_accepted, logprob, mu, status (the caller's `out` dict if given;
     with `out` and `workspace` given the call allocates nothing and can be
-    captured in a CUDA graph)."""
+    captured in a CUDA graph). stop_ids / max_new [B] / counters (int64
+    [B, 4], updated in place) select the finish step of include/spec_verify.h
+    and add out["out_len"]."""
     lib = load_library()
     x, stride = _rows_view(target_logits, "target_logits")
     B, R, V = x.shape
@@ -212,18 +252,20 @@ def spec_verify_greedy(target_logits, draft_tokens, workspace=None, out=None):
     if need == 0 and B > 0:
         raise SpecVerifyError("invalid sizes")
     ws = _ws(workspace, need, dev, stream)
-    rc = lib.spec_verify_greedy(_ptr(x), _dtype_code(x), stride, _ptr(d), B, K, V,
-                                _ptr(out["tokens"]), _ptr(out["num_accepted"]),
-                                _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
-                                _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+    fin, _keep = _finish(B, dev, out, stop_ids, max_new, counters)
+    rc = lib.spec_verify_greedy_ex(_ptr(x), _dtype_code(x), stride, _ptr(d), B, K, V,
+                                   _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                   _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]), fin,
+                                   _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out
 
 
 def spec_verify_sample(target_logits, draft_tokens, uniforms, draft_logits=None,
                        temperature=1.0, rule=RULE_EXACT, tau=0.0, top_k=0, alpha=1.0,
-                       workspace=None, out=None):
-    """Stochastic chain verification (see include/spec_verify.h)."""
+                       workspace=None, out=None, stop_ids=None, max_new=None, counters=None):
+    """Stochastic chain verification (see include/spec_verify.h); finish
+    options as for spec_verify_greedy."""
     lib = load_library()
     x, stride = _rows_view(target_logits, "target_logits")
     B, R, V = x.shape
@@ -242,20 +284,22 @@ def spec_verify_sample(target_logits, draft_tokens, uniforms, draft_logits=None,
     stream = torch.cuda.current_stream(dev).cuda_stream
     need = lib.spec_verify_sample_workspace_size(B, K, V, _dtype_code(x), int(y is not None))
     ws = _ws(workspace, need, dev, stream)
-    rc = lib.spec_verify_sample(_ptr(x), _dtype_code(x), stride, _ptr(y), dstride, _ptr(d),
-                                B, K, V, float(temperature), _ptr(u),
-                                _rule(rule, tau, top_k, alpha),
-                                _ptr(out["tokens"]), _ptr(out["num_accepted"]),
-                                _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
-                                _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+    fin, _keep = _finish(B, dev, out, stop_ids, max_new, counters)
+    rc = lib.spec_verify_sample_ex(_ptr(x), _dtype_code(x), stride, _ptr(y), dstride, _ptr(d),
+                                   B, K, V, float(temperature), _ptr(u),
+                                   _rule(rule, tau, top_k, alpha),
+                                   _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                   _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]), fin,
+                                   _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out
 
 
 def spec_verify_tree(target_logits, node_tokens, parents, max_depth, temperature=0.0,
                      uniforms=None, rule=RULE_EXACT, tau=0.0, top_k=0, alpha=1.0,
-                     workspace=None, out=None):
-    """Tree verification (see include/spec_verify.h). temperature 0 = greedy."""
+                     workspace=None, out=None, stop_ids=None, max_new=None, counters=None):
+    """Tree verification (see include/spec_verify.h). temperature 0 = greedy;
+    finish options as for spec_verify_greedy."""
     lib = load_library()
     x, stride = _rows_view(target_logits, "target_logits")
     B, N, V = x.shape
@@ -272,11 +316,12 @@ def spec_verify_tree(target_logits, node_tokens, parents, max_depth, temperature
     if need == 0 and B > 0:
         raise SpecVerifyError("invalid sizes")
     ws = _ws(workspace, need, dev, stream)
-    rc = lib.spec_verify_tree(_ptr(x), _dtype_code(x), stride, _ptr(tok), _ptr(par), B, N, V,
-                              int(max_depth), float(temperature), _ptr(u),
-                              _rule(rule, tau, top_k, alpha),
-                              _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["num_accepted"]),
-                              _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
-                              _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+    fin, _keep = _finish(B, dev, out, stop_ids, max_new, counters)
+    rc = lib.spec_verify_tree_ex(_ptr(x), _dtype_code(x), stride, _ptr(tok), _ptr(par), B, N, V,
+                                 int(max_depth), float(temperature), _ptr(u),
+                                 _rule(rule, tau, top_k, alpha),
+                                 _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["num_accepted"]),
+                                 _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]), fin,
+                                 _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out

@@ -36,6 +36,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("spec_verify_greedy", "spec_verify_sample", "spec_verify_tree",
+              "spec_verify_greedy_ex", "spec_verify_sample_ex", "spec_verify_tree_ex",
               "spec_verify_status_string", "spec_verify_abi_version"):
         assert n in names
 
@@ -47,7 +48,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.spec_verify_abi_version() == 1
+    assert lib.spec_verify_abi_version() == 2
     for code in range(6):
         s = lib.spec_verify_status_string(code).decode()
         assert s and "unknown" not in s
@@ -145,3 +146,28 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros((1, 2, 8))
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify_greedy(x, torch.zeros((1, 1), dtype=torch.int32))
+
+
+def _greedy_ex(lib, fin, **kw):
+    a = dict(x=FAKE, dtype=1, stride=100, d=FAKE, B=2, K=3, V=100, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify_greedy_ex(P(a["x"]), a["dtype"], a["stride"], P(a["d"]), a["B"], a["K"], a["V"],
+                                     P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                     ctypes.byref(fin) if fin is not None else None,
+                                     P(a["ws"]), a["wsb"], P(0))
+
+
+def test_finish_params_validation(lib):
+    F = V.FinishParams
+    # out_len missing, n_stop out of range, stop ids missing, misaligned pointers
+    assert _greedy_ex(lib, F(None, 0, None, None, None)) == SV_ERR_INVALID_ARG
+    assert _greedy_ex(lib, F(FAKE, 17, None, FAKE, None)) == SV_ERR_INVALID_ARG
+    assert _greedy_ex(lib, F(FAKE, -1, None, FAKE, None)) == SV_ERR_INVALID_ARG
+    assert _greedy_ex(lib, F(None, 2, None, FAKE, None)) == SV_ERR_INVALID_ARG
+    assert _greedy_ex(lib, F(FAKE + 2, 1, None, FAKE, None)) == SV_ERR_INVALID_ARG
+    assert _greedy_ex(lib, F(FAKE, 1, None, FAKE, FAKE + 4)) == SV_ERR_INVALID_ARG
+    # valid parameters reach the workspace check; no finish behaves like the plain call
+    assert _greedy_ex(lib, F(FAKE, 2, FAKE, FAKE, FAKE), wsb=16) == SV_ERR_WORKSPACE_TOO_SMALL
+    assert _greedy_ex(lib, None, wsb=16) == SV_ERR_WORKSPACE_TOO_SMALL
+    assert _greedy_ex(lib, F(FAKE, 2, None, FAKE, None), B=0) == SV_OK
