@@ -64,6 +64,11 @@ CONFIGS = {
                                 finish=True,
                                 workload="greedy chain verify with the finish step: V=128256 bf16, K=5, B=32, "
                                          "a 2-id stop set, per-request max_new in [1, 6], running counters"),
+    "long_chain_early": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
+                             early=True,
+                             workload="long-chain greedy verify with early exit: V=50257 bf16, B=8, K+1=4096 "
+                                      "rows per request, drafts = argmax w.p. 0.95; rows after a request's "
+                                      "first mismatch are not read"),
     "long_chain": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
                        workload="long-chain greedy verify: GPT-2 vocab V=50257 bf16, B=8, K+1=4096 rows "
                                 "per request, drafts = argmax w.p. 0.95"),
@@ -102,6 +107,8 @@ _CALL_SOURCES = {
     "greedy": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "spec_verify.cu"),
     "draw": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "draw.cuh", "rules.cuh",
              "spec_verify.cu"),
+    "early": ("sv_common.cuh", "row_stats.cuh", "row_stats_early.cuh", "decide.cuh", "finish.cuh",
+              "spec_verify.cu"),
 }
 
 
@@ -114,7 +121,8 @@ def source_hash(cfg=None):
     if cfg is None:
         names = [n for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
     else:
-        names = sorted(_CALL_SOURCES["draw" if _launches_per_call(cfg) == 3 else "greedy"])
+        kind = "early" if cfg.get("early") else ("draw" if _launches_per_call(cfg) == 3 else "greedy")
+        names = sorted(_CALL_SOURCES[kind])
     for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
@@ -247,6 +255,8 @@ def make_inputs(cfg, seed, device):
 def call(cfg, x, out=None, ws=None):
     import speculative_decoding_verification_72_gb300 as sv
     if cfg["kind"] == "greedy":
+        if cfg.get("early"):
+            return sv.spec_verify_greedy_early(x.target, x.draft_tokens, workspace=ws, out=out)
         if cfg.get("finish"):
             return sv.spec_verify_greedy(x.target, x.draft_tokens, workspace=ws, out=out, stop_ids=x.stop_ids,
                                          max_new=x.max_new, counters=x.counters)
@@ -435,7 +445,17 @@ def run_gpu(args, cfg, name):
     value = aggregate(elapsed, rows, steps, world)
     step_s = elapsed / 1e3 / steps
     peak, peak_kind = measured_peak()
-    achieved = alg_bytes / step_s / 1e9
+    read_bytes = None
+    if cfg.get("early"):
+        # Early exit reads only part of the logits: the roofline uses the bytes
+        # each input set's call actually read (mean over the pool), as reported
+        # by the library, while `value` still counts every verified row.
+        tot = 0
+        for x in pool:
+            r = call(cfg, x, out=out, ws=ws)
+            tot += int(r["bytes_read"].item())
+        read_bytes = tot / len(pool)
+    achieved = (read_bytes if read_bytes is not None else alg_bytes) / step_s / 1e9
 
     e2e = _e2e(cfg, pool[0], dev, steps, out, ws)
     if world > 1:   # the slowest replica's rate, times the replicas
@@ -456,6 +476,9 @@ def run_gpu(args, cfg, name):
         "data": "synthetic (seeded; shapes from the pages, no dataset or weights)",
         "config": {"workload": cfg["workload"], "name": name, "B": cfg["B"],
                    "rows_per_step": rows, "algorithmic_bytes_per_step": alg_bytes,
+                   **({"bytes_read_per_step": read_bytes,
+                       "roofline_bytes": "bytes actually read (library-reported), not all logit bytes"}
+                      if read_bytes is not None else {}),
                    "l2_policy": f"rotating pool of {nsets} input sets, {nsets * set_bytes / 1e6:.0f} MB "
                                 f"> 4x L2 ({l2 / 1e6:.0f} MB)",
                    "timing": f"CUDA graphs of {per_graph} calls, events on the launch stream",
@@ -464,7 +487,9 @@ def run_gpu(args, cfg, name):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "one verify call: row_stats_kernel (all logit bytes) + decide kernel"
+                     "kernel": ("one verify call: row_stats_early_kernel (bytes it read) + decide kernel"
+                                if cfg.get("early") else
+                                "one verify call: row_stats_kernel (all logit bytes) + decide kernel")
                                + (" + draw kernel" if _launches_per_call(cfg) == 3 else ""),
                      "traffic": recorded_traffic(name)},
         "cpu_baseline": cpu,

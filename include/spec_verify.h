@@ -250,6 +250,27 @@ sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t 
                               const sv_finish_params* finish,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Early-exit greedy chain verification (mini-sglang PR #134, verify.py: rows
+ * after a request's first mismatch never reach the outputs). Same arguments,
+ * outputs and workspace size (spec_verify_greedy_workspace_size) as
+ * spec_verify_greedy, with identical tokens, num_accepted and status (log-
+ * probs agree to rounding: each row is summed by one CTA); the row-statistics kernel
+ * reads rows position by position across the batch and stops reading a
+ * request's rows once a mismatch at an earlier position is known, so a long
+ * chain that is rejected early costs a fraction of its logit bytes.
+ *   state           [B] int32 device array owned by the caller: zero-filled
+ *                   before its first use; every call leaves it zero again.
+ *                   Calls that overlap on the GPU need separate state arrays.
+ *   out_bytes_read  [1] uint64 device: logit bytes this call actually read
+ *                   (at least the bytes of rows 0..n of every request, at
+ *                   most all rows); may be NULL. */
+sv_status spec_verify_greedy_early(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                   const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                   int32_t* out_tokens, int32_t* out_num_accepted,
+                                   float* out_logprob, float* out_mu, int32_t* out_status,
+                                   int32_t* state, uint64_t* out_bytes_read,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of the library's static scratch array used by
  * spec_verify_greedy_static (one array per GPU that loads the library). */
 #define SV_STATIC_SCRATCH_BYTES (2u << 20)

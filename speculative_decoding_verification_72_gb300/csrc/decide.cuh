@@ -31,6 +31,7 @@
 namespace sv {
 
 constexpr int kK2Threads = 256;
+constexpr unsigned long long kEarlyAbortBit = 1ull << 63;   // set in a K1 CTA's byte count
 constexpr int kMaxTreeNodes = 1024;
 
 struct RuleArgs {
@@ -74,6 +75,14 @@ struct ChainArgs {
   uint32_t* draw_counters;  // [B], zeroed here for K3's tickets
   uint32_t* mu_counters;    // [B], zeroed here for the mu pass's tickets (or nullptr)
   FinishArgs fin;           // stop / cap / counters (greedy: applied here)
+  // Early-exit greedy calls (row_stats_early_kernel): one partial per row at
+  // slot `row`; the per-request state is zeroed here for the next call; the
+  // K1 CTAs' byte counts are summed into out_bytes.
+  int32_t row_partials;
+  int32_t* early_state;
+  const unsigned long long* cta_bytes;
+  int32_t n_cta;
+  unsigned long long* out_bytes;
 };
 
 // Inputs of one chain position, readable before K1 completes.
@@ -117,13 +126,16 @@ template <int ES>
 __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArgs a) {
   __shared__ int s_first;
   __shared__ int s_status;
-  __shared__ int s_fin;
+  __shared__ int s_fin[2];
+  __shared__ int s_stop[kMaxStopIds];
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int K = a.K, R = a.K + 1;
   const float c = a.c;
   const ChainIn pre = load_chain_in<ES>(a, b, tid < R ? tid : R);
   const float u_final = a.greedy ? 0.f : a.uniforms[static_cast<int64_t>(b) * R + K];
+  FinishPre fpre;
+  finish_prefetch(a.fin, b, s_stop, fpre);
 
   grid_dep_wait();
   grid_dep_launch();
@@ -132,6 +144,12 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     s_status = 0;
     if (a.draw_counters) a.draw_counters[b] = 0;
     if (a.mu_counters) a.mu_counters[b] = 0;
+  }
+  if (a.cta_bytes) {   // early-exit call: did any K1 CTA give up waiting?
+    __syncthreads();
+    bool aborted = false;
+    for (int g2 = tid; g2 < a.n_cta; g2 += kK2Threads) aborted |= (a.cta_bytes[g2] & kEarlyAbortBit) != 0;
+    if (__syncthreads_or(aborted) && tid == 0) s_status |= 32;   // TIMEOUT
   }
   int n = -1;
   int base = 0;
@@ -147,7 +165,15 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     const ChainIn in = (base == 0) ? pre : load_chain_in<ES>(a, b, active ? i : R);
     if (active) {
       const int64_t trow = static_cast<int64_t>(b) * R + i;
-      merge_row(a.part, trow, a.V, a.T, a.G, c, m, s, idx, err);
+      if (a.row_partials) {
+        const Partial v = a.part[trow];
+        m = v.m;
+        s = v.s;
+        idx = v.idx;
+        err = v.err;
+      } else {
+        merge_row(a.part, trow, a.V, a.T, a.G, c, m, s, idx, err);
+      }
       lp2row = m * c + log2f(s);
       if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= 4;   // NONFINITE_ROW
       if (err) st |= 32;                                                     // TIMEOUT
@@ -264,10 +290,24 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
   if (tid == 0) {
     a.out_num[b] = n;
     if (a.out_status) a.out_status[b] = s_status;
+    if (a.early_state) a.early_state[b] = 0;   // ready for the next call
+  }
+  if (a.out_bytes && b == 0) {   // bytes the early-exit K1 read, summed in a fixed order
+    __shared__ unsigned long long s_bytes[kK2Threads];
+    unsigned long long t = 0;
+    for (int g2 = tid; g2 < a.n_cta; g2 += kK2Threads) t += a.cta_bytes[g2] & ~kEarlyAbortBit;
+    s_bytes[tid] = t;
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long tot = 0;
+      for (int k = 0; k < kK2Threads; ++k) tot += s_bytes[k];
+      a.out_bytes[0] = tot;
+    }
   }
   if (a.greedy && a.fin.out_len) {   // greedy: this kernel ends the call
     __syncthreads();
-    finish_request(a.fin, b, n, R, a.out_tokens, a.out_logprob, a.out_mu, nullptr, a.out_status, &s_fin);
+    finish_request(a.fin, fpre, s_stop, b, n, R, a.out_tokens, a.out_logprob, a.out_mu, nullptr, a.out_status,
+                   s_fin);
   }
 }
 
@@ -310,7 +350,8 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   __shared__ int sm_next[kMaxTreeNodes];    // next sibling
   __shared__ unsigned char sm_bad[kMaxTreeNodes];  // row not finite / timed out
   __shared__ int s_status;
-  __shared__ int s_n, s_fin;
+  __shared__ int s_n, s_fin[2];
+  __shared__ int s_stop[kMaxStopIds];
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -337,6 +378,8 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
     sm_first[n] = -1;
   }
   __syncthreads();
+  FinishPre fpre;
+  finish_prefetch(a.fin, b, s_stop, fpre);
   if (tid == 0) {
     for (int n = N - 1; n >= 1; --n) {   // reverse insertion: lists in increasing index
       const int p = sm_par[n];
@@ -469,7 +512,8 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   if (tid == 0 && a.out_status) a.out_status[b] = s_status;
   if (a.greedy && a.fin.out_len) {   // greedy walk: this kernel ends the call
     __syncthreads();
-    finish_request(a.fin, b, s_n, W, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes, a.out_status, &s_fin);
+    finish_request(a.fin, fpre, s_stop, b, s_n, W, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes,
+                   a.out_status, s_fin);
   }
 }
 

@@ -310,6 +310,9 @@ __device__ __forceinline__ void block_sum_n(float (&v)[2 * C], float* red_n) {
 
 template <int ES>
 __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
+  __shared__ int s_stop_pre[kMaxStopIds];
+  FinishPre fpre;
+  if (a.fin_here) finish_prefetch(a.fin, blockIdx.x / a.Q, s_stop_pre, fpre);
   grid_dep_wait();
   grid_dep_launch();
   __shared__ float red_n[kK3Threads / 32 * 2 * kK3MaxCpc];
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   __shared__ float s_thr;
   __shared__ double s_S;
   __shared__ float2 s_part[kK3MaxChunks];
-  __shared__ int s_fin;
+  __shared__ int s_fin[2];
 
   const int tid = threadIdx.x;
   const int b = blockIdx.x / a.Q;
@@ -502,8 +505,8 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   }
   if (a.fin_here) {   // no mu pass follows: this kernel ends the call
     __syncthreads();
-    finish_request(a.fin, b, d.pos, a.out_cols, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes, a.out_status,
-                   &s_fin);
+    finish_request(a.fin, fpre, s_stop_pre, b, d.pos, a.out_cols, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes,
+                   a.out_status, s_fin);
   }
 }
 

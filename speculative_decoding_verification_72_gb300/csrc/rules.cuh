@@ -215,11 +215,14 @@ template <int ES>
 __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
   __shared__ float red[kMuThreads / 32];
   __shared__ float s_lp2, s_lq2;
-  __shared__ int s_last, s_fin;
+  __shared__ int s_last, s_fin[2];
+  __shared__ int s_stop[kMaxStopIds];
+  const int per_req = a.K * a.P;
+  FinishPre fpre;
+  finish_prefetch(a.fin, blockIdx.x / per_req, s_stop, fpre);
   grid_dep_wait();
   grid_dep_launch();
   const int tid = threadIdx.x;
-  const int per_req = a.K * a.P;
   const int b = blockIdx.x / per_req;
   const int r = blockIdx.x - b * per_req;
   const int j = r / a.P;
@@ -283,7 +286,8 @@ __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
   if (tid == 0) a.counters[b] = 0u;
   if (a.fin.out_len) {   // this kernel ends the call
     __syncthreads();
-    finish_request(a.fin, b, n, a.K + 1, a.out_tokens, a.out_logprob, a.out_mu, nullptr, a.out_status, &s_fin);
+    finish_request(a.fin, fpre, s_stop, b, n, a.K + 1, a.out_tokens, a.out_logprob, a.out_mu, nullptr,
+                   a.out_status, s_fin);
   }
 }
 

@@ -21,6 +21,7 @@
 #include "decide.cuh"
 #include "draw.cuh"
 #include "row_stats.cuh"
+#include "row_stats_early.cuh"
 #include "rules.cuh"
 
 namespace {
@@ -28,6 +29,7 @@ namespace {
 using namespace sv;
 
 constexpr size_t kAlign = 256;
+static_assert(SV_MAX_STOP_IDS == kMaxStopIds, "stop ids staged in shared memory");
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -169,6 +171,23 @@ cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   return launch(row_stats_kernel<ES>, a.G, kK1Threads, kK1SmemBytes, stream, true, a);
+}
+
+template <int ES>
+cudaError_t launch_row_stats_early(const EarlyArgs& e, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(row_stats_early_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kK1SmemBytes);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(row_stats_early_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (err != cudaSuccess) return err;
+    attr_set[dev] = true;
+  }
+  return launch(row_stats_early_kernel<ES>, e.rs.G, kK1Threads, kK1SmemBytes, stream, true, e);
 }
 
 cudaError_t launch_topk(const void* tgt, int64_t stride_b, int32_t rows_per_req, int32_t row_pitch,
@@ -591,6 +610,69 @@ sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t 
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_verify_greedy_early(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                   const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                   int32_t* out_tokens, int32_t* out_num_accepted, float* out_logprob,
+                                   float* out_mu, int32_t* out_status, int32_t* state,
+                                   uint64_t* out_bytes_read, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || K < 0 || V < 1 || row_stride < V) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target_logits || (K > 0 && !draft_tokens) || !out_tokens || !out_num_accepted || !workspace || !state)
+    return SV_ERR_INVALID_ARG;
+  if (!aligned(target_logits, es) || !aligned(workspace, 16) || !aligned(draft_tokens, 4) || !aligned(state, 4) ||
+      !aligned(out_bytes_read, 8) || !outputs_aligned(out_tokens, out_num_accepted, out_logprob, out_mu, out_status))
+    return SV_ERR_INVALID_ARG;
+  Plan pl;
+  const int64_t rows = static_cast<int64_t>(B) * (K + 1);
+  if (!make_plan(rows, 0, B, V, es, false, 0, 0, &pl)) return SV_ERR_INVALID_ARG;
+  if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float c = kLog2e;
+  EarlyArgs e;
+  e.rs = row_stats_args(pl, target_logits, row_stride, rows, nullptr, 0, 0, V, es, c, workspace);
+  int64_t g = static_cast<int64_t>(sm_count()) * kK1CtasPerSm;
+  if (g > rows) g = rows;
+  if (g > kK1MaxCtas) g = kK1MaxCtas;
+  e.rs.G = static_cast<int32_t>(g);
+  e.B = B;
+  e.R = K + 1;
+  e.drafts = draft_tokens;
+  e.state = state;
+  // one partial per row at slot `row`; the spare kK1MaxCtas slots after them hold the CTAs' byte counts
+  e.cta_bytes = reinterpret_cast<unsigned long long*>(e.rs.partials + rows);
+  cudaError_t err = es == 2 ? launch_row_stats_early<2>(e, st) : launch_row_stats_early<4>(e, st);
+  if (err != cudaSuccess) return SV_ERR_CUDA;
+  ChainArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tgt = static_cast<const uint8_t*>(target_logits);
+  a.tgt_stride = row_stride * es;
+  a.drafts = draft_tokens;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.part = e.rs.partials;
+  a.T = e.rs.T;
+  a.G = e.rs.G;
+  a.c = c;
+  a.greedy = 1;
+  a.out_tokens = out_tokens;
+  a.out_num = out_num_accepted;
+  a.out_logprob = out_logprob;
+  a.out_mu = out_mu;
+  a.out_status = out_status;
+  a.row_partials = 1;
+  a.early_state = state;
+  a.cta_bytes = e.cta_bytes;
+  a.n_cta = e.rs.G;
+  a.out_bytes = reinterpret_cast<unsigned long long*>(out_bytes_read);
+  err = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
+                : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+  return err == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 // ------------------------------------------------- no-allocation variant

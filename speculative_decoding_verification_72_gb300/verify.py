@@ -76,6 +76,8 @@ _SIGS = {
                                 _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_greedy_static": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                          _P, _P, _P, _P, _P, _P]),
+    "spec_verify_greedy_early": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
+                                        _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_greedy_ex": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                      _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_sample_ex": (_I32, [_P, _I32, _I64, _P, _I64, _P, _I32, _I32, _I32,
@@ -323,5 +325,44 @@ def spec_verify_tree(target_logits, node_tokens, parents, max_depth, temperature
                                  _ptr(out["tokens"]), _ptr(out["nodes"]), _ptr(out["num_accepted"]),
                                  _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]), fin,
                                  _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+    _check(rc)
+    return out
+
+
+_EARLY_STATE = {}
+
+
+def spec_verify_greedy_early(target_logits, draft_tokens, state=None, workspace=None, out=None):
+    """Early-exit greedy chain verification (include/spec_verify.h): the same
+    outputs as spec_verify_greedy, plus out["bytes_read"] (int64 [1], logit
+    bytes the call read). `state` is the caller's zero-filled int32 [B]
+    request state (left zero after each call); by default one cached per
+    device, stream and B is used."""
+    lib = load_library()
+    x, stride = _rows_view(target_logits, "target_logits")
+    B, R, V = x.shape
+    K = R - 1
+    dev = x.device
+    d = _i32(draft_tokens, "draft_tokens", (B, K), dev)
+    out = _outputs(B, R, dev, out=out)
+    if out.get("bytes_read") is None:
+        out["bytes_read"] = torch.zeros((1,), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    if state is None:
+        key = (dev.index, stream, B)
+        state = _EARLY_STATE.get(key)
+        if state is None:
+            state = _EARLY_STATE[key] = torch.zeros((B,), dtype=torch.int32, device=dev)
+    elif state.dtype != torch.int32 or tuple(state.shape) != (B,) or not state.is_contiguous() or state.device != dev:
+        raise SpecVerifyError(f"state must be a contiguous int32 ({B},) tensor on {dev}")
+    need = lib.spec_verify_greedy_workspace_size(B, K, V, _dtype_code(x))
+    if need == 0 and B > 0:
+        raise SpecVerifyError("invalid sizes")
+    ws = _ws(workspace, need, dev, stream)
+    rc = lib.spec_verify_greedy_early(_ptr(x), _dtype_code(x), stride, _ptr(d), B, K, V,
+                                      _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                      _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
+                                      _ptr(state), _ptr(out["bytes_read"]),
+                                      _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out
