@@ -24,8 +24,8 @@ taken here (the usual EAGLE construction):
   * output order is BFS: root first, then by level, within a level by score
     descending (earlier candidate first), as workloads.tree_shape orders its
     trees; the root's token is -1 and its parent -1.
-A request is flagged near_tie when a decision above compares two scores
-closer than NEAR (1e-4): the order of a level's best topk + 1 nodes, the
+A request is flagged near_tie when a decision above compares two distinct
+scores closer than NEAR (1e-4): the order of a level's best topk + 1 nodes, the
 keep boundary, or the order of two kept nodes of one level; the device
 path, summing in fp32, may then legitimately order them differently.
 
@@ -54,7 +54,10 @@ def top_tokens(y, k):
 
 
 def _close(a, b):
-    return abs(a - b) < NEAR
+    # equal scores are ordered by creation on any device (they come from equal
+    # logits of one row, computed identically); only distinct, close scores
+    # are ambiguous under rounding
+    return a != b and abs(a - b) < NEAR
 
 
 def build_tree(draft_logits, depth, topk, n_nodes, temperature=1.0):
