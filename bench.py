@@ -64,6 +64,9 @@ CONFIGS = {
                                 finish=True,
                                 workload="greedy chain verify with the finish step: V=128256 bf16, K=5, B=32, "
                                          "a 2-id stop set, per-request max_new in [1, 6], running counters"),
+    "eagle_tree_build": dict(kind="tree_build", B=32, V=128256, depth=5, topk=4, N=64, dtype="bf16", seed=7205,
+                             workload="EAGLE-3 draft-tree construction: depth 5, topk 4, 64 nodes, V=128256 bf16 "
+                                      "draft logits N(0,3^2), 17 rank-ordered draft rows per request, B=32"),
     "long_chain_early": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
                              early=True,
                              workload="long-chain greedy verify with early exit: V=50257 bf16, B=8, K+1=4096 "
@@ -74,7 +77,7 @@ CONFIGS = {
                                 "per request, drafts = argmax w.p. 0.95"),
 }
 DEFAULT_CONFIG = "llama_greedy"
-KERNELS_PER_CALL = {"greedy": 2, "sample": 3, "tree": 2}
+KERNELS_PER_CALL = {"greedy": 2, "sample": 3, "tree": 2, "tree_build": 2}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -109,6 +112,7 @@ _CALL_SOURCES = {
              "spec_verify.cu"),
     "early": ("sv_common.cuh", "row_stats.cuh", "row_stats_early.cuh", "decide.cuh", "finish.cuh",
               "spec_verify.cu"),
+    "tree_build": ("sv_common.cuh", "tree_build.cuh", "spec_verify.cu"),
 }
 
 
@@ -121,7 +125,8 @@ def source_hash(cfg=None):
     if cfg is None:
         names = [n for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
     else:
-        kind = "early" if cfg.get("early") else ("draw" if _launches_per_call(cfg) == 3 else "greedy")
+        kind = ("early" if cfg.get("early") else "tree_build" if cfg["kind"] == "tree_build"
+                else "draw" if _launches_per_call(cfg) == 3 else "greedy")
         names = sorted(_CALL_SOURCES[kind])
     for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
@@ -154,9 +159,16 @@ def recorded_traffic(config_name):
     return None
 
 
+def metric_name(cfg):
+    return "draft logit rows/s (tree construction)" if cfg["kind"] == "tree_build" else "verified logit rows/s"
+
+
 def algorithmic_bytes(cfg):
     es = 2 if cfg["dtype"] == "bf16" else 4
     B, V = cfg["B"], cfg["V"]
+    if cfg["kind"] == "tree_build":   # rows = draft rows; outputs tokens, parents, scores, status
+        rows = B * (1 + (cfg["depth"] - 1) * cfg["topk"])
+        return rows, rows * V * es + B * cfg["N"] * 12 + B * 4
     if cfg["kind"] == "tree":
         N = cfg["N"]
         W = 6
@@ -237,6 +249,13 @@ def make_inputs(cfg, seed, device):
     import torch
     from speculative_decoding_verification_72_gb300 import workloads as W
     dt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    if cfg["kind"] == "tree_build":
+        class _Rows:
+            pass
+        x = _Rows()
+        x.draft_rows = W.draft_tree_rows(B=cfg["B"], V=cfg["V"], depth=cfg["depth"], topk=cfg["topk"], dtype=dt,
+                                         seed=seed, device=device)
+        return x
     if cfg["kind"] == "greedy":
         x = W.greedy_chain(B=cfg["B"], K=cfg["K"], V=cfg["V"], dtype=dt, p_match=cfg["p_match"],
                            seed=seed, device=device)
@@ -264,6 +283,8 @@ def call(cfg, x, out=None, ws=None):
     if cfg["kind"] == "sample":
         return sv.spec_verify_sample(x.target, x.draft_tokens, x.uniforms, draft_logits=x.draft_logits,
                                      workspace=ws, out=out)
+    if cfg["kind"] == "tree_build":
+        return sv.spec_tree_build(x.draft_rows, cfg["depth"], cfg["topk"], cfg["N"], workspace=ws, out=out)
     return sv.spec_verify_tree(x.target, x.node_tokens, x.parents, x.max_depth,
                                temperature=cfg.get("T", 0.0), uniforms=x.uniforms,
                                rule=cfg.get("rule", 0), tau=cfg.get("tau", 0.0),
@@ -272,7 +293,7 @@ def call(cfg, x, out=None, ws=None):
 
 def input_bytes(x):
     n = 0
-    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents"):
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows"):
         t = getattr(x, k, None)
         if t is not None:
             n += t.numel() * t.element_size()
@@ -297,6 +318,10 @@ def oracle_rows_per_s(cfg, x_host, budget_s, max_requests=None):
             O.verify_sample(x_host["target"][sl], x_host["draft_logits"][sl], x_host["draft_tokens"][sl],
                             1.0, x_host["uniforms"][sl])
             rows = cfg["K"] + 1
+        elif cfg["kind"] == "tree_build":
+            from oracle import tree_build as TB
+            TB.build_tree(x_host["draft_rows"][sl], cfg["depth"], cfg["topk"], cfg["N"])
+            rows = 1 + (cfg["depth"] - 1) * cfg["topk"]
         else:
             O.verify_tree(x_host["target"][sl], x_host["node_tokens"][sl], x_host["parents"][sl], 5,
                           cfg.get("T", 0.0), x_host["uniforms"][sl], rule=cfg.get("rule", 0),
@@ -310,7 +335,7 @@ def oracle_rows_per_s(cfg, x_host, budget_s, max_requests=None):
 
 def host_copy(x):
     d = {}
-    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents"):
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows"):
         t = getattr(x, k, None)
         if t is None:
             continue
@@ -331,7 +356,8 @@ def run_reference(args, cfg, name):
     x = host_copy(make_inputs(cfg, cfg["seed"], "cpu"))
     # size one step's sample so the whole run stays within about two minutes
     t_req = oracle_rows_per_s(cfg, x, 0.0, max_requests=1)
-    rows_req = (cfg["K"] + 1) if cfg["kind"] != "tree" else cfg["N"]
+    rows_req = (cfg["N"] if cfg["kind"] == "tree" else
+                1 + (cfg["depth"] - 1) * cfg["topk"] if cfg["kind"] == "tree_build" else cfg["K"] + 1)
     per_req_s = rows_req / t_req[0]
     reqs_per_step = max(1, min(cfg["B"], int(120.0 / max(steps + warmup, 1) / per_req_s)))
     from oracle import spec_oracle as O  # noqa: F401
@@ -345,7 +371,7 @@ def run_reference(args, cfg, name):
         total_rows += r * rows_req
     value = total_rows / total_t
     line = {
-        "impl": "reference", "metric": "verified logit rows/s", "value": value, "unit": "rows/s",
+        "impl": "reference", "metric": metric_name(cfg), "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
         "ms_per_step": 1e3 * total_t / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -470,7 +496,7 @@ def run_gpu(args, cfg, name):
                          f"float64 NumPy oracle, one thread"}
 
     line = {
-        "metric": "verified logit rows/s", "value": value, "unit": "rows/s", "n_gpus": world,
+        "metric": metric_name(cfg), "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": elapsed / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
         "data": "synthetic (seeded; shapes from the pages, no dataset or weights)",
@@ -489,6 +515,8 @@ def run_gpu(args, cfg, name):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": ("one verify call: row_stats_early_kernel (bytes it read) + decide kernel"
                                 if cfg.get("early") else
+                                "one build call: row_topk_kernel (all draft logit bytes) + tree_select_kernel"
+                                if cfg["kind"] == "tree_build" else
                                 "one verify call: row_stats_kernel (all logit bytes) + decide kernel")
                                + (" + draw kernel" if _launches_per_call(cfg) == 3 else ""),
                      "traffic": recorded_traffic(name)},
@@ -516,6 +544,8 @@ def _workspace_need(cfg):
         return lib.spec_verify_greedy_workspace_size(cfg["B"], cfg["K"], cfg["V"], dt)
     if cfg["kind"] == "sample":
         return lib.spec_verify_sample_workspace_size(cfg["B"], cfg["K"], cfg["V"], dt, 1)
+    if cfg["kind"] == "tree_build":
+        return lib.spec_tree_build_workspace_size(cfg["B"], cfg["depth"], cfg["topk"], cfg["V"])
     return lib.spec_verify_tree_workspace_size(cfg["B"], cfg["N"], cfg["V"], dt)
 
 
@@ -524,7 +554,7 @@ def _e2e(cfg, x, dev, steps, out, ws):
     that step's inputs from pinned host memory and reads the results back."""
     import torch
     names = [k for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents",
-                         "stop_ids", "max_new")
+                         "stop_ids", "max_new", "draft_rows")
              if getattr(x, k, None) is not None]
     host = {k: getattr(x, k).cpu().pin_memory() for k in names}
     devb = {k: torch.empty_like(getattr(x, k)) for k in names}
@@ -538,7 +568,7 @@ def _e2e(cfg, x, dev, steps, out, ws):
 
     inp = Inp()
     for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents",
-              "stop_ids", "max_new"):
+              "stop_ids", "max_new", "draft_rows"):
         setattr(inp, k, devb.get(k))
     inp.max_depth = getattr(x, "max_depth", None)
     inp.counters = getattr(x, "counters", None)   # running totals stay on the device

@@ -271,6 +271,34 @@ sv_status spec_verify_greedy_early(const void* target_logits, int32_t dtype, int
                                    int32_t* state, uint64_t* out_bytes_read,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* EAGLE-style draft-tree construction, the step before spec_verify_tree
+ * (nanospec README: EAGLE-3 tree speculation, depth 5, topk 4).
+ *   draft_logits  [B, R, V], R = 1 + (depth - 1) * topk draft rows per
+ *                 request in rank order: row 0 is the root's; row
+ *                 1 + (d - 2) * topk + r belongs to the r-th best node of
+ *                 level d - 1 (d = 2..depth).
+ *   1 <= topk <= 8 and topk <= V; depth >= 1; the candidate count
+ *   topk + (depth - 1) * topk^2 is at most 1024 and R at most 128; 1 <= n_nodes <=
+ *   min(1 + candidates, SV_MAX_TREE_NODES); temperature finite, >= 1e-4.
+ * A node's score is its path's cumulative draft log-prob
+ * (log_softmax(y / T)). Level 1 holds the root row's topk tokens (largest
+ * logits, lower id first on ties); each later level expands the topk best
+ * nodes of the level above (score descending, earlier candidate first) into
+ * the topk tokens of their rows. The n_nodes - 1 best candidates are kept with
+ * the root and written in BFS order (level, then score descending, then
+ * creation order):
+ *   out_tokens [B, n_nodes] (root -1), out_parents [B, n_nodes] (root -1,
+ *   parents[n] < n), out_scores [B, n_nodes] (root 0; may be NULL),
+ *   out_status [B] (SV_STATUS_NONFINITE_ROW if a used row has no finite
+ *   maximum; may be NULL).
+ * out_tokens / out_parents feed spec_verify_tree directly. */
+size_t spec_tree_build_workspace_size(int32_t B, int32_t depth, int32_t topk, int32_t V);
+sv_status spec_tree_build(const void* draft_logits, int32_t dtype, int64_t row_stride,
+                          int32_t B, int32_t V, int32_t depth, int32_t topk, int32_t n_nodes,
+                          float temperature, int32_t* out_tokens, int32_t* out_parents,
+                          float* out_scores, int32_t* out_status,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of the library's static scratch array used by
  * spec_verify_greedy_static (one array per GPU that loads the library). */
 #define SV_STATIC_SCRATCH_BYTES (2u << 20)

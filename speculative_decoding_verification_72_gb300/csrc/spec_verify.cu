@@ -23,6 +23,7 @@
 #include "row_stats.cuh"
 #include "row_stats_early.cuh"
 #include "rules.cuh"
+#include "tree_build.cuh"
 
 namespace {
 
@@ -609,6 +610,65 @@ sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t 
   const int grid3 = B * d.Q;
   e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
               : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+size_t spec_tree_build_workspace_size(int32_t B, int32_t depth, int32_t topk, int32_t V) {
+  if (B < 0 || depth < 1 || topk < 1 || topk > kTbMaxK || V < 1) return 0;
+  const int64_t P = (V + kTbPieceElems - 1) / kTbPieceElems;
+  const int64_t rows = static_cast<int64_t>(B) * (1 + static_cast<int64_t>(depth - 1) * topk);
+  return align_up(static_cast<size_t>(rows > 0 ? rows * P : 1) * sizeof(TopRow), kAlign);
+}
+
+sv_status spec_tree_build(const void* draft_logits, int32_t dtype, int64_t row_stride, int32_t B, int32_t V,
+                          int32_t depth, int32_t topk, int32_t n_nodes, float temperature,
+                          int32_t* out_tokens, int32_t* out_parents, float* out_scores, int32_t* out_status,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || V < 1 || row_stride < V || depth < 1 || topk < 1 || topk > kTbMaxK || topk > V)
+    return SV_ERR_INVALID_ARG;
+  const int64_t cands = topk + static_cast<int64_t>(depth - 1) * topk * topk;
+  if (cands > kTbMaxCands || n_nodes < 1 || n_nodes > 1 + cands || n_nodes > SV_MAX_TREE_NODES)
+    return SV_ERR_INVALID_ARG;
+  if (!valid_temperature(temperature)) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!draft_logits || !out_tokens || !out_parents || !workspace) return SV_ERR_INVALID_ARG;
+  if (!aligned(draft_logits, es) || !aligned(workspace, 16) || !aligned(out_tokens, 4) || !aligned(out_parents, 4) ||
+      !aligned(out_scores, 4) || !aligned(out_status, 4))
+    return SV_ERR_INVALID_ARG;
+  const int32_t R = 1 + (depth - 1) * topk;
+  if (R > kTbMaxRows) return SV_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(B) * R;
+  if (rows > INT32_MAX) return SV_ERR_INVALID_ARG;
+  if (workspace_bytes < spec_tree_build_workspace_size(B, depth, topk, V)) return SV_ERR_WORKSPACE_TOO_SMALL;
+  const int32_t P = (V + kTbPieceElems - 1) / kTbPieceElems;
+  if (rows * P > INT32_MAX) return SV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float c = kLog2e / temperature;
+  RowTopkArgs ra;
+  ra.base = static_cast<const uint8_t*>(draft_logits);
+  ra.stride_bytes = row_stride * es;
+  ra.V = V;
+  ra.P = P;
+  ra.c = c;
+  ra.out = static_cast<TopRow*>(workspace);
+  cudaError_t e = es == 2 ? launch(row_topk_kernel<2>, static_cast<int>(rows * P), kTbThreads, 0, st, true, ra)
+                          : launch(row_topk_kernel<4>, static_cast<int>(rows * P), kTbThreads, 0, st, true, ra);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  TreeSelectArgs ta;
+  ta.rows = ra.out;
+  ta.R = R;
+  ta.P = P;
+  ta.depth = depth;
+  ta.topk = topk;
+  ta.n_nodes = n_nodes;
+  ta.c = c;
+  ta.out_tokens = out_tokens;
+  ta.out_parents = out_parents;
+  ta.out_scores = out_scores;
+  ta.out_status = out_status;
+  e = launch(tree_select_kernel, B, kTbSelThreads, 0, st, true, ta);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

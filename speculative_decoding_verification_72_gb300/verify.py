@@ -78,6 +78,9 @@ _SIGS = {
                                          _P, _P, _P, _P, _P, _P]),
     "spec_verify_greedy_early": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                         _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_tree_build_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "spec_tree_build": (_I32, [_P, _I32, _I64, _I32, _I32, _I32, _I32, _I32, _F,
+                               _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_greedy_ex": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                      _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_sample_ex": (_I32, [_P, _I32, _I64, _P, _I64, _P, _I32, _I32, _I32,
@@ -364,5 +367,34 @@ def spec_verify_greedy_early(target_logits, draft_tokens, state=None, workspace=
                                       _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
                                       _ptr(state), _ptr(out["bytes_read"]),
                                       _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+    _check(rc)
+    return out
+
+
+def spec_tree_build(draft_logits, depth, topk, n_nodes, temperature=1.0, workspace=None, out=None):
+    """EAGLE-style draft tree from rank-ordered draft rows (include/spec_verify.h).
+    draft_logits [B, 1 + (depth - 1) * topk, V]. Returns a dict of CUDA
+    tensors: tokens, parents, scores [B, n_nodes] and status [B]; tokens and
+    parents feed spec_verify_tree."""
+    lib = load_library()
+    x, stride = _rows_view(draft_logits, "draft_logits")
+    B, R, V = x.shape
+    if R != 1 + (int(depth) - 1) * int(topk):
+        raise SpecVerifyError(f"draft_logits must have 1 + (depth - 1) * topk = {1 + (depth - 1) * topk} rows")
+    dev = x.device
+    if out is None:
+        out = dict(tokens=torch.empty((B, n_nodes), dtype=torch.int32, device=dev),
+                   parents=torch.empty((B, n_nodes), dtype=torch.int32, device=dev),
+                   scores=torch.empty((B, n_nodes), dtype=torch.float32, device=dev),
+                   status=torch.empty((B,), dtype=torch.int32, device=dev))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    need = lib.spec_tree_build_workspace_size(B, int(depth), int(topk), V)
+    if need == 0 and B > 0:
+        raise SpecVerifyError("invalid sizes")
+    ws = _ws(workspace, need, dev, stream)
+    rc = lib.spec_tree_build(_ptr(x), _dtype_code(x), stride, B, V, int(depth), int(topk), int(n_nodes),
+                             float(temperature), _ptr(out["tokens"]), _ptr(out["parents"]),
+                             _ptr(out["scores"]), _ptr(out["status"]),
+                             _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
     return out

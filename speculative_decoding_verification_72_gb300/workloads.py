@@ -195,3 +195,10 @@ def eagle_tree(B, V, n_nodes=64, depth=5, topk=4, dtype=torch.bfloat16, std=3.0,
                       node_tokens=torch.from_numpy(tokens).to(torch.int32).to(device),
                       parents=torch.from_numpy(parents).to(torch.int32).to(device),
                       uniforms=uniforms, max_depth=depth)
+
+
+def draft_tree_rows(B, V, depth=5, topk=4, dtype=torch.bfloat16, std=3.0, seed=7205, device="cpu"):
+    """Rank-ordered draft rows for tree construction: [B, 1 + (depth - 1) * topk, V]
+    logits N(0, std^2) (row 0 the root's, then topk rows per later level)."""
+    g = _gen(device, seed)
+    return _normal_logits(B, 1 + (depth - 1) * topk, V, std, dtype, device, g)
