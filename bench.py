@@ -67,6 +67,10 @@ CONFIGS = {
     "eagle_tree_build": dict(kind="tree_build", B=32, V=128256, depth=5, topk=4, N=64, dtype="bf16", seed=7205,
                              workload="EAGLE-3 draft-tree construction: depth 5, topk 4, 64 nodes, V=128256 bf16 "
                                       "draft logits N(0,3^2), 17 rank-ordered draft rows per request, B=32"),
+    "kv_compact": dict(kind="kv_compact", B=32, N=64, page_size=16, row_elems=65536, dtype="bf16", seed=7206,
+                       workload="accepted-path KV compaction: B=32 requests, 64-node trees, paths of 0..5 accepted "
+                                "nodes, paged bf16 cache (16 rows per page, 128 KB rows = 32 layers x K,V x 8 "
+                                "heads x 128 dims), committed prefixes of 0..256 tokens"),
     "long_chain_early": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
                              early=True,
                              workload="long-chain greedy verify with early exit: V=50257 bf16, B=8, K+1=4096 "
@@ -77,7 +81,7 @@ CONFIGS = {
                                 "per request, drafts = argmax w.p. 0.95"),
 }
 DEFAULT_CONFIG = "llama_greedy"
-KERNELS_PER_CALL = {"greedy": 2, "sample": 3, "tree": 2, "tree_build": 2}
+KERNELS_PER_CALL = {"greedy": 2, "sample": 3, "tree": 2, "tree_build": 2, "kv_compact": 1}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -113,6 +117,7 @@ _CALL_SOURCES = {
     "early": ("sv_common.cuh", "row_stats.cuh", "row_stats_early.cuh", "decide.cuh", "finish.cuh",
               "spec_verify.cu"),
     "tree_build": ("sv_common.cuh", "tree_build.cuh", "spec_verify.cu"),
+    "kv_compact": ("sv_common.cuh", "kv_compact.cuh", "spec_verify.cu"),
 }
 
 
@@ -125,7 +130,7 @@ def source_hash(cfg=None):
     if cfg is None:
         names = [n for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
     else:
-        kind = ("early" if cfg.get("early") else "tree_build" if cfg["kind"] == "tree_build"
+        kind = ("early" if cfg.get("early") else cfg["kind"] if cfg["kind"] in ("tree_build", "kv_compact")
                 else "draw" if _launches_per_call(cfg) == 3 else "greedy")
         names = sorted(_CALL_SOURCES[kind])
     for name in names:
@@ -160,11 +165,36 @@ def recorded_traffic(config_name):
 
 
 def metric_name(cfg):
-    return "draft logit rows/s (tree construction)" if cfg["kind"] == "tree_build" else "verified logit rows/s"
+    if cfg["kind"] == "tree_build":
+        return "draft logit rows/s (tree construction)"
+    if cfg["kind"] == "kv_compact":
+        return "KV rows moved/s (accepted-path compaction)"
+    return "verified logit rows/s"
+
+
+def kv_paths(cfg, seed):
+    """Synthetic accepted paths: n in 0..5, node ids strictly increasing in 1..N-1."""
+    rng = np.random.default_rng(seed)
+    B, N = cfg["B"], cfg["N"]
+    nodes = np.full((B, 6), -1, dtype=np.int64)
+    n = rng.integers(0, 6, size=B)
+    for b in range(B):
+        nodes[b, 0] = 0
+        nodes[b, 1:n[b] + 1] = np.sort(rng.choice(np.arange(1, N), size=n[b], replace=False))
+    base = rng.integers(0, 257, size=B)
+    return nodes, n, base
+
+
+def kv_moved_rows(nodes, n):
+    return int(sum(1 for b in range(len(n)) for j in range(1, int(n[b]) + 1) if nodes[b, j] != j))
 
 
 def algorithmic_bytes(cfg):
     es = 2 if cfg["dtype"] == "bf16" else 4
+    if cfg["kind"] == "kv_compact":   # rows = path rows moved; each read once and written once
+        nodes, n, _ = kv_paths(cfg, cfg["seed"])
+        rows = kv_moved_rows(nodes, n)
+        return rows, 2 * rows * cfg["row_elems"] * es
     B, V = cfg["B"], cfg["V"]
     if cfg["kind"] == "tree_build":   # rows = draft rows; outputs tokens, parents, scores, status
         rows = B * (1 + (cfg["depth"] - 1) * cfg["topk"])
@@ -249,6 +279,20 @@ def make_inputs(cfg, seed, device):
     import torch
     from speculative_decoding_verification_72_gb300 import workloads as W
     dt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
+    if cfg["kind"] == "kv_compact":
+        class _Kv:
+            pass
+        x = _Kv()
+        nodes, n, base = kv_paths(cfg, cfg["seed"])   # the same paths in every set: rows/s counts them
+        P, B = cfg["page_size"], cfg["B"]
+        per_req = (257 + cfg["N"] + P - 1) // P
+        g = torch.Generator(device="cpu").manual_seed(seed)
+        x.kv = torch.randn((B * per_req, P, cfg["row_elems"]), device=device, dtype=dt)
+        x.table = torch.randperm(B * per_req, generator=g).view(B, per_req).to(device=device, dtype=torch.int32)
+        x.base = torch.tensor(base, dtype=torch.int32, device=device)
+        x.nodes = torch.tensor(nodes, dtype=torch.int32, device=device)
+        x.n = torch.tensor(n, dtype=torch.int32, device=device)
+        return x
     if cfg["kind"] == "tree_build":
         class _Rows:
             pass
@@ -285,6 +329,8 @@ def call(cfg, x, out=None, ws=None):
                                      workspace=ws, out=out)
     if cfg["kind"] == "tree_build":
         return sv.spec_tree_build(x.draft_rows, cfg["depth"], cfg["topk"], cfg["N"], workspace=ws, out=out)
+    if cfg["kind"] == "kv_compact":
+        return sv.spec_kv_compact(x.kv, x.table, x.base, x.nodes, x.n, cfg["N"], out=out)
     return sv.spec_verify_tree(x.target, x.node_tokens, x.parents, x.max_depth,
                                temperature=cfg.get("T", 0.0), uniforms=x.uniforms,
                                rule=cfg.get("rule", 0), tau=cfg.get("tau", 0.0),
@@ -293,7 +339,7 @@ def call(cfg, x, out=None, ws=None):
 
 def input_bytes(x):
     n = 0
-    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows"):
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows", "kv"):
         t = getattr(x, k, None)
         if t is not None:
             n += t.numel() * t.element_size()
@@ -318,6 +364,13 @@ def oracle_rows_per_s(cfg, x_host, budget_s, max_requests=None):
             O.verify_sample(x_host["target"][sl], x_host["draft_logits"][sl], x_host["draft_tokens"][sl],
                             1.0, x_host["uniforms"][sl])
             rows = cfg["K"] + 1
+        elif cfg["kind"] == "kv_compact":
+            from oracle import kv_compact as KC
+            pages = x_host["table"][r]                       # this request's pages only
+            small = x_host["kv"][pages]
+            KC.compact(small, np.arange(len(pages))[None], cfg["page_size"], x_host["base"][sl],
+                       x_host["nodes"][sl], x_host["n"][sl], cfg["N"])
+            rows = int(x_host["n"][r])
         elif cfg["kind"] == "tree_build":
             from oracle import tree_build as TB
             TB.build_tree(x_host["draft_rows"][sl], cfg["depth"], cfg["topk"], cfg["N"])
@@ -335,7 +388,8 @@ def oracle_rows_per_s(cfg, x_host, budget_s, max_requests=None):
 
 def host_copy(x):
     d = {}
-    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows"):
+    for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows",
+              "kv", "table", "base", "nodes", "n"):
         t = getattr(x, k, None)
         if t is None:
             continue
@@ -357,7 +411,8 @@ def run_reference(args, cfg, name):
     # size one step's sample so the whole run stays within about two minutes
     t_req = oracle_rows_per_s(cfg, x, 0.0, max_requests=1)
     rows_req = (cfg["N"] if cfg["kind"] == "tree" else
-                1 + (cfg["depth"] - 1) * cfg["topk"] if cfg["kind"] == "tree_build" else cfg["K"] + 1)
+                1 + (cfg["depth"] - 1) * cfg["topk"] if cfg["kind"] == "tree_build" else
+                3 if cfg["kind"] == "kv_compact" else cfg["K"] + 1)
     per_req_s = rows_req / t_req[0]
     reqs_per_step = max(1, min(cfg["B"], int(120.0 / max(steps + warmup, 1) / per_req_s)))
     from oracle import spec_oracle as O  # noqa: F401
@@ -517,6 +572,8 @@ def run_gpu(args, cfg, name):
                                 if cfg.get("early") else
                                 "one build call: row_topk_kernel (all draft logit bytes) + tree_select_kernel"
                                 if cfg["kind"] == "tree_build" else
+                                "one compaction call: kv_compact_kernel (path rows read + written)"
+                                if cfg["kind"] == "kv_compact" else
                                 "one verify call: row_stats_kernel (all logit bytes) + decide kernel")
                                + (" + draw kernel" if _launches_per_call(cfg) == 3 else ""),
                      "traffic": recorded_traffic(name)},
@@ -546,6 +603,8 @@ def _workspace_need(cfg):
         return lib.spec_verify_sample_workspace_size(cfg["B"], cfg["K"], cfg["V"], dt, 1)
     if cfg["kind"] == "tree_build":
         return lib.spec_tree_build_workspace_size(cfg["B"], cfg["depth"], cfg["topk"], cfg["V"])
+    if cfg["kind"] == "kv_compact":
+        return 256
     return lib.spec_verify_tree_workspace_size(cfg["B"], cfg["N"], cfg["V"], dt)
 
 
@@ -554,7 +613,7 @@ def _e2e(cfg, x, dev, steps, out, ws):
     that step's inputs from pinned host memory and reads the results back."""
     import torch
     names = [k for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents",
-                         "stop_ids", "max_new", "draft_rows")
+                         "stop_ids", "max_new", "draft_rows", "table", "base", "nodes", "n")
              if getattr(x, k, None) is not None]
     host = {k: getattr(x, k).cpu().pin_memory() for k in names}
     devb = {k: torch.empty_like(getattr(x, k)) for k in names}
@@ -568,8 +627,9 @@ def _e2e(cfg, x, dev, steps, out, ws):
 
     inp = Inp()
     for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents",
-              "stop_ids", "max_new", "draft_rows"):
+              "stop_ids", "max_new", "draft_rows", "table", "base", "nodes", "n"):
         setattr(inp, k, devb.get(k))
+    inp.kv = getattr(x, "kv", None)               # the KV cache is device-resident state
     inp.max_depth = getattr(x, "max_depth", None)
     inp.counters = getattr(x, "counters", None)   # running totals stay on the device
 

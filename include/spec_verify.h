@@ -299,6 +299,28 @@ sv_status spec_tree_build(const void* draft_logits, int32_t dtype, int64_t row_s
                           float* out_scores, int32_t* out_status,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Accepted-path KV compaction, the step after spec_verify_tree (nanospec
+ * README: paged KV cache; mini-sglang PR #134, draft.py: the cache keeps the
+ * accepted prefix and the rest is truncated). The verify pass wrote tree node
+ * n's key/value row at logical position seq_base[b] + n; logical position p
+ * of request b is slot p % page_size of page page_table[b, p / page_size] in
+ * a cache of pages of page_size rows, token_stride_bytes apart, each row
+ * row_bytes long (both multiples of 16; kv 16-byte aligned). The path
+ * path_nodes[b, 0..n] (out_nodes of spec_verify_tree, n = num_accepted[b],
+ * path_cols its row length) is moved so its j-th node lands at position
+ * seq_base[b] + j, in place; rows off the path are untouched; out_len[b] =
+ * seq_base[b] + n + 1 (the root and the accepted nodes). A path node outside
+ * [0, max_nodes), n outside [0, path_cols), or a page id < 0 or past
+ * max_pages leaves the request untouched, out_len[b] = seq_base[b] and
+ * out_status[b] = SV_STATUS_BAD_PAGE (out_status may be NULL). Requests must
+ * not share pages. All pointers are device memory. */
+#define SV_STATUS_BAD_PAGE 256
+sv_status spec_kv_compact(void* kv, int64_t token_stride_bytes, int32_t row_bytes,
+                          const int32_t* page_table, int32_t max_pages, int32_t page_size,
+                          const int32_t* seq_base, const int32_t* path_nodes, int32_t path_cols,
+                          const int32_t* num_accepted, int32_t B, int32_t max_nodes,
+                          int32_t* out_len, int32_t* out_status, void* stream);
+
 /* Bytes of the library's static scratch array used by
  * spec_verify_greedy_static (one array per GPU that loads the library). */
 #define SV_STATIC_SCRATCH_BYTES (2u << 20)

@@ -11,5 +11,5 @@ from .verify import (  # noqa: F401
     STATUS_BAD_PARENT, STATUS_BAD_TOKEN, STATUS_DEPTH_EXCEEDED,
     STATUS_NONFINITE_ROW, STATUS_TIMEOUT, STATUS_ZERO_MASS,
     SpecVerifyError, library_path, load_library,
-    spec_tree_build, spec_verify_greedy, spec_verify_greedy_early, spec_verify_sample, spec_verify_tree,
+    spec_kv_compact, spec_tree_build, spec_verify_greedy, spec_verify_greedy_early, spec_verify_sample, spec_verify_tree,
 )

@@ -24,6 +24,7 @@
 #include "row_stats_early.cuh"
 #include "rules.cuh"
 #include "tree_build.cuh"
+#include "kv_compact.cuh"
 
 namespace {
 
@@ -669,6 +670,41 @@ sv_status spec_tree_build(const void* draft_logits, int32_t dtype, int64_t row_s
   ta.out_scores = out_scores;
   ta.out_status = out_status;
   e = launch(tree_select_kernel, B, kTbSelThreads, 0, st, true, ta);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_kv_compact(void* kv, int64_t token_stride_bytes, int32_t row_bytes, const int32_t* page_table,
+                          int32_t max_pages, int32_t page_size, const int32_t* seq_base, const int32_t* path_nodes,
+                          int32_t path_cols, const int32_t* num_accepted, int32_t B, int32_t max_nodes,
+                          int32_t* out_len, int32_t* out_status, void* stream) {
+  if (B < 0 || row_bytes < 16 || row_bytes % 16 != 0 || token_stride_bytes < row_bytes || token_stride_bytes % 16 != 0 ||
+      max_pages < 1 || page_size < 1 || path_cols < 1 || max_nodes < 1)
+    return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!kv || !page_table || !seq_base || !path_nodes || !num_accepted || !out_len) return SV_ERR_INVALID_ARG;
+  if (!aligned(kv, 16) || !aligned(page_table, 4) || !aligned(seq_base, 4) || !aligned(path_nodes, 4) ||
+      !aligned(num_accepted, 4) || !aligned(out_len, 4) || !aligned(out_status, 4))
+    return SV_ERR_INVALID_ARG;
+  KvCompactArgs k;
+  k.kv = static_cast<uint8_t*>(kv);
+  k.token_stride = token_stride_bytes;
+  k.page_bytes = static_cast<int64_t>(page_size) * token_stride_bytes;
+  k.row_bytes = row_bytes;
+  k.page_table = page_table;
+  k.max_pages = max_pages;
+  k.page_size = page_size;
+  k.seq_base = seq_base;
+  k.path_nodes = path_nodes;
+  k.path_cols = path_cols;
+  k.num_accepted = num_accepted;
+  k.max_nodes = max_nodes;
+  k.chunks = (row_bytes + kKvChunkBytes - 1) / kKvChunkBytes;
+  k.out_len = out_len;
+  k.out_status = out_status;
+  const int64_t grid = static_cast<int64_t>(B) * k.chunks;
+  if (grid > INT32_MAX) return SV_ERR_INVALID_ARG;
+  const cudaError_t e = launch(kv_compact_kernel, static_cast<int>(grid), kKvThreads, 0,
+                               static_cast<cudaStream_t>(stream), true, k);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -81,6 +81,7 @@ _SIGS = {
     "spec_tree_build_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
     "spec_tree_build": (_I32, [_P, _I32, _I64, _I32, _I32, _I32, _I32, _I32, _F,
                                _P, _P, _P, _P, _P, _SZ, _P]),
+    "spec_kv_compact": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _I32, _P, _I32, _I32, _P, _P, _P]),
     "spec_verify_greedy_ex": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                      _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_sample_ex": (_I32, [_P, _I32, _I64, _P, _I64, _P, _I32, _I32, _I32,
@@ -396,5 +397,33 @@ def spec_tree_build(draft_logits, depth, topk, n_nodes, temperature=1.0, workspa
                              float(temperature), _ptr(out["tokens"]), _ptr(out["parents"]),
                              _ptr(out["scores"]), _ptr(out["status"]),
                              _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+    _check(rc)
+    return out
+
+
+def spec_kv_compact(kv, page_table, seq_base, path_nodes, num_accepted, max_nodes, out=None):
+    """Move each request's accepted tree path into consecutive cache positions
+    (include/spec_verify.h). kv [pages, page_size, ...] CUDA tensor (modified
+    in place; each token row 16-byte multiple), page_table [B, max_pages],
+    seq_base [B], path_nodes [B, cols] (out_nodes of spec_verify_tree),
+    num_accepted [B]. Returns dict(out_len [B], status [B])."""
+    lib = load_library()
+    if not kv.is_cuda or kv.dim() < 3 or not kv.is_contiguous():
+        raise SpecVerifyError("kv must be a contiguous CUDA tensor [pages, page_size, ...]")
+    dev = kv.device
+    pages, P = kv.shape[0], kv.shape[1]
+    row_bytes = kv[0, 0].numel() * kv.element_size()
+    B = page_table.shape[0]
+    pt = _i32(page_table, "page_table", tuple(page_table.shape), dev)
+    sb = _i32(seq_base, "seq_base", (B,), dev)
+    pn = _i32(path_nodes, "path_nodes", tuple(path_nodes.shape), dev)
+    na = _i32(num_accepted, "num_accepted", (B,), dev)
+    if out is None:
+        out = dict(out_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                   status=torch.empty((B,), dtype=torch.int32, device=dev))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    rc = lib.spec_kv_compact(_ptr(kv), row_bytes, row_bytes, _ptr(pt), pt.shape[1], P, _ptr(sb), _ptr(pn),
+                             pn.shape[1], _ptr(na), B, int(max_nodes), _ptr(out["out_len"]), _ptr(out["status"]),
+                             ctypes.c_void_p(stream))
     _check(rc)
     return out
