@@ -22,7 +22,7 @@
 //   All N rows' statistics and every node's gathered logit (its token in its
 //   parent's row) are staged in shared memory; one thread then walks from the
 //   root over children in increasing index (nanospec README, tree
-//   configuration), with rest / branch probabilities in double.
+//   configuration), with rest kept as a compensated fp32 sum.
 #pragma once
 
 #include "finish.cuh"
@@ -115,6 +115,19 @@ __device__ __forceinline__ ChainIn load_chain_in(const ChainArgs& a, int b, int 
     }
   }
   return in;
+}
+
+// (hi, lo) <- (hi + lo) - p as an unevaluated sum: Knuth's TwoSum of hi and -p
+// (an error-free addition), with the old low part and the rounding error
+// carried in lo.
+__device__ __forceinline__ void two_sum_sub(float& hi, float& lo, float p) {
+  const float a = hi, b = -p;
+  const float s = a + b;
+  const float bb = s - a;
+  const float err = (a - (s - bb)) + (b - bb);
+  const float l = lo + err;
+  hi = s + l;
+  lo = l - (hi - s);
 }
 
 // Rank bound of chain row i (read after the wait: its kernel runs before K2).
@@ -440,11 +453,14 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
         ++depth;
         continue;
       }
-      double rest = 1.0, reach = 1.0;
+      // rest = 1 - (rejected mass) as an unevaluated fp32 sum rest_hi + rest_lo
+      // (TwoSum keeps it exact to ~1e-14 when the rejected mass nears 1; FP64
+      // latency on this GPU made a double walk several microseconds long)
+      float rest_hi = 1.f, rest_lo = 0.f, reach = 1.f;
       int nrej = 0, accepted = -1;
       for (; kid >= 0; kid = sm_next[kid]) {
         const int t = sm_tok[kid];
-        double acc = 0.0;
+        float acc = 0.f;
         float lp2 = -INFINITY;
         bool counted = false;
         if (t < 0 || t >= a.V) {
@@ -458,25 +474,23 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
             const float p = ex2(lp2);
             if (a.rule.rule == 1) {
               const float thr = a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * N + cur] : INFINITY;
-              acc = relaxed_accepts(a.rule, lp2, sm_g[kid], thr) ? 1.0 : 0.0;
+              acc = relaxed_accepts(a.rule, lp2, sm_g[kid], thr) ? 1.f : 0.f;
             } else {
-              // rest is kept in double (it cancels when the rejected mass is
-              // close to 1); the ratio itself needs only fp32
-              const float ratio = rest <= 0.0 ? 1.f : fminf(1.f, p / static_cast<float>(rest));
-              acc = (a.rule.rule == 2) ? static_cast<double>(exp2f(a.rule.alpha * log2f(ratio)))
-                                       : static_cast<double>(ratio);
+              const float rest = rest_hi + rest_lo;
+              const float ratio = rest <= 0.f ? 1.f : fminf(1.f, p / rest);
+              acc = (a.rule.rule == 2) ? exp2f(a.rule.alpha * log2f(ratio)) : ratio;
             }
-            rest -= static_cast<double>(p);
+            two_sum_sub(rest_hi, rest_lo, p);
           }
         }
-        if (static_cast<double>(sm_u[kid]) < acc) {
+        if (sm_u[kid] < acc) {
           accepted = kid;
           a.out_tokens[ob + depth] = t;
           if (a.out_logprob) a.out_logprob[ob + depth] = lp2 * kLn2;
-          if (a.out_mu) a.out_mu[ob + depth] = static_cast<float>(reach * acc);
+          if (a.out_mu) a.out_mu[ob + depth] = reach * acc;
           break;
         }
-        reach *= (1.0 - acc);
+        reach *= (1.f - acc);
         if (counted) excl[nrej++] = t;
       }
       if (accepted >= 0) {
@@ -492,7 +506,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
       d.u = sm_u[0];
       d.lp2 = sm_l2[cur];
       d.lq2 = 0.f;
-      d.scale = static_cast<float>(reach);
+      d.scale = reach;
       d.n_excl = nrej;
       d.pad0 = d.pad1 = d.pad2 = 0;
       a.draws[b] = d;

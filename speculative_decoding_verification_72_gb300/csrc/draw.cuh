@@ -11,7 +11,7 @@
 // issued before any arithmetic: 16-byte vectors when both rows are 16-byte
 // aligned and the CTA's range holds no removed token, else element-strided
 // scalars. The last CTA of request b forms the ordered prefix over the P chunk
-// sums in double, finds the chunk where u * S falls, recomputes that chunk's
+// sums (one warp, fp32 scans), finds the chunk where u * S falls, recomputes that chunk's
 // weights (just read, so L2-resident) into shared memory, and resolves the
 // smallest j whose inclusive prefix sum exceeds u * S with a block scan over
 // contiguous shared-memory segments. Per-element weights are recomputed by the
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   __shared__ int s_nex;
   __shared__ int s_last, s_chunk, s_usep, s_pick, s_lastpos;
   __shared__ float s_thr;
-  __shared__ double s_S;
+  __shared__ float s_S;
   __shared__ float2 s_part[kK3MaxChunks];
   __shared__ int s_fin[2];
 
@@ -368,51 +368,72 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
 
   // Last CTA of request b: the chunk sums are loaded together into shared
   // memory (a loop of dependent loads would pay one L2 round trip per
-  // chunk), then thread 0 forms their ordered prefix in double.
+  // chunk), then warp 0 finds the chunk holding u * S with fp32 warp scans,
+  // 32 chunks at a time (a serial fp64 prefix here cost ~9 us: FP64 latency
+  // is long on this GPU). fp32 adds at most a few ulps of S, far inside the
+  // 1e-5 * S band the comparison rules allow at a boundary.
   const float2* pp_g = a.part + static_cast<int64_t>(b) * a.P;
   for (int k = tid; k < a.P && k < kK3MaxChunks; k += kK3Threads) s_part[k] = __ldcg(&pp_g[k]);
   __syncthreads();
-  if (tid == 0) {
-    double S = 0.0;
-    for (int k = 0; k < a.P; ++k) S += static_cast<double>(chunk_sum(s_part, pp_g, k).x);
-    int usep = !(S > 0.0);
-    if (usep) {
-      S = 0.0;
-      for (int k = 0; k < a.P; ++k) S += static_cast<double>(chunk_sum(s_part, pp_g, k).y);
-    }
-    const double thr = static_cast<double>(d.u) * S;
-    double pre = 0.0;
-    int cstar = -1;
-    for (int k = 0; k < a.P; ++k) {
+  if (tid < 32) {
+    const int lane = tid;
+    float sw = 0.f, sp = 0.f;
+    for (int k = lane; k < a.P; k += 32) {
       const float2 v = chunk_sum(s_part, pp_g, k);
-      const double w = usep ? v.y : v.x;
-      if (pre + w > thr) {
-        cstar = k;
-        break;
-      }
-      pre += w;
+      sw += v.x;
+      sp += v.y;
     }
-    if (cstar < 0) {   // rounding left no crossing: last chunk with weight
-      double run = 0.0, pre_last = 0.0;
-      for (int k = 0; k < a.P; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sw += __shfl_xor_sync(0xffffffffu, sw, o);
+      sp += __shfl_xor_sync(0xffffffffu, sp, o);
+    }
+    const int usep = !(sw > 0.f);
+    const float S = usep ? sp : sw;
+    const float thr = d.u * S;
+    float run = 0.f, pre = 0.f, pre_last = 0.f;
+    int cstar = -1, last_pos = -1;
+    for (int base = 0; base < a.P; base += 32) {
+      const int k = base + lane;
+      float w = 0.f;
+      if (k < a.P) {
         const float2 v = chunk_sum(s_part, pp_g, k);
-        const double w = usep ? v.y : v.x;
-        if (w > 0.0) {
-          cstar = k;
-          pre_last = run;
-        }
-        run += w;
+        w = usep ? v.y : v.x;
       }
-      pre = pre_last;
-      if (cstar < 0) cstar = a.P - 1;
+      float incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const float excl = run + (incl - w);
+      const unsigned hit = __ballot_sync(0xffffffffu, k < a.P && excl + w > thr);
+      if (cstar < 0 && hit) {
+        const int l = __ffs(hit) - 1;
+        cstar = base + l;
+        pre = __shfl_sync(0xffffffffu, excl, l);
+      }
+      const unsigned pos = __ballot_sync(0xffffffffu, k < a.P && w > 0.f);
+      if (pos) {   // last chunk with weight so far (the fallback when rounding leaves no crossing)
+        const int l = 31 - __clz(pos);
+        last_pos = base + l;
+        pre_last = __shfl_sync(0xffffffffu, excl, l);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    s_chunk = cstar;
-    s_usep = usep;
-    s_thr = static_cast<float>(thr - pre);
-    s_S = S;
-    s_pick = INT_MAX;
-    s_lastpos = -1;
-    a.counters[b] = 0u;
+    if (cstar < 0) {
+      cstar = last_pos >= 0 ? last_pos : a.P - 1;
+      pre = last_pos >= 0 ? pre_last : 0.f;
+    }
+    if (lane == 0) {
+      s_chunk = cstar;
+      s_usep = usep;
+      s_thr = thr - pre;
+      s_S = S;
+      s_pick = INT_MAX;
+      s_lastpos = -1;
+      a.counters[b] = 0u;
+    }
   }
   __syncthreads();
 
@@ -499,7 +520,7 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
     if (a.out_logprob) a.out_logprob[o] = (x * a.c - d.lp2) * kLn2;
     if (a.out_mu) {
       float mu = p;
-      if (d.type == kDrawMaskedP) mu = static_cast<float>(static_cast<double>(d.scale) * p / s_S);
+      if (d.type == kDrawMaskedP) mu = d.scale * p / s_S;
       a.out_mu[o] = mu;
     }
   }

@@ -23,7 +23,7 @@
 //   (res_j = p_j when that mass is zero), which needs two full-row sums per
 //   emitted draft row. Grid = B x K x P CTAs; CTA (b, j, c) sums vocabulary
 //   chunk c of row j when j <= n_b, then takes a ticket; the last CTA of
-//   request b adds the chunk sums in order (double) and writes mu for
+//   request b adds the chunk sums in order and writes mu for
 //   positions 0..min(n_b, K-1), reading the draw at position n_b from K3's
 //   output.
 #pragma once
@@ -263,11 +263,11 @@ __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
   const int jmax = min(n, a.K - 1);
   for (int jj = tid; jj <= jmax; jj += kMuThreads) {
     const float2* pp = a.mpart + (static_cast<int64_t>(b) * a.K + jj) * a.P;
-    double keep = 0.0, rsum = 0.0;
+    float keep = 0.f, rsum = 0.f;   // fp32 (FP64 latency is long on this GPU); ~1e-6 relative
     for (int k = 0; k < a.P; ++k) {
       const float2 v = __ldcg(&pp[k]);
-      keep += static_cast<double>(v.x);
-      rsum += static_cast<double>(v.y);
+      keep += v.x;
+      rsum += v.y;
     }
     float lp2, lq2;
     row_lse2<ES>(a, b, jj, lp2, lq2);
@@ -278,10 +278,10 @@ __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
     const float y = Elem<ES>::load(a.dft + (static_cast<int64_t>(b) * a.K + jj) * a.dft_stride, t);
     const float lp = fmaf(x, a.c, -lp2), lq = fmaf(y, a.c, -lq2);
     const float thr_j = a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * a.K + jj] : INFINITY;
-    const double p = ex2(lp), q = ex2(lq);
-    const double res = rsum > 0.0 ? fmax(p - q, 0.0) / rsum : p;
-    const double mu = static_cast<double>(kept_mass(a.rule, lp, lq, x, thr_j)) + (1.0 - keep) * res;
-    if (a.out_mu) a.out_mu[o] = static_cast<float>(mu);
+    const float p = ex2(lp), q = ex2(lq);
+    const float res = rsum > 0.f ? fmaxf(p - q, 0.f) / rsum : p;
+    const float mu = kept_mass(a.rule, lp, lq, x, thr_j) + (1.f - keep) * res;
+    if (a.out_mu) a.out_mu[o] = mu;
   }
   if (tid == 0) a.counters[b] = 0u;
   if (a.fin.out_len) {   // this kernel ends the call
