@@ -72,7 +72,6 @@ struct ChainArgs {
   DrawDesc* draws;
   int32_t* excl;         // [B * excl_stride]
   int32_t excl_stride;
-  uint32_t* draw_counters;  // [B], zeroed here for K3's tickets
   uint32_t* mu_counters;    // [B], zeroed here for the mu pass's tickets (or nullptr)
   FinishArgs fin;           // stop / cap / counters (greedy: applied here)
   // Early-exit greedy calls (row_stats_early_kernel): one partial per row at
@@ -155,7 +154,6 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
 
   if (tid == 0) {
     s_status = 0;
-    if (a.draw_counters) a.draw_counters[b] = 0;
     if (a.mu_counters) a.mu_counters[b] = 0;
   }
   if (a.cta_bytes) {   // early-exit call: did any K1 CTA give up waiting?
@@ -346,7 +344,6 @@ struct TreeArgs {
   DrawDesc* draws;
   int32_t* excl;
   int32_t excl_stride;
-  uint32_t* draw_counters;
   FinishArgs fin;          // stop / cap / counters (greedy walk: applied here)
 };
 
@@ -406,7 +403,6 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   grid_dep_wait();
   grid_dep_launch();
 
-  if (tid == 0 && a.draw_counters) a.draw_counters[b] = 0;
   for (int n = tid; n < N; n += kK2Threads) {
     float m, s;
     int idx, err;

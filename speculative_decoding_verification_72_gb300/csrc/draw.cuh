@@ -4,18 +4,31 @@
 // nanospec README's tree and deterministic-draft rules draw from p with the
 // rejected tokens removed).
 //
-// Grid = B x Q CTAs; CTA (b, q) sums the weights w_j of vocabulary chunks
-// q*cpc .. q*cpc + cpc - 1 (kK3ChunkElems elements each) of request b's row
-// (and, for the zero-mass fallback, sum p_j), one sum pair per chunk, and
-// takes a ticket. Chunks are read two at a time with every load of the pair
-// issued before any arithmetic: 16-byte vectors when both rows are 16-byte
-// aligned and the CTA's range holds no removed token, else element-strided
-// scalars. The last CTA of request b forms the ordered prefix over the P chunk
-// sums (one warp, fp32 scans), finds the chunk where u * S falls, recomputes that chunk's
-// weights (just read, so L2-resident) into shared memory, and resolves the
-// smallest j whose inclusive prefix sum exceeds u * S with a block scan over
-// contiguous shared-memory segments. Per-element weights are recomputed by the
-// same code in both passes.
+// The draw is an inverse CDF over the row's weights w_j in index order. It
+// runs as two kernels:
+//
+//  * draw_sum_kernel (K3a) streams the drawn rows once and writes, per
+//    request b and vocabulary chunk k (kK3ChunkBytes of each row), the pair
+//    (sum w, sum p) over the chunk. It is persistent and warp-specialized like
+//    the row-statistics pass: the B * P (request, chunk) items are split into
+//    equal contiguous ranges, one per CTA; warp 0's lane 0 copies each item's
+//    target chunk (and draft chunk for a residual) into a 6-stage
+//    shared-memory ring with 1-D bulk copies (TMA), and 7 consumer warps sum
+//    the weights from shared memory. The last consumer warp to finish an item
+//    merges the warps' sums in a fixed order and writes them, so no warp waits
+//    for another. Copies cover the 16-byte-aligned hull of a chunk (clipped to
+//    the caller's buffer); elements outside the chunk are skipped and the few
+//    elements a clipped hull misses are read from global memory.
+//  * draw_pick_kernel (K3b), one CTA per request, forms the ordered prefix of
+//    the chunk sums with fp32 warp scans, finds the chunk where u * S falls,
+//    loads that chunk (one 16-byte vector per thread and row, so each thread
+//    owns a contiguous run of elements), and resolves the smallest j whose
+//    inclusive prefix sum exceeds u * S with a block scan. The drawn token's
+//    logit stays in the picking thread's registers for the log-prob and mu.
+//
+// Per-element weights come from weight_of in both kernels. A wait that gives
+// up marks every chunk sum of the CTA's range NaN; the pick kernel then
+// reports status bit 32 for that request.
 #pragma once
 
 #include "finish.cuh"
@@ -23,360 +36,500 @@
 
 namespace sv {
 
-constexpr int kK3Threads = 256;
-constexpr int kK3PerThread = 16;                          // elements per thread per chunk
-constexpr int kK3ChunkElems = kK3Threads * kK3PerThread;  // 4096
-constexpr int kK3SegStride = kK3PerThread + 1;           // padded shared-memory segment
-constexpr int kK3LocalExcl = 64;
-// Chunk sums staged in shared memory by the last CTA (V up to 1M elements;
-// beyond that the rest are read from global memory).
-constexpr int kK3MaxChunks = 256;
-// Chunks one CTA sums in pass 1: its loads for all of them are in flight at
-// once (64 data registers per thread for fp32 with draft rows).
-template <int ES>
-constexpr int kK3Cpc = ES == 2 ? 4 : 2;
-constexpr int kK3MaxCpc = 4;
+constexpr int kK3Consumers = 7;
+constexpr int kK3Threads = 32 * (kK3Consumers + 1);
+constexpr int kK3ConsumerThreads = 32 * kK3Consumers;
+constexpr int kK3CtasPerSm = 2;
+constexpr int kK3ChunkBytes = 16384;                   // per row and chunk
+constexpr int kK3SlotBytes = kK3ChunkBytes + 32;      // a chunk's 16-byte hull
+constexpr int kK3Stages = 6;
+constexpr int kK3SmemBytes = kK3Stages * kK3SlotBytes;
+constexpr int kK3Req = 8;           // requests whose descriptor and exclusions a CTA caches
+constexpr int kK3LocalExcl = 64;    // exclusions cached per request
+constexpr int kK3MaxChunks = 256;   // chunk sums the pick kernel stages in shared memory
+constexpr int kK3PickThreads = 1024;
+constexpr int kStatusWaitErr = 32;
 
-__device__ __forceinline__ float2 chunk_sum(const float2* s_part, const float2* g_part, int k) {
-  return k < kK3MaxChunks ? s_part[k] : __ldcg(&g_part[k]);
-}
+template <int ES>
+constexpr int kK3ChunkElems = kK3ChunkBytes / ES;
+// Elements one pick thread owns in the chosen chunk: one 16-byte vector.
+template <int ES>
+constexpr int kK3PickElems = kK3ChunkElems<ES> / kK3PickThreads;
 
 struct DrawArgs {
   const uint8_t* tgt;
   int64_t tgt_stride;   // bytes
+  uintptr_t tgt_lo, tgt_hi;   // bytes the target buffer holds
   const uint8_t* dft;
   int64_t dft_stride;   // bytes
+  uintptr_t dft_lo, dft_hi;
   int32_t V, P, chunk_elems;
-  int32_t Q;            // CTAs per request: ceil(P / kK3Cpc<ES>)
+  int32_t B;
+  int32_t G;            // K3a CTAs
   float c;              // log2(e) / T
   const DrawDesc* draws;
   const int32_t* excl;
   int32_t excl_stride;
   float2* part;         // [B * P]: (sum w, sum p)
-  uint32_t* counters;   // [B], zeroed by K2 of the same call
   int32_t out_cols;
   int32_t* out_tokens;
   float* out_logprob;
   float* out_mu;
   int32_t* out_nodes;    // tree calls, else nullptr
   int32_t* out_status;
-  FinishArgs fin;        // applied by the last CTA of a request when fin_here
+  FinishArgs fin;        // applied by the pick kernel when fin_here
   int32_t fin_here;
 };
 
-template <int ES>
-struct DrawRow {
-  const uint8_t* t;
-  const uint8_t* d;   // nullptr unless kDrawResid
-  float c, lp2, lq2;
-  __device__ __forceinline__ void weight(int j, float& w, float& p) const {
-    const float x = Elem<ES>::load(t, j);
-    p = ex2(fmaf(x, c, -lp2));
-    if (d) {
-      const float q = ex2(fmaf(Elem<ES>::load(d, j), c, -lq2));
-      w = fmaxf(p - q, 0.f);
-    } else {
-      w = p;
-    }
-  }
-};
-
-__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < kK3Threads / 32; ++w) t += red[w];
-  return t;   // valid in thread 0
-}
-
-// Load the exclusions that fall in [lo, hi) into shared memory; returns the
-// count (a value above kK3LocalExcl means "use the global list").
-__device__ __forceinline__ int gather_excl(const DrawDesc& d, const int32_t* ex, int lo, int hi,
-                                           int* s_ex, int* s_nex) {
-  __syncthreads();
-  if (threadIdx.x == 0) *s_nex = 0;
-  __syncthreads();
-  if (d.type == kDrawMaskedP) {
-    for (int k = threadIdx.x; k < d.n_excl; k += kK3Threads) {
-      const int t = ex[k];
-      if (t >= lo && t < hi) {
-        const int slot = atomicAdd(s_nex, 1);
-        if (slot < kK3LocalExcl) s_ex[slot] = t;
-      }
-    }
-  }
-  __syncthreads();
-  return *s_nex;
-}
-
-__device__ __forceinline__ bool is_excluded(int j, int nex, const int* s_ex, const int32_t* ex,
-                                            int n_all) {
-  if (nex == 0) return false;
-  if (nex <= kK3LocalExcl) {
-    for (int k = 0; k < nex; ++k)
-      if (s_ex[k] == j) return true;
-    return false;
-  }
-  for (int k = 0; k < n_all; ++k)
-    if (ex[k] == j) return true;
-  return false;
-}
-
-// Weights of one element from its logits (same arithmetic as DrawRow::weight).
+// Weights of one element from its logits: p = 2^(x c - lp2), w = relu(p - q)
+// for a residual, else p.
 __device__ __forceinline__ void weight_of(float x, float y, bool resid, float c, float lp2, float lq2,
                                           float& w, float& p) {
   p = ex2(fmaf(x, c, -lp2));
   w = resid ? fmaxf(p - ex2(fmaf(y, c, -lq2)), 0.f) : p;
 }
 
-// Pass 1 of one CTA: the (w, p) sums of its kK3Cpc<ES> chunks c0, c0 + 1, ...
-// (those below c_end), in acc[2 * i], acc[2 * i + 1]. When both rows are
-// 16-byte aligned every load is issued before any arithmetic, so a CTA pays
-// one memory round trip (16-byte vectors, chunk-relative vector
-// t + k * kK3Threads of thread t; the row's last partial vector element by
-// element). A vector holding a removed token is left out of that loop and
-// summed afterwards element by element. Unaligned rows take element-strided
-// scalar loads, one chunk at a time.
-template <int ES>
-struct Pass1 {
-  static constexpr int N = Elem<ES>::kVec;
-  static constexpr int VPT = kK3ChunkElems / N / kK3Threads;   // vectors per thread per chunk
-  static constexpr int C = kK3Cpc<ES>;
+// ------------------------------------------------------------------ K3a
 
-  __device__ __forceinline__ static void vec(const DrawRow<ES>& row, int c0, int c_end, int V, int chunk,
-                                             int nex, const int* s_ex, const int32_t* ex, int n_all,
-                                             float (&acc)[2 * C]) {
-    const bool resid = row.d != nullptr;
-    uint4 xv[C][VPT], yv[C][VPT];
-    const uint4* tv = reinterpret_cast<const uint4*>(row.t + static_cast<int64_t>(c0) * chunk * ES);
-    const uint4* dv = resid ? reinterpret_cast<const uint4*>(row.d + static_cast<int64_t>(c0) * chunk * ES) : nullptr;
-    const int nfull = (min(V, c_end * chunk) - c0 * chunk) / N;   // whole vectors in the range
-    constexpr int kChunkVecs = kK3ChunkElems / N;
-    // Bit i * VPT + k: this thread's vector k of chunk c0 + i holds a removed token.
-    uint32_t exmask = 0u;
-    if (nex) {
-      const int n_list = nex <= kK3LocalExcl ? nex : n_all;
-      for (int r = 0; r < n_list; ++r) {
-        const int v = ((nex <= kK3LocalExcl ? s_ex[r] : ex[r]) - c0 * chunk);
-        if (v < 0 || v >= nfull * N) continue;
-        const int vv = v / N, i = vv / kChunkVecs, vc = vv - i * kChunkVecs;
-        if (vc % kK3Threads == static_cast<int>(threadIdx.x)) exmask |= 1u << (i * VPT + vc / kK3Threads);
-      }
-    }
+// One copied row chunk, as the producer describes it to the consumers. A
+// masked draw's excluded tokens that fall in the chunk travel with it (the
+// first kStageExcl; with more, consumers scan the request's whole list).
+constexpr int kStageExcl = 4;
+struct StageDesc {
+  const uint8_t* rowp;   // row start
+  const int32_t* xl;     // the request's exclusion list (shared or global memory)
+  int32_t item;          // b * P + k; -1 ends the stream
+  int32_t e0;            // row index of the copy's first element (may precede the chunk)
+  int32_t nel;           // elements copied (0: nothing copied)
+  int32_t type;          // DrawType
+  int32_t nx;            // excluded tokens inside the chunk
+  int32_t nxl;           // length of xl
+  float lp2, lq2;
+  int32_t x[kStageExcl];
+};
+
+// 16-byte-aligned hull of elements [lo, hi) of a row, clipped to [safe_lo, safe_hi).
+template <int ES>
+__device__ __forceinline__ void chunk_hull(const uint8_t* rowp, int lo, int hi, uintptr_t safe_lo,
+                                           uintptr_t safe_hi, uintptr_t& clo, uint32_t& bytes, int& e0) {
+  const uintptr_t L = reinterpret_cast<uintptr_t>(rowp) + static_cast<uintptr_t>(lo) * ES;
+  const uintptr_t H = reinterpret_cast<uintptr_t>(rowp) + static_cast<uintptr_t>(hi) * ES;
+  uintptr_t a = L & ~static_cast<uintptr_t>(15);
+  if (a < safe_lo) a = (L + 15) & ~static_cast<uintptr_t>(15);
+  uintptr_t z = (H + 15) & ~static_cast<uintptr_t>(15);
+  if (z > safe_hi) z = H & ~static_cast<uintptr_t>(15);
+  if (z <= a) {
+    clo = 0;
+    bytes = 0;
+    e0 = lo;
+    return;
+  }
+  clo = a;
+  bytes = static_cast<uint32_t>(z - a);
+  e0 = static_cast<int>((static_cast<int64_t>(a) - static_cast<int64_t>(reinterpret_cast<uintptr_t>(rowp))) / ES);
+}
+
+// Element j of a row from its stage copy when the copy holds it, else from
+// global memory.
+template <int ES>
+__device__ __forceinline__ float stage_elem(const uint8_t* sm, const StageDesc& s, int j) {
+  const int k = j - s.e0;
+  if (k >= 0 && k < s.nel) {
+    if constexpr (ES == 4) return reinterpret_cast<const float*>(sm)[k];
+    else return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(sm)[k]) << 16);
+  }
+  return Elem<ES>::load(s.rowp, j);
+}
+
+// Bit e set when element jv + e (e < n) is on the list.
+__device__ __forceinline__ uint32_t excl_bits(int jv, int n, int nex, const int* lst) {
+  uint32_t m = 0u;
+  for (int r = 0; r < nex; ++r) {
+    const unsigned d = static_cast<unsigned>(lst[r] - jv);
+    if (d < static_cast<unsigned>(n)) m |= 1u << d;
+  }
+  return m;
+}
+
+__device__ __forceinline__ bool stage_excludes(const StageDesc& s, int j) {
+  if (s.nx <= kStageExcl) {
+    bool hit = false;
 #pragma unroll
-    for (int i = 0; i < C; ++i) {
+    for (int r = 0; r < kStageExcl; ++r) hit |= (r < s.nx && s.x[r] == j);
+    return hit;
+  }
+  return excl_bits(j, 1, s.nxl, s.xl) != 0u;
+}
+
+// A pair of elements as two floats (bf16: one 32-bit word; fp32: two).
+template <int ES>
+__device__ __forceinline__ float2 pair_of(const uint4& q, int i) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if constexpr (ES == 2) return make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  else return make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+}
+
+// The (sum w, sum p) share of consumer thread ct over one copied chunk
+// [lo, hi). Vectors wholly inside the chunk and free of excluded tokens take
+// the packed fp32x2 path (the same per-element arithmetic as weight_of, two
+// lanes at a time); the chunk's edge vectors and those holding an excluded
+// token go element by element.
+template <int ES, bool RESID>
+__device__ __forceinline__ void sum_stage(const StageDesc& ts, const StageDesc& ds, const uint8_t* tsm,
+                                          const uint8_t* dsm, int lo, int hi, int ct, float c, float& sw,
+                                          float& sp) {
+  constexpr int N = Elem<ES>::kVec;
+  const uint4* tv = reinterpret_cast<const uint4*>(tsm);
+  const uint4* dv = reinterpret_cast<const uint4*>(dsm);
+  const float2 c2 = make_float2(c, c);
+  const float2 nlp = make_float2(-ts.lp2, -ts.lp2);
+  const float2 nlq = make_float2(-ts.lq2, -ts.lq2);
+  float2 accp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 accw[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float sws = 0.f, sps = 0.f;
+  if (!RESID || (ds.e0 == ts.e0 && ds.nel == ts.nel)) {
+    // (for a residual the draft copy holds the same elements at the same places)
+    const int nv = ts.nel / N;
+    const int dlo = lo - ts.e0, dhi = hi - ts.e0;
+    const int v_lo = dlo <= 0 ? 0 : (dlo + N - 1) / N;
+    const int v_hi = min(nv, dhi / N);
+    const bool all_slow = ts.nx > kStageExcl;
+    uint32_t xmask = 0u;   // bit i: this thread's i-th vector holds an excluded token
+    if (!all_slow) {
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int v = i * kChunkVecs + static_cast<int>(threadIdx.x) + k * kK3Threads;
-        xv[i][k] = make_uint4(0u, 0u, 0u, 0u);
-        yv[i][k] = make_uint4(0u, 0u, 0u, 0u);
-        if (v < nfull) {
-          xv[i][k] = __ldg(tv + v);
-          if (resid) yv[i][k] = __ldg(dv + v);
+      for (int r = 0; r < kStageExcl; ++r) {
+        const int d = ts.x[r] - ts.e0;
+        if (r < ts.nx && d >= 0) {
+          const int vt = d / N;
+          if (vt < nv && vt % kK3ConsumerThreads == ct) xmask |= 1u << (vt / kK3ConsumerThreads);
         }
       }
     }
+    int i = 0;
+    for (int v = ct; v < nv; v += kK3ConsumerThreads, ++i) {
+      if (!all_slow && v >= v_lo && v < v_hi && !((xmask >> i) & 1u)) {
+        const uint4 xq = tv[v];
+        uint4 yq;
+        if (RESID) yq = dv[v];
 #pragma unroll
-    for (int i = 0; i < C; ++i) {
-      float sw = 0.f, sp = 0.f;
+        for (int h = 0; h < N / 2; ++h) {
+          const float2 t = __ffma2_rn(pair_of<ES>(xq, h), c2, nlp);
+          const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+          accp[h & 1] = __fadd2_rn(accp[h & 1], pp);
+          if (RESID) {
+            const float2 u = __ffma2_rn(pair_of<ES>(yq, h), c2, nlq);
+            const float2 w = make_float2(fmaxf(pp.x - ex2(u.x), 0.f), fmaxf(pp.y - ex2(u.y), 0.f));
+            accw[h & 1] = __fadd2_rn(accw[h & 1], w);
+          }
+        }
+      } else {
+        const int jv = ts.e0 + v * N;
+        float xf[N], yf[N];
+        Elem<ES>::unpack(tv[v], xf);
+        if (RESID) Elem<ES>::unpack(dv[v], yf);
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        if (i * kChunkVecs + static_cast<int>(threadIdx.x) + k * kK3Threads < nfull &&
-            !((exmask >> (i * VPT + k)) & 1u)) {
-          float xf[N], yf[N];
-          Elem<ES>::unpack(xv[i][k], xf);
-          Elem<ES>::unpack(yv[i][k], yf);
-#pragma unroll
-          for (int e = 0; e < N; ++e) {
+        for (int e = 0; e < N; ++e) {
+          const int j = jv + e;
+          if (j >= lo && j < hi) {
             float w, p;
-            weight_of(xf[e], yf[e], resid, row.c, row.lp2, row.lq2, w, p);
-            sw += w;
-            sp += p;
+            weight_of(xf[e], RESID ? yf[e] : 0.f, RESID, c, ts.lp2, ts.lq2, w, p);
+            if (!RESID && ts.nx && stage_excludes(ts, j)) w = 0.f;
+            sws += w;
+            sps += p;
           }
         }
       }
-      acc[2 * i] = sw;
-      acc[2 * i + 1] = sp;
     }
-    // vectors holding a removed token, element by element
-#pragma unroll 1
-    while (exmask) {
-      const int bit = __ffs(exmask) - 1;
-      exmask &= exmask - 1u;
-      const int i = bit / VPT, k = bit - i * VPT;
-      const int j0 = (c0 + i) * chunk + (static_cast<int>(threadIdx.x) + k * kK3Threads) * N;
-      float sw = 0.f, sp = 0.f;
-#pragma unroll 1
-      for (int e = 0; e < N; ++e) {
-        float w, p;
-        row.weight(j0 + e, w, p);
-        if (is_excluded(j0 + e, nex, s_ex, ex, n_all)) w = 0.f;
-        sw += w;
-        sp += p;
-      }
-#pragma unroll
-      for (int q = 0; q < C; ++q)
-        if (q == i) {
-          acc[2 * q] += sw;
-          acc[2 * q + 1] += sp;
-        }
-    }
-    // elements after the last whole vector (fewer than N), in the last chunk
-    const int jt = c0 * chunk + nfull * N + static_cast<int>(threadIdx.x);
-    if (static_cast<int>(threadIdx.x) < N && jt < min(V, c_end * chunk)) {
+    // Elements of the chunk the (clipped) copy does not hold, from global memory.
+    const int c_lo = ts.nel ? max(lo, ts.e0) : hi;
+    const int c_hi = ts.nel ? min(hi, ts.e0 + ts.nel) : hi;
+    int j = -1;
+    if (ct < c_lo - lo) j = lo + ct;
+    else if (ct - (c_lo - lo) < hi - c_hi) j = c_hi + ct - (c_lo - lo);
+    if (j >= 0 && j < hi && (j < c_lo || j >= c_hi)) {
       float w, p;
-      row.weight(jt, w, p);
-      if (nex && is_excluded(jt, nex, s_ex, ex, n_all)) w = 0.f;
-      const int i = (jt - c0 * chunk) / chunk;
-#pragma unroll
-      for (int q = 0; q < C; ++q)
-        if (q == i) {
-          acc[2 * q] += w;
-          acc[2 * q + 1] += p;
-        }
+      const float x = Elem<ES>::load(ts.rowp, j);
+      const float y = RESID ? Elem<ES>::load(ds.rowp, j) : 0.f;
+      weight_of(x, y, RESID, c, ts.lp2, ts.lq2, w, p);
+      if (!RESID && ts.nx && stage_excludes(ts, j)) w = 0.f;
+      sws += w;
+      sps += p;
+    }
+  } else {
+    // Target and draft copies hold different element ranges: element by element.
+    for (int j = lo + ct; j < hi; j += kK3ConsumerThreads) {
+      float w, p;
+      weight_of(stage_elem<ES>(tsm, ts, j), stage_elem<ES>(dsm, ds, j), true, c, ts.lp2, ts.lq2, w, p);
+      sws += w;
+      sps += p;
     }
   }
-
-  // Scalar variant, one chunk at a time: element j = chunk start + t + k * kK3Threads.
-  __device__ __forceinline__ static void scalar(const DrawRow<ES>& row, int c0, int c_end, int V, int chunk,
-                                                int nex, const int* s_ex, const int32_t* ex, int n_all,
-                                                float (&acc)[2 * C]) {
-    const bool resid = row.d != nullptr;
-#pragma unroll
-    for (int q = 0; q < 2 * C; ++q) acc[q] = 0.f;
-#pragma unroll 1
-    for (int i = 0; i < C && c0 + i < c_end; ++i) {
-      const int lo = (c0 + i) * chunk, hi = min(V, lo + chunk);
-      float xs[kK3PerThread], ys[kK3PerThread];
-#pragma unroll
-      for (int k = 0; k < kK3PerThread; ++k) {
-        const int j = lo + static_cast<int>(threadIdx.x) + k * kK3Threads;
-        xs[k] = -INFINITY;
-        ys[k] = -INFINITY;
-        if (j < hi) {
-          xs[k] = Elem<ES>::load(row.t, j);
-          if (resid) ys[k] = Elem<ES>::load(row.d, j);
-        }
-      }
-      float sw = 0.f, sp = 0.f;
-#pragma unroll
-      for (int k = 0; k < kK3PerThread; ++k) {
-        const int j = lo + static_cast<int>(threadIdx.x) + k * kK3Threads;
-        if (j < hi) {
-          float w, p;
-          weight_of(xs[k], ys[k], resid, row.c, row.lp2, row.lq2, w, p);
-          if (nex && is_excluded(j, nex, s_ex, ex, n_all)) w = 0.f;
-          sw += w;
-          sp += p;
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < C; ++q)
-        if (q == i) {
-          acc[2 * q] = sw;
-          acc[2 * q + 1] = sp;
-        }
-    }
-  }
-};
-
-// Reduce 2 * C per-thread values over the CTA (fixed order); valid in thread 0.
-template <int C>
-__device__ __forceinline__ void block_sum_n(float (&v)[2 * C], float* red_n) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int q = 0; q < 2 * C; ++q) v[q] += __shfl_down_sync(0xffffffffu, v[q], off);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0)
-#pragma unroll
-    for (int q = 0; q < 2 * C; ++q) red_n[warp * 2 * C + q] = v[q];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int q = 0; q < 2 * C; ++q) {
-      float t = 0.f;
-      for (int w = 0; w < kK3Threads / 32; ++w) t += red_n[w * 2 * C + q];
-      v[q] = t;
-    }
+  const float2 ap = __fadd2_rn(accp[0], accp[1]);
+  sp = (ap.x + ap.y) + sps;
+  if (RESID) {
+    const float2 aw = __fadd2_rn(accw[0], accw[1]);
+    sw = (aw.x + aw.y) + sws;
+  } else {
+    sw = (ap.x + ap.y) + sws;   // w = p away from excluded tokens
   }
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
-  __shared__ int s_stop_pre[kMaxStopIds];
-  FinishPre fpre;
-  if (a.fin_here) finish_prefetch(a.fin, blockIdx.x / a.Q, s_stop_pre, fpre);
-  grid_dep_wait();
+__global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(const DrawArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full_bar[kK3Stages];
+  __shared__ __align__(8) uint64_t empty_bar[kK3Stages];
+  __shared__ StageDesc sdesc[kK3Stages];
+  __shared__ float2 red[kK3Stages][kK3Consumers];
+  __shared__ int red_cnt[kK3Stages];
+  __shared__ DrawDesc s_desc[kK3Req];
+  __shared__ int s_ex[kK3Req][kK3LocalExcl];
+  __shared__ int s_err;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t n_items = static_cast<int64_t>(a.B) * a.P;
+  const int64_t i0 = n_items * blockIdx.x / a.G;
+  const int64_t i1 = n_items * (blockIdx.x + 1) / a.G;
+  const int b_first = static_cast<int>(i0 / a.P);
+
+  grid_dep_wait();   // the draw descriptors come from the decide kernel
   grid_dep_launch();
-  __shared__ float red_n[kK3Threads / 32 * 2 * kK3MaxCpc];
-  __shared__ float scan_w[kK3Threads / 32];
-  __shared__ float seg[kK3Threads * kK3SegStride];
-  __shared__ int s_ex[kK3LocalExcl];
-  __shared__ int s_nex;
-  __shared__ int s_last, s_chunk, s_usep, s_pick, s_lastpos;
-  __shared__ float s_thr;
-  __shared__ float s_S;
+
+  // Descriptors and exclusion lists of the first kK3Req requests of the range.
+  const int nreq = min(kK3Req, static_cast<int>((i1 - 1) / a.P) - b_first + 1);
+  if (tid < nreq) s_desc[tid] = a.draws[b_first + tid];
+  for (int x = tid; x < nreq * kK3LocalExcl; x += kK3Threads) {
+    const int r = x / kK3LocalExcl, e = x - r * kK3LocalExcl;
+    if (e < a.excl_stride) s_ex[r][e] = a.excl[static_cast<int64_t>(b_first + r) * a.excl_stride + e];
+  }
+  if (tid < kK3Stages) red_cnt[tid] = 0;
+  if (tid == 0) {
+    s_err = 0;
+    for (int i = 0; i < kK3Stages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), kK3Consumers);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int st = 0, slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int b = b_first, k = static_cast<int>(i0 - static_cast<int64_t>(b_first) * a.P);
+      // Claim the next slot (its previous use released) and describe it.
+      auto claim = [&](const StageDesc& sd) -> bool {
+        if (st >= kK3Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) return false;
+        sdesc[slot] = sd;
+        return true;
+      };
+      auto advance = [&]() {
+        ++st;
+        if (++slot == kK3Stages) {
+          slot = 0;
+          phase ^= 1;
+        }
+      };
+      for (int64_t i = i0; i < i1 && ok; ++i) {
+        const int r = b - b_first;
+        const DrawDesc d = r < kK3Req ? s_desc[r] : a.draws[b];
+        if (d.type != kDrawNone) {
+          const int lo = k * a.chunk_elems;
+          const int hi = min(a.V, lo + a.chunk_elems);
+          StageDesc sd;
+          sd.item = static_cast<int32_t>(i);
+          sd.type = d.type;
+          sd.lp2 = d.lp2;
+          sd.lq2 = d.lq2;
+          sd.nx = 0;
+          sd.nxl = d.type == kDrawMaskedP ? d.n_excl : 0;
+          sd.xl = (r < kK3Req && sd.nxl <= kK3LocalExcl) ? s_ex[r] : a.excl + static_cast<int64_t>(b) * a.excl_stride;
+#pragma unroll
+          for (int q = 0; q < kStageExcl; ++q) sd.x[q] = -1;
+          for (int q = 0; q < sd.nxl; ++q) {
+            const int t = sd.xl[q];
+            if (t >= lo && t < hi) {
+#pragma unroll
+              for (int u = 0; u < kStageExcl; ++u)
+                if (sd.nx == u) sd.x[u] = t;
+              ++sd.nx;
+            }
+          }
+          const int nrow = d.type == kDrawResid ? 2 : 1;
+          for (int h = 0; h < nrow && ok; ++h) {
+            sd.rowp = h == 0 ? a.tgt + static_cast<int64_t>(d.t_row) * a.tgt_stride
+                             : a.dft + static_cast<int64_t>(d.d_row) * a.dft_stride;
+            uintptr_t clo;
+            uint32_t bytes;
+            chunk_hull<ES>(sd.rowp, lo, hi, h == 0 ? a.tgt_lo : a.dft_lo, h == 0 ? a.tgt_hi : a.dft_hi, clo,
+                           bytes, sd.e0);
+            sd.nel = static_cast<int32_t>(bytes / ES);
+            if (!claim(sd)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&full_bar[slot]);
+            mbar_arrive_expect_tx(fb, bytes);
+            if (bytes) bulk_g2s(smem_u32(ring + slot * kK3SlotBytes), reinterpret_cast<const void*>(clo), bytes, fb);
+            advance();
+          }
+        }
+        if (++k == a.P) {
+          k = 0;
+          ++b;
+        }
+      }
+      bool ended = false;
+      if (ok) {   // end of stream: a descriptor with no copy
+        StageDesc sd;
+        sd.rowp = nullptr;
+        sd.xl = nullptr;
+        sd.item = -1;
+        sd.e0 = sd.nel = sd.type = sd.nx = sd.nxl = 0;
+        sd.lp2 = sd.lq2 = 0.f;
+        if (claim(sd)) {
+          mbar_arrive(smem_u32(&full_bar[slot]));
+          ended = true;
+        } else {
+          ok = false;
+        }
+      }
+      if (!ok) atomicOr(&s_err, 1);
+      // Copies still in flight (among the last kK3Stages issued) land before
+      // the CTA exits. The end marker reused the slot of stage st - kK3Stages
+      // after its release, so that copy has landed (and its parity is taken).
+      for (int q = max(0, st - kK3Stages + (ended ? 1 : 0)); q < st; ++q)
+        (void)mbar_wait_bounded(smem_u32(&full_bar[q % kK3Stages]), (q / kK3Stages) & 1);
+    }
+    __syncwarp();   // the whole warp reaches the block barrier below together
+  } else {
+    // -------------------------------------------------------------- consumers
+    const int ct = tid - 32;
+    const int cw = warp - 1;
+    int slot = 0;
+    uint32_t phase = 0;
+    while (true) {
+      if (!mbar_wait_bounded(smem_u32(&full_bar[slot]), phase)) {
+        atomicOr(&s_err, 1);
+        break;
+      }
+      const StageDesc ts = sdesc[slot];
+      if (ts.item < 0) break;
+      const bool resid = ts.type == kDrawResid;
+      int slot2 = slot + 1;
+      uint32_t phase2 = phase;
+      if (slot2 == kK3Stages) {
+        slot2 = 0;
+        phase2 ^= 1;
+      }
+      StageDesc ds = ts;
+      if (resid) {
+        if (!mbar_wait_bounded(smem_u32(&full_bar[slot2]), phase2)) {
+          atomicOr(&s_err, 1);
+          break;
+        }
+        ds = sdesc[slot2];
+      }
+      const int kc = ts.item % a.P;
+      const int lo = kc * a.chunk_elems;
+      const int hi = min(a.V, lo + a.chunk_elems);
+      float sw, sp;
+      if (resid)
+        sum_stage<ES, true>(ts, ds, ring + slot * kK3SlotBytes, ring + slot2 * kK3SlotBytes, lo, hi, ct, a.c, sw, sp);
+      else
+        sum_stage<ES, false>(ts, ds, ring + slot * kK3SlotBytes, ring + slot * kK3SlotBytes, lo, hi, ct, a.c, sw, sp);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sw += __shfl_xor_sync(0xffffffffu, sw, o);
+        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+      }
+      int merger = 0;
+      if (lane == 0) {
+        red[slot][cw] = make_float2(sw, sp);
+        __threadfence_block();
+        merger = atomicAdd(&red_cnt[slot], 1) == kK3Consumers - 1;
+      }
+      if (__shfl_sync(0xffffffffu, merger, 0)) {
+        __threadfence_block();
+        float2 v = lane < kK3Consumers ? red[slot][lane] : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        }
+        if (lane == 0) {
+          atomicExch(&red_cnt[slot], 0);
+          a.part[ts.item] = v;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&empty_bar[slot]));
+        if (resid) mbar_arrive(smem_u32(&empty_bar[slot2]));
+      }
+      slot = resid ? slot2 : slot;
+      phase = resid ? phase2 : phase;
+      if (++slot == kK3Stages) {
+        slot = 0;
+        phase ^= 1;
+      }
+    }
+  }
+  __syncthreads();
+  if (s_err) {   // this CTA's sums are not to be trusted
+    const float nan = __int_as_float(0x7fc00000);
+    for (int64_t i = i0 + tid; i < i1; i += kK3Threads) a.part[i] = make_float2(nan, nan);
+  }
+}
+
+// ------------------------------------------------------------------ K3b
+
+__device__ __forceinline__ float2 chunk_sum(const float2* s_part, const float2* g_part, int k) {
+  return k < kK3MaxChunks ? s_part[k] : __ldcg(&g_part[k]);
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kK3PickThreads) draw_pick_kernel(const DrawArgs a) {
+  constexpr int E = kK3PickElems<ES>;
+  constexpr int N = Elem<ES>::kVec;
+  static_assert(E == N, "a pick thread owns one 16-byte vector of each row");
+  constexpr int kWarps = kK3PickThreads / 32;
+  __shared__ int s_stop_pre[kMaxStopIds];
   __shared__ float2 s_part[kK3MaxChunks];
+  __shared__ int s_ex[kK3LocalExcl];
+  __shared__ float scan_w[kWarps];
+  __shared__ int s_chunk, s_usep, s_pick, s_lastpos;
+  __shared__ float s_thr, s_S;
   __shared__ int s_fin[2];
 
   const int tid = threadIdx.x;
-  const int b = blockIdx.x / a.Q;
-  const int q = blockIdx.x - b * a.Q;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x;
+  FinishPre fpre;
+  if (a.fin_here) finish_prefetch(a.fin, b, s_stop_pre, fpre);
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // The descriptor, the chunk sums and the exclusion list, loaded together.
   const DrawDesc d = a.draws[b];
-  if (d.type == kDrawNone) return;
-  const int32_t* ex = a.excl + static_cast<int64_t>(b) * a.excl_stride;
-  DrawRow<ES> row;
-  row.t = a.tgt + static_cast<int64_t>(d.t_row) * a.tgt_stride;
-  row.d = d.type == kDrawResid ? a.dft + static_cast<int64_t>(d.d_row) * a.dft_stride : nullptr;
-  row.c = a.c;
-  row.lp2 = d.lp2;
-  row.lq2 = d.lq2;
-
-  // Pass 1: the weight sums of this CTA's chunks.
-  constexpr int C = kK3Cpc<ES>;
-  const int c0 = q * C;
-  const int c1 = min(a.P, c0 + C);
-  const int lo = c0 * a.chunk_elems;
-  const int hi = min(a.V, c1 * a.chunk_elems);
-  int nex = gather_excl(d, ex, lo, hi, s_ex, &s_nex);
-  const bool vec = (reinterpret_cast<uintptr_t>(row.t) & 15u) == 0 &&
-                   (row.d == nullptr || (reinterpret_cast<uintptr_t>(row.d) & 15u) == 0);
-  float acc[2 * C];
-  if (vec) Pass1<ES>::vec(row, c0, c1, a.V, a.chunk_elems, nex, s_ex, ex, d.n_excl, acc);
-  else Pass1<ES>::scalar(row, c0, c1, a.V, a.chunk_elems, nex, s_ex, ex, d.n_excl, acc);
-  block_sum_n<C>(acc, red_n);
-  if (tid == 0) {
-#pragma unroll
-    for (int i = 0; i < C; ++i)
-      if (c0 + i < c1) a.part[static_cast<int64_t>(b) * a.P + c0 + i] = make_float2(acc[2 * i], acc[2 * i + 1]);
-  }
-  if (tid == 0) {
-    __threadfence();
-    const uint32_t ticket = atomicAdd(&a.counters[b], 1u);
-    s_last = (ticket == static_cast<uint32_t>(a.Q - 1));
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // Last CTA of request b: the chunk sums are loaded together into shared
-  // memory (a loop of dependent loads would pay one L2 round trip per
-  // chunk), then warp 0 finds the chunk holding u * S with fp32 warp scans,
-  // 32 chunks at a time (a serial fp64 prefix here cost ~9 us: FP64 latency
-  // is long on this GPU). fp32 adds at most a few ulps of S, far inside the
-  // 1e-5 * S band the comparison rules allow at a boundary.
   const float2* pp_g = a.part + static_cast<int64_t>(b) * a.P;
-  for (int k = tid; k < a.P && k < kK3MaxChunks; k += kK3Threads) s_part[k] = __ldcg(&pp_g[k]);
+  for (int k = tid; k < a.P && k < kK3MaxChunks; k += kK3PickThreads) s_part[k] = __ldcg(&pp_g[k]);
+  const int32_t* gex = a.excl + static_cast<int64_t>(b) * a.excl_stride;
+  if (tid < kK3LocalExcl && tid < a.excl_stride) s_ex[tid] = gex[tid];
   __syncthreads();
-  if (tid < 32) {
-    const int lane = tid;
+  if (d.type == kDrawNone) return;
+  const bool resid = d.type == kDrawResid;
+  const int nex = d.type == kDrawMaskedP ? d.n_excl : 0;
+  const int* lst = nex <= kK3LocalExcl ? s_ex : gex;
+
+  // Warp 0: the chunk holding u * S (fp32 warp scans, 32 chunks at a time;
+  // the sums' rounding is far inside the 1e-5 * S band the comparison rules
+  // allow at a boundary).
+  if (warp == 0) {
     float sw = 0.f, sp = 0.f;
     for (int k = lane; k < a.P; k += 32) {
       const float2 v = chunk_sum(s_part, pp_g, k);
@@ -427,61 +580,66 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
     }
     if (lane == 0) {
       s_chunk = cstar;
-      s_usep = usep;
+      s_usep = usep | (S == S ? 0 : 2);   // bit 1: a chunk sum was NaN (a wait gave up)
       s_thr = thr - pre;
       s_S = S;
       s_pick = INT_MAX;
       s_lastpos = -1;
-      a.counters[b] = 0u;
     }
   }
   __syncthreads();
 
-  // Pass 2: the chosen chunk's weights into shared memory (coalesced), then a
-  // scan over contiguous segments: thread t owns elements [t*16, t*16 + 16).
-  const int c2 = s_chunk;
-  const int usep = s_usep;
+  // The chosen chunk: thread t owns elements [my0, my0 + E), one 16-byte
+  // vector of each row where the row allows, and keeps them in registers.
+  const int usep = s_usep & 1;
   const float thr = s_thr;
-  const int lo2 = c2 * a.chunk_elems;
+  const int lo2 = s_chunk * a.chunk_elems;
   const int hi2 = min(a.V, lo2 + a.chunk_elems);
-  nex = usep ? 0 : gather_excl(d, ex, lo2, hi2, s_ex, &s_nex);
+  const int my0 = lo2 + tid * E;
+  const uint8_t* trow = a.tgt + static_cast<int64_t>(d.t_row) * a.tgt_stride;
+  const uint8_t* drow = resid ? a.dft + static_cast<int64_t>(d.d_row) * a.dft_stride : nullptr;
+  float xs[E], ys[E];
   {
-    float xs[kK3PerThread], ys[kK3PerThread];   // loads first, all in flight together
+    const bool tvec = (reinterpret_cast<uintptr_t>(trow) & 15u) == 0 && my0 + E <= hi2;
+    const bool dvec = !resid || ((reinterpret_cast<uintptr_t>(drow) & 15u) == 0 && my0 + E <= hi2);
+    uint4 tq, dq;
+    if (tvec) tq = __ldg(reinterpret_cast<const uint4*>(trow + static_cast<int64_t>(my0) * ES));
+    if (resid && dvec) dq = __ldg(reinterpret_cast<const uint4*>(drow + static_cast<int64_t>(my0) * ES));
+    if (tvec) {
+      Elem<ES>::unpack(tq, xs);
+    } else {
 #pragma unroll
-    for (int k = 0; k < kK3PerThread; ++k) {
-      const int j = lo2 + tid + k * kK3Threads;
-      xs[k] = -INFINITY;
-      ys[k] = -INFINITY;
-      if (j < hi2) {
-        xs[k] = Elem<ES>::load(row.t, j);
-        if (row.d) ys[k] = Elem<ES>::load(row.d, j);
-      }
+      for (int e = 0; e < E; ++e) xs[e] = my0 + e < hi2 ? Elem<ES>::load(trow, my0 + e) : -INFINITY;
     }
+    if (!resid) {
 #pragma unroll
-    for (int k = 0; k < kK3PerThread; ++k) {
-      const int i = tid + k * kK3Threads;   // chunk offset
-      const int j = lo2 + i;
-      float w = 0.f;
-      if (j < hi2) {
-        float p;
-        weight_of(xs[k], ys[k], row.d != nullptr, row.c, row.lp2, row.lq2, w, p);
-        if (usep) w = p;
-        else if (nex && is_excluded(j, nex, s_ex, ex, d.n_excl)) w = 0.f;
-      }
-      seg[(i / kK3PerThread) * kK3SegStride + (i % kK3PerThread)] = w;
+      for (int e = 0; e < E; ++e) ys[e] = 0.f;
+    } else if (dvec) {
+      Elem<ES>::unpack(dq, ys);
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) ys[e] = my0 + e < hi2 ? Elem<ES>::load(drow, my0 + e) : -INFINITY;
     }
   }
-  __syncthreads();
-  const float* mine = seg + tid * kK3SegStride;
+  const uint32_t exm = (nex && !usep) ? excl_bits(my0, E, nex, lst) : 0u;
+  float ws[E];
   float tsum = 0.f;
   int lastpos = -1;
 #pragma unroll
-  for (int k = 0; k < kK3PerThread; ++k) {
-    tsum += mine[k];
-    if (mine[k] > 0.f) lastpos = lo2 + tid * kK3PerThread + k;
+  for (int e = 0; e < E; ++e) {
+    float w = 0.f;
+    if (my0 + e < hi2) {
+      float p;
+      weight_of(xs[e], ys[e], resid, a.c, d.lp2, d.lq2, w, p);
+      if (usep) w = p;
+      else if ((exm >> e) & 1u) w = 0.f;
+      if (w > 0.f) lastpos = my0 + e;
+    }
+    ws[e] = w;
+    tsum += w;
   }
-  // Block exclusive scan of the per-thread sums (thread order = index order).
-  const int warp = tid >> 5, lane = tid & 31;
+  // Block exclusive scan of the per-thread sums (thread order = index order):
+  // warp scans, then one warp scans the warp totals.
   float incl = tsum;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -490,39 +648,58 @@ __global__ void __launch_bounds__(kK3Threads) draw_kernel(const DrawArgs a) {
   }
   if (lane == 31) scan_w[warp] = incl;
   __syncthreads();
-  float wbase = 0.f;
-  for (int w = 0; w < warp; ++w) wbase += scan_w[w];
-  const float excl_sum = wbase + incl - tsum;
+  if (warp == 0) {
+    const float t = lane < kWarps ? scan_w[lane] : 0.f;
+    float ti = t;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, ti, off);
+      if (lane >= off) ti += v;
+    }
+    __syncwarp();
+    if (lane < kWarps) scan_w[lane] = ti - t;
+  }
+  __syncthreads();
+  const float excl_sum = scan_w[warp] + (incl - tsum);
   if (excl_sum + tsum > thr && tsum > 0.f) atomicMin(&s_pick, tid);
   if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
   __syncthreads();
+  // The thread owning the drawn element: the crossing, else the last element
+  // with weight, else the chunk's last element.
   int j_out = -1;
-  if (s_pick == INT_MAX) {
-    if (tid == 0) j_out = s_lastpos >= 0 ? s_lastpos : hi2 - 1;
-  } else if (tid == s_pick) {
-    float part = 0.f;
-    j_out = lastpos;
+  if (s_pick != INT_MAX) {
+    if (tid == s_pick) {
+      float part = 0.f;
+      bool found = false;
+      j_out = lastpos;   // rounding left no crossing inside the thread
 #pragma unroll
-    for (int k = 0; k < kK3PerThread; ++k) {
-      part += mine[k];
-      if (excl_sum + part > thr && mine[k] > 0.f) {
-        j_out = lo2 + tid * kK3PerThread + k;
-        break;
+      for (int e = 0; e < E; ++e) {
+        part += ws[e];
+        if (!found && excl_sum + part > thr && ws[e] > 0.f) {
+          j_out = my0 + e;
+          found = true;
+        }
       }
     }
+  } else {
+    const int jf = s_lastpos >= 0 ? s_lastpos : hi2 - 1;
+    if (jf >= my0 && jf < my0 + E) j_out = jf;
   }
   if (j_out >= 0) {
+    float x = 0.f, y = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (my0 + e == j_out) {
+        x = xs[e];
+        y = ys[e];
+      }
     float w, p;
-    row.weight(j_out, w, p);
-    const float x = Elem<ES>::load(row.t, j_out);
+    weight_of(x, y, resid, a.c, d.lp2, d.lq2, w, p);
     const int64_t o = static_cast<int64_t>(b) * a.out_cols + d.pos;
     a.out_tokens[o] = j_out;
     if (a.out_logprob) a.out_logprob[o] = (x * a.c - d.lp2) * kLn2;
-    if (a.out_mu) {
-      float mu = p;
-      if (d.type == kDrawMaskedP) mu = d.scale * p / s_S;
-      a.out_mu[o] = mu;
-    }
+    if (a.out_mu) a.out_mu[o] = d.type == kDrawMaskedP ? d.scale * p / s_S : p;
+    if ((s_usep & 2) && a.out_status) atomicOr(&a.out_status[b], kStatusWaitErr);
   }
   if (a.fin_here) {   // no mu pass follows: this kernel ends the call
     __syncthreads();

@@ -166,7 +166,21 @@ __global__ void __launch_bounds__(kTkThreads) topk_threshold_kernel(const TopkAr
 
 // ----------------------------------------------------------- mu pass
 
-constexpr int kMuThreads = kK3Threads;
+constexpr int kMuThreads = 256;
+
+// Sum over the CTA in a fixed order; the result is valid in thread 0.
+__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kMuThreads / 32; ++w) t += red[w];
+  return t;
+}
 
 struct MuArgs {
   const uint8_t* tgt;

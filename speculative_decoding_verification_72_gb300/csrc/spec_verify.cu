@@ -47,7 +47,7 @@ struct Plan {
   int32_t P = 0;            // K3 chunks per row
   int32_t chunk_elems = 0;
   int32_t excl_stride = 0;
-  size_t off_part = 0, off_draw = 0, off_excl = 0, off_k3part = 0, off_k3cnt = 0;
+  size_t off_part = 0, off_draw = 0, off_excl = 0, off_k3part = 0;
   size_t off_thr = 0, off_mupart = 0, off_mucnt = 0;
   size_t total = 0;
 };
@@ -59,8 +59,8 @@ struct Plan {
 bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, bool draw,
                int64_t excl_stride, int64_t mu_rows, Plan* pl) {
   if (V < 1 || es == 0 || B < 0 || rows_t < 0 || rows_d < 0) return false;
-  pl->chunk_elems = kK3ChunkElems;
-  pl->P = static_cast<int32_t>((V + kK3ChunkElems - 1) / kK3ChunkElems);
+  pl->chunk_elems = kK3ChunkBytes / es;
+  pl->P = static_cast<int32_t>((V + pl->chunk_elems - 1) / pl->chunk_elems);
   pl->rows_total = rows_t + rows_d;
   if (pl->rows_total > INT32_MAX / 2) return false;
   pl->T = pl->rows_total * V;
@@ -77,8 +77,6 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
     off += align_up(static_cast<size_t>(B) * pl->excl_stride * sizeof(int32_t), kAlign);
     pl->off_k3part = off;
     off += align_up(static_cast<size_t>(B) * pl->P * sizeof(float2), kAlign);
-    pl->off_k3cnt = off;
-    off += align_up(static_cast<size_t>(B) * sizeof(uint32_t), kAlign);
     pl->off_thr = off;
     off += align_up(static_cast<size_t>(rows_t) * sizeof(float), kAlign);
     if (mu_rows > 0) {
@@ -233,35 +231,62 @@ RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride,
   return r;
 }
 
-DrawArgs draw_args(const Plan& pl, int es, const void* tgt, int64_t tgt_stride_b, const void* dft,
-                   int64_t dft_stride_b, int32_t V, float c, void* ws, int32_t out_cols,
-                   int32_t* out_tokens, float* out_logprob, float* out_mu) {
+DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride, int64_t rows_t, const void* dft,
+                   int64_t dft_stride, int64_t rows_d, int32_t B, int32_t V, int es, float c, void* ws,
+                   int32_t out_cols, int32_t* out_tokens, float* out_logprob, float* out_mu) {
   uint8_t* w = static_cast<uint8_t*>(ws);
+  const RowSet t = row_set(tgt, tgt_stride, rows_t, V, es);
+  const RowSet d0 = row_set(dft, dft_stride, rows_d, V, es);
   DrawArgs d;
-  d.tgt = static_cast<const uint8_t*>(tgt);
-  d.tgt_stride = tgt_stride_b;
-  d.dft = static_cast<const uint8_t*>(dft);
-  d.dft_stride = dft_stride_b;
+  std::memset(&d, 0, sizeof(d));
+  d.tgt = t.base;
+  d.tgt_stride = t.stride_bytes;
+  d.tgt_lo = t.safe_lo;
+  d.tgt_hi = t.safe_hi;
+  d.dft = d0.base;
+  d.dft_stride = d0.stride_bytes;
+  d.dft_lo = d0.safe_lo;
+  d.dft_hi = d0.safe_hi;
   d.V = V;
   d.P = pl.P;
   d.chunk_elems = pl.chunk_elems;
-  const int cpc = es == 2 ? kK3Cpc<2> : kK3Cpc<4>;
-  d.Q = (pl.P + cpc - 1) / cpc;
+  d.B = B;
+  const int64_t items = static_cast<int64_t>(B) * pl.P;
+  const int64_t g = static_cast<int64_t>(sm_count()) * kK3CtasPerSm;
+  d.G = static_cast<int32_t>(items < g ? items : g);
   d.c = c;
   d.draws = reinterpret_cast<const DrawDesc*>(w + pl.off_draw);
   d.excl = reinterpret_cast<const int32_t*>(w + pl.off_excl);
   d.excl_stride = pl.excl_stride;
   d.part = reinterpret_cast<float2*>(w + pl.off_k3part);
-  d.counters = reinterpret_cast<uint32_t*>(w + pl.off_k3cnt);
   d.out_cols = out_cols;
   d.out_tokens = out_tokens;
   d.out_logprob = out_logprob;
   d.out_mu = out_mu;
   d.out_nodes = nullptr;
   d.out_status = nullptr;
-  std::memset(&d.fin, 0, sizeof(d.fin));
   d.fin_here = 0;
   return d;
+}
+
+// The draw: chunk sums over the drawn rows (K3a), then the pick (K3b).
+template <int ES>
+cudaError_t launch_draw(const DrawArgs& d, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(draw_sum_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kK3SmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(draw_sum_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaError_t e = launch(draw_sum_kernel<ES>, d.G, kK3Threads, kK3SmemBytes, stream, true, d);
+  if (e != cudaSuccess) return e;
+  return launch(draw_pick_kernel<ES>, d.B, kK3PickThreads, 0, stream, true, d);
 }
 
 // Finish-step arguments of a call (disabled when fin is null).
@@ -468,19 +493,15 @@ sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_
   a.draws = reinterpret_cast<DrawDesc*>(w + pl.off_draw);
   a.excl = reinterpret_cast<int32_t*>(w + pl.off_excl);
   a.excl_stride = pl.excl_stride;
-  a.draw_counters = reinterpret_cast<uint32_t*>(w + pl.off_k3cnt);
   e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
               : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, draft_logits,
-                         draft_logits ? draft_row_stride * es : 0, V, c, workspace, K + 1,
-                         out_tokens, out_logprob, out_mu);
+  DrawArgs d = draw_args(pl, target_logits, row_stride, rows_t, draft_logits, draft_logits ? draft_row_stride : 0,
+                         rows_d, B, V, es, c, workspace, K + 1, out_tokens, out_logprob, out_mu);
   d.out_status = out_status;
   d.fin = fa;
   d.fin_here = (fa.out_len && !mu_pass) ? 1 : 0;
-  const int grid3 = B * d.Q;
-  e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
-              : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
+  e = es == 2 ? launch_draw<2>(d, st) : launch_draw<4>(d, st);
   if (e != cudaSuccess || !mu_pass) return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
   MuArgs m;
   std::memset(&m, 0, sizeof(m));
@@ -597,20 +618,17 @@ sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t 
   a.draws = reinterpret_cast<DrawDesc*>(w + pl.off_draw);
   a.excl = reinterpret_cast<int32_t*>(w + pl.off_excl);
   a.excl_stride = pl.excl_stride;
-  a.draw_counters = reinterpret_cast<uint32_t*>(w + pl.off_k3cnt);
   e = es == 2 ? launch(tree_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
               : launch(tree_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   if (greedy) return SV_OK;
-  DrawArgs d = draw_args(pl, es, target_logits, row_stride * es, nullptr, 0, V, c, workspace,
-                         max_depth + 1, out_tokens, out_logprob, out_mu);
+  DrawArgs d = draw_args(pl, target_logits, row_stride, rows, nullptr, 0, 0, B, V, es, c, workspace, max_depth + 1,
+                         out_tokens, out_logprob, out_mu);
   d.out_nodes = out_nodes;
   d.out_status = out_status;
   d.fin = fa;
   d.fin_here = fa.out_len ? 1 : 0;
-  const int grid3 = B * d.Q;
-  e = es == 2 ? launch(draw_kernel<2>, grid3, kK3Threads, 0, st, true, d)
-              : launch(draw_kernel<4>, grid3, kK3Threads, 0, st, true, d);
+  e = es == 2 ? launch_draw<2>(d, st) : launch_draw<4>(d, st);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
