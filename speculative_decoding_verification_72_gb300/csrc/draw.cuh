@@ -108,6 +108,38 @@ struct StageDesc {
   int32_t x[kStageExcl];
 };
 
+// A descriptor read with volatile loads: only requests past the CTA's cache
+// take this path, and the compiler may not hoist it onto the common one (a
+// speculated global load there cost the producer a round trip per item).
+__device__ __forceinline__ uint4 ld_volatile_v4(const void* p) {
+  uint4 q;
+  asm volatile("ld.volatile.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+               : "l"(p));
+  return q;
+}
+
+__device__ __forceinline__ DrawDesc load_desc_volatile(const DrawDesc* p) {
+  static_assert(sizeof(DrawDesc) == 48, "three 16-byte words");
+  const uint4 q0 = ld_volatile_v4(p);
+  const uint4 q1 = ld_volatile_v4(reinterpret_cast<const uint4*>(p) + 1);
+  const uint4 q2 = ld_volatile_v4(reinterpret_cast<const uint4*>(p) + 2);
+  DrawDesc d;
+  d.type = static_cast<int32_t>(q0.x);
+  d.t_row = static_cast<int32_t>(q0.y);
+  d.d_row = static_cast<int32_t>(q0.z);
+  d.pos = static_cast<int32_t>(q0.w);
+  d.u = __uint_as_float(q1.x);
+  d.lp2 = __uint_as_float(q1.y);
+  d.lq2 = __uint_as_float(q1.z);
+  d.scale = __uint_as_float(q1.w);
+  d.n_excl = static_cast<int32_t>(q2.x);
+  d.pad0 = static_cast<int32_t>(q2.y);
+  d.pad1 = static_cast<int32_t>(q2.z);
+  d.pad2 = static_cast<int32_t>(q2.w);
+  return d;
+}
+
 // 16-byte-aligned hull of elements [lo, hi) of a row, clipped to [safe_lo, safe_hi).
 template <int ES>
 __device__ __forceinline__ void chunk_hull(const uint8_t* rowp, int lo, int hi, uintptr_t safe_lo,
@@ -321,11 +353,9 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
       uint32_t phase = 0;
       bool ok = true;
       int b = b_first, k = static_cast<int>(i0 - static_cast<int64_t>(b_first) * a.P);
-      // Claim the next slot (its previous use released) and describe it.
-      auto claim = [&](const StageDesc& sd) -> bool {
-        if (st >= kK3Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) return false;
-        sdesc[slot] = sd;
-        return true;
+      // Claim the next slot: its previous use has been released.
+      auto claim = [&]() -> bool {
+        return st < kK3Stages || mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1);
       };
       auto advance = [&]() {
         ++st;
@@ -336,7 +366,7 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
       };
       for (int64_t i = i0; i < i1 && ok; ++i) {
         const int r = b - b_first;
-        const DrawDesc d = r < kK3Req ? s_desc[r] : a.draws[b];
+        const DrawDesc d = r < kK3Req ? s_desc[r] : load_desc_volatile(a.draws + b);
         if (d.type != kDrawNone) {
           const int lo = k * a.chunk_elems;
           const int hi = min(a.V, lo + a.chunk_elems);
@@ -368,10 +398,11 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
             chunk_hull<ES>(sd.rowp, lo, hi, h == 0 ? a.tgt_lo : a.dft_lo, h == 0 ? a.tgt_hi : a.dft_hi, clo,
                            bytes, sd.e0);
             sd.nel = static_cast<int32_t>(bytes / ES);
-            if (!claim(sd)) {
+            if (!claim()) {
               ok = false;
               break;
             }
+            sdesc[slot] = sd;
             const uint32_t fb = smem_u32(&full_bar[slot]);
             mbar_arrive_expect_tx(fb, bytes);
             if (bytes) bulk_g2s(smem_u32(ring + slot * kK3SlotBytes), reinterpret_cast<const void*>(clo), bytes, fb);
@@ -391,7 +422,8 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
         sd.item = -1;
         sd.e0 = sd.nel = sd.type = sd.nx = sd.nxl = 0;
         sd.lp2 = sd.lq2 = 0.f;
-        if (claim(sd)) {
+        if (claim()) {
+          sdesc[slot] = sd;
           mbar_arrive(smem_u32(&full_bar[slot]));
           ended = true;
         } else {
@@ -417,7 +449,7 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
         atomicOr(&s_err, 1);
         break;
       }
-      const StageDesc ts = sdesc[slot];
+      const StageDesc& ts = sdesc[slot];   // stays put until the slot is released
       if (ts.item < 0) break;
       const bool resid = ts.type == kDrawResid;
       int slot2 = slot + 1;
@@ -426,14 +458,11 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
         slot2 = 0;
         phase2 ^= 1;
       }
-      StageDesc ds = ts;
-      if (resid) {
-        if (!mbar_wait_bounded(smem_u32(&full_bar[slot2]), phase2)) {
-          atomicOr(&s_err, 1);
-          break;
-        }
-        ds = sdesc[slot2];
+      if (resid && !mbar_wait_bounded(smem_u32(&full_bar[slot2]), phase2)) {
+        atomicOr(&s_err, 1);
+        break;
       }
+      const StageDesc& ds = resid ? sdesc[slot2] : ts;
       const int kc = ts.item % a.P;
       const int lo = kc * a.chunk_elems;
       const int hi = min(a.V, lo + a.chunk_elems);
