@@ -176,6 +176,12 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     const ChainIn in = (base == 0) ? pre : load_chain_in<ES>(a, b, active ? i : R);
     if (active) {
       const int64_t trow = static_cast<int64_t>(b) * R + i;
+      const int64_t drow = static_cast<int64_t>(a.B) * R + static_cast<int64_t>(b) * K + i;
+      const bool with_draft = !a.greedy && a.dft && i < K;
+      // both rows' partial loads in flight together
+      RowPartials tp, dp;
+      if (!a.row_partials) row_partials_load(a.part, trow, a.V, a.T, a.G, tp);
+      if (with_draft) row_partials_load(a.part, drow, a.V, a.T, a.G, dp);
       if (a.row_partials) {
         const Partial v = a.part[trow];
         m = v.m;
@@ -183,7 +189,7 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
         idx = v.idx;
         err = v.err;
       } else {
-        merge_row(a.part, trow, a.V, a.T, a.G, c, m, s, idx, err);
+        row_partials_merge(a.part, trow, tp, c, m, s, idx, err);
       }
       lp2row = m * c + log2f(s);
       if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= 4;   // NONFINITE_ROW
@@ -194,10 +200,9 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
         } else {
           if (!in.bad) lp2 = in.x * c - lp2row;   // log2 p(t)
           if (a.dft) {
-            const int64_t drow = static_cast<int64_t>(a.B) * R + static_cast<int64_t>(b) * K + i;
             float md, sd;
             int id, ed;
-            merge_row(a.part, drow, a.V, a.T, a.G, c, md, sd, id, ed);
+            row_partials_merge(a.part, drow, dp, c, md, sd, id, ed);
             lq2row = md * c + log2f(sd);
             if (!(fabsf(md) <= FLT_MAX) || !(sd > 0.f && sd <= FLT_MAX)) st |= 4;
             if (ed) st |= 32;

@@ -541,35 +541,54 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   }
 }
 
-// Merge one row's partials (one per CTA whose range meets the row), in CTA
-// order; the first four are loaded together.
-__device__ __forceinline__ void merge_row(const Partial* __restrict__ parts, int64_t row, int V,
-                                          int64_t T, int G, float c, float& m, float& s, int& idx,
-                                          int& err) {
+// One row's partials (one per CTA whose range meets the row): the first four
+// are loaded by row_partials_load (so several rows' loads can be in flight
+// together), then row_partials_merge folds them in CTA order, loading any
+// further ones itself.
+struct RowPartials {
+  Partial v[4];
+  int g_lo, g_hi;
+};
+
+__device__ __forceinline__ void row_partials_load(const Partial* __restrict__ parts, int64_t row, int V, int64_t T,
+                                                  int G, RowPartials& rp) {
+  const int64_t e0 = row * V;
+  rp.g_lo = cta_of(e0, T, G);
+  rp.g_hi = cta_of(e0 + V - 1, T, G);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (rp.g_lo + k <= rp.g_hi) rp.v[k] = parts[row + rp.g_lo + k];
+}
+
+__device__ __forceinline__ void row_partials_merge(const Partial* __restrict__ parts, int64_t row,
+                                                   const RowPartials& rp, float c, float& m, float& s, int& idx,
+                                                   int& err) {
   m = -INFINITY;
   s = 0.f;
   idx = INT_MAX;
   err = 0;
-  const int64_t e0 = row * V;
-  const int g_lo = cta_of(e0, T, G);
-  const int g_hi = cta_of(e0 + V - 1, T, G);
-  Partial v[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    if (g_lo + k <= g_hi) v[k] = parts[row + g_lo + k];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    if (g_lo + k <= g_hi) {
-      merge_stats(m, s, idx, v[k].m, v[k].s, v[k].idx, c);
-      err |= v[k].err;
+    if (rp.g_lo + k <= rp.g_hi) {
+      merge_stats(m, s, idx, rp.v[k].m, rp.v[k].s, rp.v[k].idx, c);
+      err |= rp.v[k].err;
     }
   }
-  for (int g = g_lo + 4; g <= g_hi; ++g) {
+  for (int g = rp.g_lo + 4; g <= rp.g_hi; ++g) {
     const Partial w = parts[row + g];
     merge_stats(m, s, idx, w.m, w.s, w.idx, c);
     err |= w.err;
   }
   if (m == -INFINITY) idx = 0;   // every element is -inf: the lowest index attains the max
+}
+
+// Merge one row's partials.
+__device__ __forceinline__ void merge_row(const Partial* __restrict__ parts, int64_t row, int V,
+                                          int64_t T, int G, float c, float& m, float& s, int& idx,
+                                          int& err) {
+  RowPartials rp;
+  row_partials_load(parts, row, V, T, G, rp);
+  row_partials_merge(parts, row, rp, c, m, s, idx, err);
 }
 
 }  // namespace sv
