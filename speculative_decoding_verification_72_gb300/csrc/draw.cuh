@@ -325,6 +325,16 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
   const int64_t i1 = n_items * (blockIdx.x + 1) / a.G;
   const int b_first = static_cast<int>(i0 / a.P);
 
+  // Shared-memory setup overlaps the decide kernel's tail.
+  if (tid < kK3Stages) red_cnt[tid] = 0;
+  if (tid == 0) {
+    s_err = 0;
+    for (int i = 0; i < kK3Stages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), kK3Consumers);
+    }
+    fence_barrier_init();
+  }
   grid_dep_wait();   // the draw descriptors come from the decide kernel
   grid_dep_launch();
 
@@ -334,15 +344,6 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
   for (int x = tid; x < nreq * kK3LocalExcl; x += kK3Threads) {
     const int r = x / kK3LocalExcl, e = x - r * kK3LocalExcl;
     if (e < a.excl_stride) s_ex[r][e] = a.excl[static_cast<int64_t>(b_first + r) * a.excl_stride + e];
-  }
-  if (tid < kK3Stages) red_cnt[tid] = 0;
-  if (tid == 0) {
-    s_err = 0;
-    for (int i = 0; i < kK3Stages; ++i) {
-      mbar_init(smem_u32(&full_bar[i]), 1);
-      mbar_init(smem_u32(&empty_bar[i]), kK3Consumers);
-    }
-    fence_barrier_init();
   }
   __syncthreads();
 

@@ -374,11 +374,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   const int row0 = static_cast<int>(E0 / a.V);   // the one division; pieces then step row by row
   const int j00 = static_cast<int>(E0 - static_cast<int64_t>(row0) * a.V);
 
-  // Inputs may come from the kernel before this one, and the partials this
-  // kernel writes may still be read by the previous call: wait for it first.
-  grid_dep_wait();
-  grid_dep_launch();
-
+  // Shared-memory setup overlaps the previous kernel's tail.
   if (tid < kK1RedBufs) red_cnt[tid] = 0;
   if (tid == 0) {
     for (int i = 0; i < kK1Stages; ++i) {
@@ -388,6 +384,11 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
     fence_barrier_init();
   }
   __syncthreads();
+
+  // Inputs may come from the kernel before this one, and the partials this
+  // kernel writes may still be read by the previous call: wait for it first.
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

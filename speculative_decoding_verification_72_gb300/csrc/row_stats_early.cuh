@@ -60,10 +60,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
   const int g = blockIdx.x;
   const int rows = e.B * e.R;
 
-  grid_dep_wait();
-  grid_dep_launch();
-
-  if (tid < kK1RedBufs) red_cnt[tid] = 0;
+  if (tid < kK1RedBufs) red_cnt[tid] = 0;   // shared-memory setup overlaps the previous kernel
   if (tid == 0) {
     for (int i = 0; i < kK1Stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
@@ -72,6 +69,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
     fence_barrier_init();
   }
   __syncthreads();
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
