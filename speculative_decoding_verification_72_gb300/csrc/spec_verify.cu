@@ -269,6 +269,24 @@ DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride, int64_t 
   return d;
 }
 
+// Draft-tree construction's row pass (a TMA ring of kTbSmemBytes per CTA).
+template <int ES>
+cudaError_t launch_row_topk(const RowTopkArgs& a, int grid, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(row_topk_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTbSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(row_topk_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return launch(row_topk_kernel<ES>, grid, kTbThreads, kTbSmemBytes, stream, true, a);
+}
+
 // The draw: chunk sums over the drawn rows (K3a), then the pick (K3b).
 template <int ES>
 cudaError_t launch_draw(const DrawArgs& d, cudaStream_t stream) {
@@ -666,14 +684,17 @@ sv_status spec_tree_build(const void* draft_logits, int32_t dtype, int64_t row_s
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = kLog2e / temperature;
   RowTopkArgs ra;
-  ra.base = static_cast<const uint8_t*>(draft_logits);
-  ra.stride_bytes = row_stride * es;
+  const RowSet rs = row_set(draft_logits, row_stride, rows, V, es);
+  ra.base = rs.base;
+  ra.stride_bytes = rs.stride_bytes;
+  ra.safe_lo = rs.safe_lo;
+  ra.safe_hi = rs.safe_hi;
   ra.V = V;
   ra.P = P;
   ra.c = c;
   ra.out = static_cast<TopRow*>(workspace);
-  cudaError_t e = es == 2 ? launch(row_topk_kernel<2>, static_cast<int>(rows * P), kTbThreads, 0, st, true, ra)
-                          : launch(row_topk_kernel<4>, static_cast<int>(rows * P), kTbThreads, 0, st, true, ra);
+  cudaError_t e = es == 2 ? launch_row_topk<2>(ra, static_cast<int>(rows * P), st)
+                          : launch_row_topk<4>(ra, static_cast<int>(rows * P), st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   TreeSelectArgs ta;
   ta.rows = ra.out;

@@ -9,7 +9,13 @@
 //
 // row_topk_kernel: one CTA per draft row streams it once and produces its
 // log-sum-exp and its 8 largest logits (lower index first on ties), i.e. the
-// candidate tokens of any node whose row it is.
+// candidate tokens of any node whose row it is. The CTA is warp-specialized
+// like the verify pass: warp 0's lane 0 copies the row's 16-byte-aligned hull
+// into a 3-stage shared-memory ring with 1-D bulk copies (TMA); 7 consumer
+// warps fold each stage into (max, sum of exponentials) and keep per-thread
+// top-8 lists. After the first stage the consumers agree on a bound (the 8th
+// largest of their maxima: 8 elements of the row reach it), and from then on
+// only vectors whose maximum reaches it are inserted.
 // tree_select_kernel: one CTA per request expands level by level (the topk
 // best nodes of a level, score descending and earlier candidate first on
 // ties, each take the topk tokens of their row), keeps the n_nodes - 1 best
@@ -18,12 +24,20 @@
 // order (level, then score descending, then creation order).
 #pragma once
 
+#include "row_stats.cuh"
 #include "sv_common.cuh"
 
 namespace sv {
 
 constexpr int kTbMaxK = 8;          // largest topk
 constexpr int kTbThreads = 256;
+constexpr int kTbConsumers = 7;     // consumer warps of row_topk_kernel (warp 0 copies)
+constexpr int kTbConsumerThreads = 32 * kTbConsumers;
+constexpr int kTbStageVecs = 8;     // 16-byte vectors per consumer thread per stage
+constexpr int kTbStageBytes = kTbConsumerThreads * kTbStageVecs * 16;   // 28 KB
+constexpr int kTbStages = 3;
+constexpr int kTbSmemBytes = kTbStages * kTbStageBytes;
+constexpr int kTbCtasPerSm = 2;
 constexpr int kTbMaxCands = 1024;   // topk + (depth - 1) * topk^2
 constexpr int kTbBatch = 8;         // 16-byte vectors a thread loads together
 constexpr int kTbSelThreads = 256;  // threads per request in tree_select_kernel
@@ -36,7 +50,8 @@ constexpr int kTbMaxRows = 1 + (kTbMaxCands - kTbMaxK) / kTbMaxK;   // rows per 
 struct __align__(16) TopRow {
   float lse2;                 // log2-domain log-sum-exp of y * c
   int32_t bad;                // 1 if the row's maximum is not finite
-  int32_t pad0, pad1;
+  int32_t err;                // 1 if a bounded wait in the producing CTA gave up
+  int32_t pad1;
   float val[kTbMaxK];         // largest raw logits, descending
   int32_t idx[kTbMaxK];       // their tokens
 };
@@ -44,6 +59,7 @@ struct __align__(16) TopRow {
 struct RowTopkArgs {
   const uint8_t* base;
   int64_t stride_bytes;
+  uintptr_t safe_lo, safe_hi;   // bytes the caller's buffer holds
   int32_t V;
   int32_t P;                  // pieces per row (kTbPieceElems elements each, the last shorter)
   float c;                    // log2(e) / T
@@ -75,83 +91,24 @@ __device__ __forceinline__ void tb_insert(float (&v)[kTbMaxK], int (&ix)[kTbMaxK
   }
 }
 
-// One element outside the vector body (scalar head / tail).
-__device__ __forceinline__ void tb_visit(float x, int j, float c, float& m, float& s, float (&v)[kTbMaxK],
-                                         int (&ix)[kTbMaxK]) {
-  if (x > m) {
-    s = (m == -INFINITY) ? 0.f : s * ex2((m - x) * c);
-    m = x;
-  }
-  if (x > -INFINITY) s += ex2(fmaf(x, c, -m * c));
-  tb_insert(v, ix, x, j);
-}
-
-// One 16-byte vector folded into (m, s): the running max moves once per
-// vector and the sum takes one exponential per element. Returns the
-// vector's maximum (the caller decides whether it may enter the list).
-template <int ES>
-__device__ __forceinline__ float tb_vector(const uint4& w, float c, float& m, float& s, float (&f)[Elem<ES>::kVec]) {
-  constexpr int N = Elem<ES>::kVec;
-  Elem<ES>::unpack(w, f);
-  float vm = f[0];
+// The 8th largest of the consumer threads' values x (-inf if fewer than 8
+// are finite). Every consumer thread calls it (named barrier 1); scratch
+// holds kTbConsumerThreads floats.
+__device__ __forceinline__ float tb_consumer_bound(float x, int ct, float* scratch, float* s_bound) {
+  scratch[ct] = x;
+  named_barrier_sync(1, kTbConsumerThreads);
+  if (ct < 32) {
+    constexpr int L = kTbConsumerThreads / 32;
+    const int lane = ct;
+    float loc[L];
 #pragma unroll
-  for (int e = 1; e < N; ++e) vm = fmaxf(vm, f[e]);
-  // exponentials against the running max from before this vector (they do
-  // not wait on vm), in two independent f32x2 chains; moved to vm afterwards
-  auto vsum = [&](float ref) {
-    const float2 c2 = make_float2(c, c), nr = make_float2(-ref, -ref);
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < N; e += 4) {
-      const float2 t0 = __ffma2_rn(make_float2(f[e], f[e + 1]), c2, nr);
-      acc0 = __fadd2_rn(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
-      if (e + 2 < N) {
-        const float2 t1 = __ffma2_rn(make_float2(f[e + 2], f[e + 3]), c2, nr);
-        acc1 = __fadd2_rn(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
-      }
-    }
-    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
-  };
-  if (m == -INFINITY) {
-    if (vm > -INFINITY) {
-      m = vm;
-      s = vsum(vm * c);
-    }
-  } else {
-    float vs = vsum(m * c);
-    if (vm > m) {
-      const float d = (m - vm) * c;
-      if (d > -64.f && vs <= FLT_MAX) {
-        s = (s + vs) * ex2(d);
-      } else {
-        s = s * ex2(d) + vsum(vm * c);
-      }
-      m = vm;
-    } else {
-      s += vs;
-    }
-  }
-  return vm;
-}
-
-// The 8th largest of the CTA's per-thread values x (-inf if fewer than 8 are
-// finite). Every thread calls it; scratch holds kTbThreads floats.
-__device__ __forceinline__ float tb_block_bound(float x, float* scratch) {
-  __shared__ float s_bound;
-  __syncthreads();   // scratch may still be read from an earlier use
-  scratch[threadIdx.x] = x;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float loc[kTbThreads / 32];
-#pragma unroll
-    for (int q = 0; q < kTbThreads / 32; ++q) loc[q] = scratch[lane * (kTbThreads / 32) + q];
+    for (int q = 0; q < L; ++q) loc[q] = scratch[lane * L + q];
     float kth = -INFINITY;
     for (int r = 0; r < kTbMaxK; ++r) {   // remove the current maximum 8 times
       float lm = loc[0];
       int lq = 0;
 #pragma unroll
-      for (int q = 1; q < kTbThreads / 32; ++q)
+      for (int q = 1; q < L; ++q)
         if (loc[q] > lm) {
           lm = loc[q];
           lq = q;
@@ -162,25 +119,85 @@ __device__ __forceinline__ float tb_block_bound(float x, float* scratch) {
       const unsigned own = __ballot_sync(0xffffffffu, lm == wm);
       if (lane == __ffs(own) - 1) {   // one copy of the maximum leaves
 #pragma unroll
-        for (int q = 0; q < kTbThreads / 32; ++q)
+        for (int q = 0; q < L; ++q)
           if (q == lq) loc[q] = -INFINITY;
       }
       kth = wm;
     }
-    if (lane == 0) s_bound = kth;
+    if (lane == 0) *s_bound = kth;
   }
-  __syncthreads();
-  return s_bound;
+  named_barrier_sync(1, kTbConsumerThreads);
+  return *s_bound;
+}
+
+// One element outside the copied hull: folded into (m, s) with s relative to
+// the reference mc (= m c once m is finite, as in the verify pass) and
+// offered to the list.
+__device__ __forceinline__ void tb_visit_ref(float x, int j, float c, float& m, float& mc, float& s,
+                                             float (&v)[kTbMaxK], int (&ix)[kTbMaxK]) {
+  if (x > m) {
+    s = (m == -INFINITY) ? 0.f : s * ex2(mc - x * c);
+    m = x;
+    mc = x * c;
+  }
+  if (x > -INFINITY) s += ex2(fmaf(x, c, -mc));
+  tb_insert(v, ix, x, j);
+}
+
+// Offer the elements of half h of this thread's share of a stage that reach
+// the bound to the list (vectors ct + (4h + k) * kTbConsumerThreads),
+// skipping those outside the piece [0, Vp). A half is offered when its
+// maximum reaches the bound, which is rare per thread but frequent per warp,
+// so the path first narrows to the vectors, then the elements, that reach it.
+template <int ES>
+__device__ __forceinline__ void tb_offer_half(const uint4* sv4, int ct, int h, int jbase, int Vp, int j_lo,
+                                              float bound, float (&v)[kTbMaxK], int (&ix)[kTbMaxK]) {
+  constexpr int N = Elem<ES>::kVec;
+#pragma unroll
+  for (int k = 0; k < kGroupVecs; ++k) {
+    const int vi = ct + (h * kGroupVecs + k) * kTbConsumerThreads;
+    float f[N];
+    Elem<ES>::unpack(sv4[vi], f);
+    const int jv = jbase + vi * N;
+    unsigned cand = 0u;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (f[e] >= bound && jv + e >= 0 && jv + e < Vp) cand |= 1u << e;
+#pragma unroll 1
+    while (cand) {
+      const int e = __ffs(cand) - 1;
+      cand &= cand - 1u;
+      float fe = f[0];
+#pragma unroll
+      for (int q = 1; q < N; ++q) fe = (e == q) ? f[q] : fe;
+      tb_insert(v, ix, fe, j_lo + jv + e);
+    }
+  }
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kTbThreads, 3) row_topk_kernel(const RowTopkArgs a) {
+__global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(const RowTopkArgs a) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full_bar[kTbStages];
+  __shared__ __align__(8) uint64_t empty_bar[kTbStages];
   __shared__ float sv_[kTbThreads][kTbMaxK];
   __shared__ int si_[kTbThreads][kTbMaxK];
   __shared__ float sm_[kTbThreads], ss_[kTbThreads];
+  __shared__ float s_bound;
+  __shared__ int s_err;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {   // shared-memory setup overlaps the previous kernel
+    s_err = 0;
+    for (int i = 0; i < kTbStages; ++i) {
+      mbar_init(smem_u32(&full_bar[i]), 1);
+      mbar_init(smem_u32(&empty_bar[i]), kTbConsumers);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
   grid_dep_wait();
   grid_dep_launch();
-  const int tid = threadIdx.x;
   // this CTA's piece: elements [j_lo, j_lo + Vp) of row blockIdx.x / P
   const int rowi = blockIdx.x / a.P;
   const int piece = blockIdx.x - rowi * a.P;
@@ -188,6 +205,20 @@ __global__ void __launch_bounds__(kTbThreads, 3) row_topk_kernel(const RowTopkAr
   const int Vp = min(kTbPieceElems, a.V - j_lo);
   const uint8_t* row = a.base + static_cast<int64_t>(rowi) * a.stride_bytes + static_cast<int64_t>(j_lo) * ES;
   const float c = a.c;
+  // 16-byte hull of the piece, clipped to the buffer; elements it misses are
+  // read from global memory (at most 15 bytes at each end)
+  const uintptr_t L = reinterpret_cast<uintptr_t>(row);
+  const uintptr_t H = L + static_cast<uintptr_t>(Vp) * ES;
+  uintptr_t clo = L & ~static_cast<uintptr_t>(15);
+  if (clo < a.safe_lo) clo = (L + 15) & ~static_cast<uintptr_t>(15);
+  uintptr_t chi = (H + 15) & ~static_cast<uintptr_t>(15);
+  if (chi > a.safe_hi) chi = H & ~static_cast<uintptr_t>(15);
+  const uint32_t nbytes = chi > clo ? static_cast<uint32_t>(chi - clo) : 0u;
+  const int e0 = nbytes ? static_cast<int>((static_cast<int64_t>(clo) - static_cast<int64_t>(L)) / ES) : 0;
+  const int nst = static_cast<int>((nbytes + kTbStageBytes - 1) / kTbStageBytes);
+  const int c_lo = nbytes ? max(0, e0) : Vp;             // copied piece elements [c_lo, c_hi)
+  const int c_hi = nbytes ? min(Vp, e0 + static_cast<int>(nbytes / ES)) : Vp;
+
   float m = -INFINITY, s = 0.f;
   float v[kTbMaxK];
   int ix[kTbMaxK];
@@ -196,76 +227,111 @@ __global__ void __launch_bounds__(kTbThreads, 3) row_topk_kernel(const RowTopkAr
     v[q] = -INFINITY;
     ix[q] = INT_MAX;
   }
-  constexpr int N = Elem<ES>::kVec;
-  // 16-byte body [h, h + nv * N) when the row start allows it; the rest scalar
-  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(row) & 15u) / ES);
-  const int h = mis ? min(Vp, N - mis) : 0;
-  const int nv = (Vp - h) / N;
-  // scalar head first, so every thread visits its indices in increasing order
-  for (int j = tid; j < h; j += kTbThreads) tb_visit(Elem<ES>::load(row, j), j_lo + j, c, m, s, v, ix);
-  const uint4* body = reinterpret_cast<const uint4*>(row + static_cast<int64_t>(h) * ES);
-  // After the first batch, `bound` = the 8th largest of the threads' maxima so
-  // far: at least 8 elements of the row are >= it, so an element below it is
-  // outranked by 8 others and can never enter the row's top 8. Vectors whose
-  // maximum is below it skip the list entirely.
-  uint4 w[kTbBatch];
-  float vmx[kTbBatch];
-  // load kTbBatch vectors, fold them into (m, s) and note each one's maximum
-  auto load_fold = [&](int q0) {
-#pragma unroll
-    for (int u = 0; u < kTbBatch; ++u)
-      w[u] = (q0 + u * kTbThreads < nv) ? __ldg(body + q0 + u * kTbThreads) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int u = 0; u < kTbBatch; ++u) {
-      vmx[u] = -INFINITY;
-      if (q0 + u * kTbThreads < nv) {
-        float f[N];
-        vmx[u] = tb_vector<ES>(w[u], c, m, s, f);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int st = 0; st < nst; ++st) {
+        if (st >= kTbStages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t off = static_cast<uint32_t>(st) * kTbStageBytes;
+        const uint32_t bytes = min(static_cast<uint32_t>(kTbStageBytes), nbytes - off);
+        const uint32_t fb = smem_u32(&full_bar[slot]);
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(smem_u32(ring + slot * kTbStageBytes), reinterpret_cast<const void*>(clo + off), bytes, fb);
+        if (++slot == kTbStages) {
+          slot = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) atomicOr(&s_err, 1);
+      // the copies still in flight land before the CTA exits
+      const int issued = ok ? nst : 0;
+      for (int q = max(0, issued - kTbStages); q < issued; ++q)
+        (void)mbar_wait_bounded(smem_u32(&full_bar[q % kTbStages]), (q / kTbStages) & 1);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- consumers
+    // The verify pass's fold (two 16-word groups per stage, packed max and
+    // fp32x2 exponential sums against the reference from before the group),
+    // plus the list: a half whose maximum reaches the bound is offered
+    // element by element.
+    static_assert(kTbStageVecs == kStageVecs && kTbConsumerThreads == kK1ConsumerThreads, "verify-pass stage layout");
+    const int ct = tid - 32;
+    float mc = 0.f;   // exponent reference of s
+    // the head the copy misses, first: each thread visits its indices in increasing order
+    for (int j = ct; j < c_lo; j += kTbConsumerThreads) tb_visit_ref(Elem<ES>::load(row, j), j_lo + j, c, m, mc, s, v, ix);
+    float bound = -INFINITY;
+    int slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    constexpr int kStageElems = kTbStageBytes / ES;
+    for (int st = 0; st < nst; ++st) {
+      if (ok && !mbar_wait_bounded(smem_u32(&full_bar[slot]), phase)) {
+        ok = false;
+        atomicOr(&s_err, 1);
+      }
+      uint4* sv4 = reinterpret_cast<uint4*>(ring + slot * kTbStageBytes);
+      float ga = -INFINITY, gb = -INFINITY;
+      const int jbase = e0 + st * kStageElems;   // piece index of the stage's first element
+      if (ok) {
+        const int nvec = static_cast<int>(min(static_cast<uint32_t>(kTbStageBytes), nbytes - st * kTbStageBytes) / 16);
+        const bool first_edge = st == 0 && e0 < 0;
+        const bool last_hull = st == nst - 1 && e0 + static_cast<int>(nbytes / ES) > Vp;
+        if (first_edge || last_hull || nvec != kStageFullVecs)
+          mask_stage<ES>(sv4, ct, nvec, jbase, 0, Vp, first_edge ? 0 : -1, last_hull ? nvec - 1 : -1);
+        uint32_t w[kGroupWords];
+        load_half(sv4, ct, 0, w);
+        const float sa = group_sum<ES>(w, c, mc);
+        ga = group_max<ES>(w);
+        load_half(sv4, ct, 1, w);
+        const float sb = group_sum<ES>(w, c, mc);
+        gb = group_max<ES>(w);
+        const float gmax = fmaxf(ga, gb);
+        const float gsum = sa + sb;
+        if (gmax > m) {
+          const float nmc = gmax * c;
+          const float d = mc - nmc;
+          if (gsum <= FLT_MAX && d <= 20.f) {
+            s = (s + gsum) * ex2(d);
+          } else {
+            float r = group_sum<ES>(w, c, nmc);
+            load_half(sv4, ct, 0, w);
+            r += group_sum<ES>(w, c, nmc);
+            s = (m == -INFINITY ? 0.f : s * ex2(d)) + r;
+          }
+          m = gmax;
+          mc = nmc;
+        } else if (gmax > -INFINITY) {
+          s += gsum;
+        }
+      }
+      if (st == 0) bound = tb_consumer_bound(m, ct, sm_, &s_bound);
+      if (ok) {
+        if (ga >= bound && (ga > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
+          tb_offer_half<ES>(sv4, ct, 0, jbase, Vp, j_lo, bound, v, ix);
+        if (gb >= bound && (gb > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
+          tb_offer_half<ES>(sv4, ct, 1, jbase, Vp, j_lo, bound, v, ix);
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+      if (++slot == kTbStages) {
+        slot = 0;
+        phase ^= 1;
       }
     }
-  };
-  // the vectors that may enter the list, element by element (one copy of the insertion)
-  auto insert = [&](int q0, float bound) {
-    unsigned pend = 0;
-#pragma unroll
-    for (int u = 0; u < kTbBatch; ++u)
-      if (q0 + u * kTbThreads < nv && vmx[u] >= bound &&
-          (vmx[u] > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
-        pend |= 1u << u;
-#pragma unroll 1
-    while (pend) {
-      const int u = __ffs(pend) - 1;
-      pend &= pend - 1;
-      uint4 wu = w[0];
-#pragma unroll
-      for (int q = 1; q < kTbBatch; ++q) wu = (u == q) ? w[q] : wu;
-      float f[N];
-      Elem<ES>::unpack(wu, f);
-      const int j0 = j_lo + h + (q0 + u * kTbThreads) * N;
-#pragma unroll 1
-      for (int e = 0; e < N; ++e) {
-        float fe = f[0];
-#pragma unroll
-        for (int q = 1; q < N; ++q) fe = (e == q) ? f[q] : fe;
-        tb_insert(v, ix, fe, j0 + e);
-      }
-    }
-  };
-  // After the first batch is folded, `bound` = the 8th largest of the threads'
-  // maxima: at least 8 elements of the row are >= it, so an element below it
-  // is outranked by 8 others and can never enter the row's top 8. Only
-  // vectors whose maximum reaches it are inserted, the first batch included.
-  if (tid < nv) load_fold(tid);
-  const float bound = tb_block_bound(m, sm_);   // every thread, outside any loop
-  if (tid < nv) insert(tid, bound);
-  for (int q0 = tid + kTbBatch * kTbThreads; q0 < nv; q0 += kTbBatch * kTbThreads) {
-    load_fold(q0);
-    insert(q0, bound);
+    for (int j = c_hi + ct; j < Vp; j += kTbConsumerThreads) tb_visit_ref(Elem<ES>::load(row, j), j_lo + j, c, m, mc, s, v, ix);
+    if (m > -INFINITY) s = s * ex2(mc - m * c);   // s relative to m c for the merge (mc == m c already)
   }
-  for (int j = h + nv * N + tid; j < Vp; j += kTbThreads) tb_visit(Elem<ES>::load(row, j), j_lo + j, c, m, s, v, ix);
+  __syncthreads();   // the bound's scratch (sm_) is free again
 
   // block merge: pairwise, fixed tree (the order among threads does not matter
-  // for the lists: ties are broken by index)
+  // for the lists: ties are broken by index); warp 0 contributes empty lists
 #pragma unroll
   for (int q = 0; q < kTbMaxK; ++q) {
     sv_[tid][q] = v[q];
@@ -315,7 +381,8 @@ __global__ void __launch_bounds__(kTbThreads, 3) row_topk_kernel(const RowTopkAr
     const float mm = sm_[0];
     r.bad = !(fabsf(mm) <= FLT_MAX) ? 1 : 0;
     r.lse2 = mm * c + log2f(ss_[0]);
-    r.pad0 = r.pad1 = 0;
+    r.err = s_err;
+    r.pad1 = 0;
 #pragma unroll
     for (int q = 0; q < kTbMaxK; ++q) {
       r.val[q] = sv_[0][q];
@@ -356,14 +423,16 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
   const int b = blockIdx.x, lane = threadIdx.x;
   const int k = a.topk;
   const float ln2 = kLn2;
-  int bad = 0;
+  int bad = 0, err = 0;
   // merge each row's piece records: top 8 by (value desc, index asc), and the
   // log-sum-exps (pieces in order, fixed)
   for (int r = lane; r < a.R; r += kTbSelThreads) {
     const TopRow* pr = a.rows + (static_cast<int64_t>(b) * a.R + r) * a.P;
     TopRow out = pr[0];
+    err |= out.err;
     for (int p = 1; p < a.P; ++p) {
       const TopRow q = pr[p];
+      err |= q.err;
       float rv[kTbMaxK];
       int ri[kTbMaxK];
       int pa = 0, pb = 0;
@@ -460,7 +529,8 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     if (a.out_scores) a.out_scores[ob] = 0.f;
   }
   bad = __syncthreads_or(bad);
-  if (lane == 0 && a.out_status) a.out_status[b] = bad ? 4 : 0;   // NONFINITE_ROW
+  err = __syncthreads_or(err);
+  if (lane == 0 && a.out_status) a.out_status[b] = (bad ? 4 : 0) | (err ? 32 : 0);   // NONFINITE_ROW, TIMEOUT
 }
 
 }  // namespace sv
