@@ -144,6 +144,17 @@ __device__ __forceinline__ void tb_visit_ref(float x, int j, float c, float& m, 
   tb_insert(v, ix, x, j);
 }
 
+// Maximum of one 16-byte vector from its packed words.
+template <int ES>
+__device__ __forceinline__ float tb_vec_max(const uint4& q) {
+  if constexpr (ES == 2) {
+    const uint32_t a = max_bf16x2(max_bf16x2(q.x, q.y), max_bf16x2(q.z, q.w));
+    return fmaxf(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u));
+  } else {
+    return fmaxf(max3f(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z)), __uint_as_float(q.w));
+  }
+}
+
 // Offer the elements of half h of this thread's share of a stage that reach
 // the bound to the list (vectors ct + (4h + k) * kTbConsumerThreads),
 // skipping those outside the piece [0, Vp). A half is offered when its
@@ -156,8 +167,10 @@ __device__ __forceinline__ void tb_offer_half(const uint4* sv4, int ct, int h, i
 #pragma unroll
   for (int k = 0; k < kGroupVecs; ++k) {
     const int vi = ct + (h * kGroupVecs + k) * kTbConsumerThreads;
+    const uint4 q4 = sv4[vi];
+    if (!(tb_vec_max<ES>(q4) >= bound)) continue;   // packed maximum first
     float f[N];
-    Elem<ES>::unpack(sv4[vi], f);
+    Elem<ES>::unpack(q4, f);
     const int jv = jbase + vi * N;
     unsigned cand = 0u;
 #pragma unroll
@@ -416,7 +429,7 @@ __device__ __forceinline__ int tb_rank(const float* sc, const int* ids, int n, i
 __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSelectArgs a) {
   __shared__ float sc[kTbMaxCands];
   __shared__ int par[kTbMaxCands], tok[kTbMaxCands], dep[kTbMaxCands], pos[kTbMaxCands];
-  __shared__ int lvl[kTbMaxK * kTbMaxK], front[kTbMaxK], all_ids[kTbMaxCands];
+  __shared__ int lvl[kTbMaxK * kTbMaxK], front[kTbMaxK];
   __shared__ TopRow rows[kTbMaxRows];
   grid_dep_wait();
   grid_dep_launch();
@@ -497,22 +510,35 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     lvl_n = k * k;
     __syncthreads();
   }
-  // keep the n_nodes - 1 best candidates
-  for (int i = lane; i < n; i += kTbSelThreads) all_ids[i] = i;
-  __syncthreads();
+  // keep the n_nodes - 1 best candidates: one warp per candidate counts,
+  // 32 at a time, the candidates ranked before it (score desc, creation asc)
   const int keep = a.n_nodes - 1;
-  for (int i = lane; i < n; i += kTbSelThreads) pos[i] = tb_rank(sc, all_ids, n, i) < keep ? 1 : -1;
+  const int wid = lane >> 5, wl = lane & 31;
+  for (int i = wid; i < n; i += kTbSelThreads / 32) {
+    const float si = sc[i];
+    int r = 0;
+    for (int q0 = 0; q0 < n; q0 += 32) {
+      const int q = q0 + wl;
+      const bool before = q < n && (sc[q] > si || (sc[q] == si && q < i));
+      r += __popc(__ballot_sync(0xffffffffu, before));
+    }
+    if (wl == 0) pos[i] = r < keep ? 1 : -1;
+  }
   __syncthreads();
   // BFS position among the kept: (depth, score desc, creation)
-  for (int i = lane; i < n; i += kTbSelThreads) {
-    if (pos[i] < 0) continue;
+  for (int i = wid; i < n; i += kTbSelThreads / 32) {
+    if (pos[i] < 0) continue;   // warp-uniform
+    const float si = sc[i];
+    const int di = dep[i];
     int p = 1;
-    for (int q = 0; q < n; ++q) {
-      if (pos[q] < 0) continue;
-      const bool before = dep[q] < dep[i] || (dep[q] == dep[i] && (sc[q] > sc[i] || (sc[q] == sc[i] && q < i)));
-      p += before ? 1 : 0;
+    for (int q0 = 0; q0 < n; q0 += 32) {
+      const int q = q0 + wl;
+      const bool before = q < n && pos[q] > 0 &&
+                          (dep[q] < di || (dep[q] == di && (sc[q] > si || (sc[q] == si && q < i))));
+      p += __popc(__ballot_sync(0xffffffffu, before));
     }
-    pos[i] = p + 1000000;   // marked: BFS position + offset (kept)
+    __syncwarp();
+    if (wl == 0) pos[i] = p + 1000000;   // marked: BFS position + offset (still kept for the others' tests)
   }
   __syncthreads();
   const int64_t ob = static_cast<int64_t>(b) * a.n_nodes;
