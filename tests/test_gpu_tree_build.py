@@ -93,3 +93,30 @@ def test_built_tree_feeds_tree_verification():
     got = sv.spec_verify_tree(x, tree["tokens"], tree["parents"], 5)
     ref = O.verify_tree(f64(x), host(tree["tokens"]), host(tree["parents"]), 5, 0.0)
     compare(got, ref)
+
+
+@pytest.mark.parametrize("dtype,off,pad", [(torch.bfloat16, 3, 5), (torch.float32, 1, 2)])
+def test_unaligned_nan_padded_rows(dtype, off, pad):
+    """Rows whose buffer starts off a 16-byte boundary, with NaN between rows:
+    the row pass must read exactly each row's elements."""
+    B, depth, topk, V = 6, 3, 3, 7001
+    y = W.draft_tree_rows(B=B, V=V, depth=depth, topk=topk, dtype=dtype, seed=7706, device=DEV)
+    R = y.shape[1]
+    pitch = V + pad
+    buf = torch.full((off + B * R * pitch + 8,), float("nan"), dtype=dtype, device=DEV)
+    view = buf[off: off + B * R * pitch].view(B, R, pitch)[:, :, :V]
+    view.copy_(y)
+    got = sv.spec_tree_build(view, depth, topk, 1 + topk + topk * topk)
+    ref = sv.spec_tree_build(y, depth, topk, 1 + topk + topk * topk)
+    # the same tree as from the contiguous rows; the log-sum-exps are summed
+    # in an order that depends on the rows' alignment, so scores agree to rounding
+    for k in ("tokens", "parents", "status"):
+        assert torch.equal(got[k], ref[k]), k
+    assert torch.allclose(got["scores"], ref["scores"], atol=1e-5, rtol=0)
+    _check(y, depth, topk, 1 + topk + topk * topk, max_ties=0.5)
+
+
+def test_rows_longer_than_one_piece():
+    # V > 2^20: each row is read by two CTAs whose records the selection merges
+    y = W.draft_tree_rows(B=2, V=(1 << 20) + 4099, depth=2, topk=2, dtype=torch.bfloat16, seed=7707, device=DEV)
+    _check(y, 2, 2, 7, max_ties=1.0)
