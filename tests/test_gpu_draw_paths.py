@@ -3,8 +3,9 @@ logits whose buffers start off a 16-byte boundary (chunk copies clipped at
 the buffer's ends, elements read from global memory), target and draft rows
 at different alignments (element-by-element sums), more requests per CTA
 than the CTA caches (descriptors and exclusion lists read from global
-memory), and masked draws with more rejected tokens in one chunk than a
-stage descriptor carries, or more than are cached per request."""
+memory), masked draws with more rejected tokens in one chunk than a stage
+descriptor carries, or more than are cached per request, and rows with more
+chunks than the pick kernel keeps in shared memory."""
 
 import numpy as np
 import pytest
@@ -103,3 +104,16 @@ def test_wide_root_with_every_child_rejected(children, V):
     drawn = host(got["tokens"])[:, 0]
     for b in range(B):
         assert drawn[b] not in set(tok[b, 1:].tolist())
+
+
+def test_more_chunks_than_the_pick_stages():
+    # fp32 V = 1.2M: 293 chunks of 4096, past the 256 chunk sums the pick
+    # kernel keeps in shared memory
+    ci = W.stochastic_chain(B=3, K=1, V=1_200_000, seed=7940, device=DEV)
+    got = sv.spec_verify_sample(ci.target, ci.draft_tokens, ci.uniforms, draft_logits=ci.draft_logits,
+                                temperature=ci.temperature)
+    compare(got, _oracle_sample(ci), stochastic=True)
+    ci.uniforms[:, 0] = 0.999999          # reject the draft: residual draws over all chunks
+    got = sv.spec_verify_sample(ci.target, ci.draft_tokens, ci.uniforms, draft_logits=ci.draft_logits,
+                                temperature=ci.temperature)
+    compare(got, _oracle_sample(ci), stochastic=True)
