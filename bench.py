@@ -32,6 +32,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -226,7 +227,10 @@ class ClockSampler:
 
     def __init__(self, gpu_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank_gpu{gpu_index}.csv")
+        # raw samples (SV_CLOCKS_DIR, else the system temp directory); the
+        # summary goes into the JSON line
+        out_dir = os.environ.get("SV_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_rank_gpu{gpu_index}.csv")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
