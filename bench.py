@@ -117,7 +117,7 @@ _CALL_SOURCES = {
              "spec_verify.cu"),
     "early": ("sv_common.cuh", "row_stats.cuh", "row_stats_early.cuh", "decide.cuh", "finish.cuh",
               "spec_verify.cu"),
-    "tree_build": ("sv_common.cuh", "tree_build.cuh", "spec_verify.cu"),
+    "tree_build": ("sv_common.cuh", "row_stats.cuh", "tree_build.cuh", "spec_verify.cu"),
     "kv_compact": ("sv_common.cuh", "kv_compact.cuh", "spec_verify.cu"),
 }
 
