@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int slot = 0;
+      int slot = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int st = 0; st < nst; ++st) {
+      for (int st = 0; st < nst; ++st, issued = st) {
         if (st >= kTbStages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) {
           ok = false;
           break;
@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
         }
       }
       if (!ok) atomicOr(&s_err, 1);
-      // the copies still in flight land before the CTA exits
-      const int issued = ok ? nst : 0;
+      // the copies still in flight (among the last kTbStages issued, also
+      // after a wait gave up) land before the CTA exits
       for (int q = max(0, issued - kTbStages); q < issued; ++q)
         (void)mbar_wait_bounded(smem_u32(&full_bar[q % kTbStages]), (q / kTbStages) & 1);
     }
