@@ -307,8 +307,10 @@ sv_status spec_tree_build(const void* draft_logits, int32_t dtype, int64_t row_s
  * a cache of pages of page_size rows, token_stride_bytes apart, each row
  * row_bytes long (both multiples of 16; kv 16-byte aligned). The path
  * path_nodes[b, 0..n] (out_nodes of spec_verify_tree, n = num_accepted[b],
- * path_cols its row length) is moved so its j-th node lands at position
- * seq_base[b] + j, in place; rows off the path are untouched; out_len[b] =
+ * path_cols its row length; node ids strictly increasing along the path, as
+ * a tree walk writes them, otherwise the moved rows are unspecified) is moved
+ * so its j-th node lands at position seq_base[b] + j, in place; rows off the
+ * path are untouched; out_len[b] =
  * seq_base[b] + n + 1 (the root and the accepted nodes). A path node outside
  * [0, max_nodes), n outside [0, path_cols), or a page id < 0 or past
  * max_pages leaves the request untouched, out_len[b] = seq_base[b] and

@@ -64,3 +64,30 @@ def _depths(par):
     for n in range(1, len(par)):
         d[n] = d[par[n]] + 1
     return d
+
+
+def test_tied_logits_take_the_lower_token():
+    # depth 2, topk 1: the root row's top logit is shared by tokens 2 and 4,
+    # the next row's by tokens 1 and 5; the lower id wins each time
+    y = np.zeros((1, 2, 6))
+    y[0, 0, [4, 2]] = 3.0
+    y[0, 1, [5, 1]] = 1.5
+    out = T.build_tree(y, depth=2, topk=1, n_nodes=3)
+    assert out["tokens"][0].tolist() == [-1, 2, 1]
+
+
+def test_temperature_limits():
+    # a very hot softmax is uniform: a depth-d node scores -d log V; a very
+    # cold one puts all mass on the argmax: the argmax chain scores ~0
+    rng = np.random.default_rng(5)
+    V = 50
+    y = rng.normal(0, 3, (2, 4, V))                  # depth 2, topk 3: rows 0..3
+    hot = T.build_tree(y, 2, 3, 13, temperature=1e6)
+    for b in range(2):
+        dep = _depths(hot["parents"][b])
+        assert np.allclose(hot["scores"][b, 1:], -dep[1:] * np.log(V), atol=1e-4)
+    cold = T.build_tree(y, 2, 3, 13, temperature=1e-3)
+    for b in range(2):
+        best = int(np.argmax(cold["scores"][b, 1:])) + 1
+        assert cold["scores"][b, best] > -1e-6
+        assert cold["tokens"][b, 1] == int(np.argmax(y[b, 0]))
