@@ -82,7 +82,8 @@ CONFIGS = {
                                 "per request, drafts = argmax w.p. 0.95"),
 }
 DEFAULT_CONFIG = "llama_greedy"
-KERNELS_PER_CALL = {"greedy": 2, "sample": 3, "tree": 2, "tree_build": 2, "kv_compact": 1}
+# K1 + K2, plus the draw's two kernels (chunk sums, pick) when a call samples
+KERNELS_PER_CALL = {"greedy": 2, "sample": 4, "tree": 2, "tree_build": 2, "kv_compact": 1}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -131,8 +132,9 @@ def source_hash(cfg=None):
     if cfg is None:
         names = [n for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
     else:
+        draws = cfg["kind"] == "sample" or (cfg["kind"] == "tree" and cfg.get("T"))
         kind = ("early" if cfg.get("early") else cfg["kind"] if cfg["kind"] in ("tree_build", "kv_compact")
-                else "draw" if _launches_per_call(cfg) == 3 else "greedy")
+                else "draw" if draws else "greedy")
         names = sorted(_CALL_SOURCES[kind])
     for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
@@ -594,7 +596,7 @@ def run_gpu(args, cfg, name):
 
 
 def _launches_per_call(cfg):
-    return KERNELS_PER_CALL[cfg["kind"]] + (1 if cfg["kind"] == "tree" and cfg.get("T") else 0)
+    return KERNELS_PER_CALL[cfg["kind"]] + (2 if cfg["kind"] == "tree" and cfg.get("T") else 0)
 
 
 def _workspace_need(cfg):
