@@ -10,8 +10,8 @@ A step is one verification call (all of its kernels) over one batch of
 seeded synthetic inputs. Inputs are resident in HBM before timing. Steps cycle
 through a pool of input sets whose total size exceeds 4x the L2 cache, so no
 step reads inputs another step left in L2. Steps are replayed from CUDA graphs
-(one call = the row-statistics kernel plus the decide kernel, and the draw
-kernel for stochastic rules) and timed with CUDA events on the launching
+(one call = the row-statistics kernel plus the decide kernel, and the draw's
+chunk-sum and pick kernels for stochastic rules) and timed with CUDA events on the launching
 stream, bracketed by a barrier and a device synchronize.
 
   python bench.py                      # default workload, 1 GPU
@@ -581,7 +581,7 @@ def run_gpu(args, cfg, name):
                                 "one compaction call: kv_compact_kernel (path rows read + written)"
                                 if cfg["kind"] == "kv_compact" else
                                 "one verify call: row_stats_kernel (all logit bytes) + decide kernel")
-                               + (" + draw kernel" if _launches_per_call(cfg) == 3 else ""),
+                               + (" + draw kernels (chunk sums, pick)" if _launches_per_call(cfg) == 4 else ""),
                      "traffic": recorded_traffic(name)},
         "cpu_baseline": cpu,
         "e2e": e2e,
