@@ -10,13 +10,18 @@ A step is one verification call (all of its kernels) over one batch of
 seeded synthetic inputs. Inputs are resident in HBM before timing. Steps cycle
 through a pool of input sets whose total size exceeds 4x the L2 cache, so no
 step reads inputs another step left in L2. Steps are replayed from CUDA graphs
-(one call = the row-statistics kernel plus the decide kernel, and the draw's
-chunk-sum and pick kernels for stochastic rules) and timed with CUDA events on the launching
-stream, bracketed by a barrier and a device synchronize.
+and timed with CUDA events on the launching stream, bracketed by a barrier and
+a device synchronize. One timed repetition is exactly K steps; a workload is
+timed as at least five repetitions (more until the repetitions span enough
+wall time for the clock sampler) and the median repetition is reported.
 
-  python bench.py                      # default workload, 1 GPU
-  python bench.py --config qwen_sample --steps 2000 --warmup 20
-  python bench.py --impl reference     # the float64 CPU oracle as the reference arm
+The headline line is the long-chain workload (the largest single-GPU
+configuration). The same line carries `per_config`: every other workload
+timed the same way (at least 200 steps per repetition).
+
+  python bench.py                      # long chain headline + per_config, 1 GPU
+  python bench.py --config qwen_sample --steps 2000 --warmup 20 --no-per-config
+  python bench.py --impl reference     # the float64 CPU oracle on all host cores
   torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas (weak scaling)
 
 One JSON line is printed by rank 0.
@@ -61,10 +66,18 @@ CONFIGS = {
     "eagle_tree_relaxed": dict(kind="tree", B=32, N=64, V=128256, dtype="bf16", T=1.0, rule=1, tau=0.1,
                                seed=7203, workload="EAGLE-3 tree verify (relaxed rule tau=0.1, T=1), "
                                                    "64 nodes, V=128256 bf16, B=32"),
+    "long_chain": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
+                       workload="long-chain greedy verify: GPT-2 vocab V=50257 bf16, B=8, K+1=4096 rows "
+                                "per request, drafts = argmax w.p. 0.95"),
     "llama_greedy_finish": dict(kind="greedy", B=32, K=5, V=128256, dtype="bf16", p_match=0.8, seed=7201,
                                 finish=True,
                                 workload="greedy chain verify with the finish step: V=128256 bf16, K=5, B=32, "
                                          "a 2-id stop set, per-request max_new in [1, 6], running counters"),
+    "long_chain_early": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
+                             early=True,
+                             workload="long-chain greedy verify with early exit: V=50257 bf16, B=8, K+1=4096 "
+                                      "rows per request, drafts = argmax w.p. 0.95; rows after a request's "
+                                      "first mismatch are not read"),
     "eagle_tree_build": dict(kind="tree_build", B=32, V=128256, depth=5, topk=4, N=64, dtype="bf16", seed=7205,
                              workload="EAGLE-3 draft-tree construction: depth 5, topk 4, 64 nodes, V=128256 bf16 "
                                       "draft logits N(0,3^2), 17 rank-ordered draft rows per request, B=32"),
@@ -72,19 +85,21 @@ CONFIGS = {
                        workload="accepted-path KV compaction: B=32 requests, 64-node trees, paths of 0..5 accepted "
                                 "nodes, paged bf16 cache (16 rows per page, 128 KB rows = 32 layers x K,V x 8 "
                                 "heads x 128 dims), committed prefixes of 0..256 tokens"),
-    "long_chain_early": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
-                             early=True,
-                             workload="long-chain greedy verify with early exit: V=50257 bf16, B=8, K+1=4096 "
-                                      "rows per request, drafts = argmax w.p. 0.95; rows after a request's "
-                                      "first mismatch are not read"),
-    "long_chain": dict(kind="greedy", B=8, K=4095, V=50257, dtype="bf16", p_match=0.95, seed=7204,
-                       workload="long-chain greedy verify: GPT-2 vocab V=50257 bf16, B=8, K+1=4096 rows "
-                                "per request, drafts = argmax w.p. 0.95"),
 }
-DEFAULT_CONFIG = "llama_greedy"
+# The verification workloads the HBM-fraction target applies to, then the
+# steps before and after verification.
+CONTRACT_CONFIGS = ("long_chain", "llama_greedy", "llama_greedy_b8", "llama_greedy_b1", "qwen_sample",
+                    "eagle_tree_greedy", "eagle_tree_power", "eagle_tree_relaxed")
+NEXT_CONFIGS = ("llama_greedy_finish", "long_chain_early", "eagle_tree_build", "kv_compact")
+DEFAULT_CONFIG = "long_chain"
 # K1 + K2, plus the draw's two kernels (chunk sums, pick) when a call samples
 KERNELS_PER_CALL = {"greedy": 2, "sample": 4, "tree": 2, "tree_build": 2, "kv_compact": 1}
 FALLBACK_HBM_GBS = 6800.0
+MIN_REPS = 5                 # timed repetitions per workload (median reported)
+MAX_REPS = 2000
+MIN_WINDOW_S = 0.6           # repetitions continue until they span this much wall time
+PER_CONFIG_MIN_STEPS = 200   # steps per repetition in per_config
+CLOCK_PERIOD_MS = 100
 
 
 # ------------------------------------------------------------ host helpers
@@ -192,6 +207,17 @@ def kv_moved_rows(nodes, n):
     return int(sum(1 for b in range(len(n)) for j in range(1, int(n[b]) + 1) if nodes[b, j] != j))
 
 
+def rows_per_request(cfg):
+    """Rows the metric counts for one request of workload `cfg`."""
+    if cfg["kind"] == "tree":
+        return cfg["N"]
+    if cfg["kind"] == "tree_build":
+        return 1 + (cfg["depth"] - 1) * cfg["topk"]
+    if cfg["kind"] == "kv_compact":
+        return None   # data-dependent (the path rows moved)
+    return cfg["K"] + 1
+
+
 def algorithmic_bytes(cfg):
     es = 2 if cfg["dtype"] == "bf16" else 4
     if cfg["kind"] == "kv_compact":   # rows = path rows moved; each read once and written once
@@ -220,9 +246,28 @@ def algorithmic_bytes(cfg):
     return rows, logits + small + outs
 
 
+def launches_per_call(cfg):
+    return KERNELS_PER_CALL[cfg["kind"]] + (2 if cfg["kind"] == "tree" and cfg.get("T") else 0)
+
+
+def config_dict(cfg, name, world):
+    """The `config` object of a result line; the GPU arm and the reference
+    arm print the same one for the same workload."""
+    rows, alg = algorithmic_bytes(cfg)
+    return {"workload": cfg["workload"], "name": name, "B": cfg["B"], "rows_per_step": rows,
+            "algorithmic_bytes_per_step": alg,
+            "l2_policy": "inputs larger than L2: a rotating pool of input sets totalling more than 4x the L2 "
+                         "cache, so no step reads inputs left in L2 by another",
+            "timing": f"median of >= {MIN_REPS} repetitions of exactly `steps` steps, each bracketed by a barrier "
+                      f"and a device synchronize",
+            "parallelism": f"{world} independent replica(s)"}
+
+
 # ------------------------------------------------------------ clock sampler
 
 class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every CLOCK_PERIOD_MS while
+    the run lasts; summary(t0, t1) reports the samples inside a wall window."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -230,7 +275,7 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
         # raw samples (SV_CLOCKS_DIR, else the system temp directory); the
-        # summary goes into the JSON line
+        # summaries go into the JSON line
         out_dir = os.environ.get("SV_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(out_dir, f"clocks_rank_gpu{gpu_index}.csv")
         try:
@@ -238,7 +283,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", str(CLOCK_PERIOD_MS), "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -251,9 +296,7 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self, t0, t1):
-        if self.proc is None:
-            return None
+    def _rows(self):
         rows = []
         try:
             with open(self.path) as f:
@@ -267,10 +310,17 @@ class ClockSampler:
                     except ValueError:
                         continue
         except OSError:
+            return []
+        return rows
+
+    def summary(self, t0, t1):
+        if self.proc is None:
             return None
+        rows = self._rows()
         if not rows:
             return None
         inside = [r for r in rows if t0 <= r[0] <= t1]
+        # no sample inside a short window: the two nearest ones, flagged by samples_in_timed_region = 0
         used = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v.lower() == "active"})
@@ -353,46 +403,34 @@ def input_bytes(x):
 
 
 # ------------------------------------------------------------ CPU oracle
+#
+# The float64 oracle, as it stands, on a bounded host sample of the workload:
+# the same recipe and seed drawn by the CPU generator (`b` whole requests,
+# float64 logits). Both CPU legs run before the GPU arm touches CUDA, so the
+# all-core leg can fork its workers (which then share the sample
+# copy-on-write).
 
-def oracle_rows_per_s(cfg, x_host, budget_s, max_requests=None):
-    """The float64 oracle, as it stands, on whole requests of one input set
-    until budget_s elapses (at least one request). Returns (rows/s, requests)."""
-    from oracle import spec_oracle as O
-    B = cfg["B"]
-    done_rows, t_used, r = 0, 0.0, 0
-    while (t_used < budget_s or r == 0) and r < B and (max_requests is None or r < max_requests):
-        sl = slice(r, r + 1)
-        t0 = time.perf_counter()
-        if cfg["kind"] == "greedy":
-            O.verify_greedy(x_host["target"][sl], x_host["draft_tokens"][sl])
-            rows = cfg["K"] + 1
-        elif cfg["kind"] == "sample":
-            O.verify_sample(x_host["target"][sl], x_host["draft_logits"][sl], x_host["draft_tokens"][sl],
-                            1.0, x_host["uniforms"][sl])
-            rows = cfg["K"] + 1
-        elif cfg["kind"] == "kv_compact":
-            from oracle import kv_compact as KC
-            pages = x_host["table"][r]                       # this request's pages only
-            small = x_host["kv"][pages]
-            KC.compact(small, np.arange(len(pages))[None], cfg["page_size"], x_host["base"][sl],
-                       x_host["nodes"][sl], x_host["n"][sl], cfg["N"])
-            rows = int(x_host["n"][r])
-        elif cfg["kind"] == "tree_build":
-            from oracle import tree_build as TB
-            TB.build_tree(x_host["draft_rows"][sl], cfg["depth"], cfg["topk"], cfg["N"])
-            rows = 1 + (cfg["depth"] - 1) * cfg["topk"]
-        else:
-            O.verify_tree(x_host["target"][sl], x_host["node_tokens"][sl], x_host["parents"][sl], 5,
-                          cfg.get("T", 0.0), x_host["uniforms"][sl], rule=cfg.get("rule", 0),
-                          tau=cfg.get("tau", 0.0), alpha=cfg.get("alpha", 1.0))
-            rows = cfg["N"]
-        t_used += time.perf_counter() - t0
-        done_rows += rows
-        r += 1
-    return done_rows / t_used, r
+def _mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def _f64_bytes_per_request(cfg):
+    if cfg["kind"] == "kv_compact":
+        return ((257 + cfg["N"] + cfg["page_size"] - 1) // cfg["page_size"]) * cfg["page_size"] * cfg["row_elems"] * 8
+    rows = rows_per_request(cfg) + (cfg["K"] if cfg["kind"] == "sample" else 0)
+    return rows * cfg["V"] * 8
 
 
 def host_copy(x):
+    """float64 / integer NumPy copies of an input set (logits one request at a
+    time, so the float32 intermediate stays small)."""
     d = {}
     for k in ("target", "draft_logits", "draft_tokens", "uniforms", "node_tokens", "parents", "draft_rows",
               "kv", "table", "base", "nodes", "n"):
@@ -400,46 +438,170 @@ def host_copy(x):
         if t is None:
             continue
         if t.is_floating_point():
-            d[k] = t.float().cpu().numpy().astype(np.float64)
+            a = np.empty(tuple(t.shape), dtype=np.float64)
+            for i in range(t.shape[0]):
+                a[i] = t[i].float().cpu().numpy()
+            d[k] = a
         else:
             d[k] = t.cpu().numpy()
     return d
 
 
+def cpu_sample(cfg, mem_frac=0.25):
+    """(sample config, host arrays): up to B requests, fewer if their float64
+    copy would exceed mem_frac of the host's available memory."""
+    b = cfg["B"]
+    avail = _mem_available_bytes()
+    if avail:
+        b = max(1, min(b, int(mem_frac * avail // _f64_bytes_per_request(cfg))))
+    small = dict(cfg, B=b)
+    xh = host_copy(make_inputs(small, cfg["seed"], "cpu"))
+    return small, xh
+
+
+def oracle_request(cfg, xh, r):
+    """The oracle on request r of a host sample; returns the rows the metric
+    counts for it."""
+    from oracle import spec_oracle as O
+    sl = slice(r, r + 1)
+    if cfg["kind"] == "greedy":
+        O.verify_greedy(xh["target"][sl], xh["draft_tokens"][sl])
+        return cfg["K"] + 1
+    if cfg["kind"] == "sample":
+        O.verify_sample(xh["target"][sl], xh["draft_logits"][sl], xh["draft_tokens"][sl], 1.0, xh["uniforms"][sl])
+        return cfg["K"] + 1
+    if cfg["kind"] == "kv_compact":
+        from oracle import kv_compact as KC
+        pages = xh["table"][r]                       # this request's pages only
+        KC.compact(xh["kv"][pages], np.arange(len(pages))[None], cfg["page_size"], xh["base"][sl],
+                   xh["nodes"][sl], xh["n"][sl], cfg["N"])
+        return int(xh["n"][r])
+    if cfg["kind"] == "tree_build":
+        from oracle import tree_build as TB
+        TB.build_tree(xh["draft_rows"][sl], cfg["depth"], cfg["topk"], cfg["N"])
+        return 1 + (cfg["depth"] - 1) * cfg["topk"]
+    O.verify_tree(xh["target"][sl], xh["node_tokens"][sl], xh["parents"][sl], 5, cfg.get("T", 0.0),
+                  xh["uniforms"][sl], rule=cfg.get("rule", 0), tau=cfg.get("tau", 0.0), alpha=cfg.get("alpha", 1.0))
+    return cfg["N"]
+
+
+def oracle_one_core(cfg, xh, nreq, budget_s):
+    """Requests in turn on this thread until budget_s elapses (at least one).
+    Returns (rows/s, requests done)."""
+    rows, t_used, done = 0, 0.0, 0
+    while t_used < budget_s or done == 0:
+        t0 = time.perf_counter()
+        rows += oracle_request(cfg, xh, done % nreq)
+        t_used += time.perf_counter() - t0
+        done += 1
+    return rows / t_used, done
+
+
+def _oracle_worker(cfg, xh, nreq, w, nworkers, conn):
+    """Forked worker: on command k, verifies request (w + k * nworkers) mod nreq."""
+    os.environ["OMP_NUM_THREADS"] = "1"
+    while True:
+        k = conn.recv()
+        if k is None:
+            break
+        t0 = time.monotonic()
+        rows = oracle_request(cfg, xh, (w + k * nworkers) % nreq)
+        conn.send((rows, t0, time.monotonic()))
+    conn.close()
+
+
+class OraclePool:
+    """One forked process per host core, each running the oracle on whole
+    requests of the host sample. Must be created before any CUDA call."""
+
+    def __init__(self, cfg, xh, nreq, nworkers=None):
+        import multiprocessing as mp
+        import oracle.spec_oracle  # noqa: F401  (imported before the fork)
+        ctx = mp.get_context("fork")
+        self.n = nworkers or os.cpu_count() or 1
+        self.conns, self.procs = [], []
+        for w in range(self.n):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(cfg, xh, nreq, w, self.n, b), daemon=True)
+            p.start()
+            b.close()
+            self.conns.append(a)
+            self.procs.append(p)
+
+    def step(self, k):
+        """Every worker verifies one request; returns (rows, wall seconds from
+        the first start to the last finish)."""
+        for c in self.conns:
+            c.send(k)
+        res = [c.recv() for c in self.conns]
+        return sum(r[0] for r in res), max(r[2] for r in res) - min(r[1] for r in res)
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+                c.close()
+            except OSError:
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def cpu_baseline(cfg, budget_s):
+    """The oracle on a bounded host sample: one thread, then every host core."""
+    small, xh = cpu_sample(cfg)
+    nreq = small["B"]
+    one, done1 = oracle_one_core(cfg, xh, nreq, budget_s)
+    pool = OraclePool(cfg, xh, nreq)
+    rows, wall, k = 0, 0.0, 0
+    try:
+        while wall < budget_s or k == 0:
+            r, t = pool.step(k)
+            rows, wall, k = rows + r, wall + t, k + 1
+    finally:
+        pool.close()
+    sample = (f"{nreq} of {cfg['B']} requests of the workload's recipe drawn on the host (seed {cfg['seed']}), "
+              f"float64 NumPy oracle")
+    return {"value": rows / wall, "unit": "rows/s", "cores": pool.n, "kind": "oracle",
+            "sample": f"{sample}; {pool.n} forked processes, one request each per round, {k} rounds "
+                      f"(~{wall:.0f} s)",
+            "one_core": {"value": one, "unit": "rows/s", "cores": 1,
+                         "sample": f"{sample}; one thread, {done1} requests (~{budget_s:.0f} s)"},
+            "host_cores": os.cpu_count()}
+
+
 def run_reference(args, cfg, name):
-    """Reference arm: the float64 CPU oracle timed on the host cores."""
+    """Reference arm: the float64 CPU oracle, as it stands, on every host core.
+    A step is one round of the oracle pool (each process verifies one whole
+    request of the host sample)."""
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if rank != 0:
         return 0
     steps = args.steps if args.steps is not None else 20
     warmup = args.warmup if args.warmup is not None else 3
-    x = host_copy(make_inputs(cfg, cfg["seed"], "cpu"))
-    # size one step's sample so the whole run stays within about two minutes
-    t_req = oracle_rows_per_s(cfg, x, 0.0, max_requests=1)
-    rows_req = (cfg["N"] if cfg["kind"] == "tree" else
-                1 + (cfg["depth"] - 1) * cfg["topk"] if cfg["kind"] == "tree_build" else
-                3 if cfg["kind"] == "kv_compact" else cfg["K"] + 1)
-    per_req_s = rows_req / t_req[0]
-    reqs_per_step = max(1, min(cfg["B"], int(120.0 / max(steps + warmup, 1) / per_req_s)))
-    from oracle import spec_oracle as O  # noqa: F401
-    for _ in range(warmup):
-        oracle_rows_per_s(cfg, x, 0.0, max_requests=1)
-    total_rows, total_t = 0, 0.0
-    for _ in range(steps):
-        t0 = time.perf_counter()
-        rps, r = oracle_rows_per_s(cfg, x, 1e9, max_requests=reqs_per_step)
-        total_t += time.perf_counter() - t0
-        total_rows += r * rows_req
+    small, xh = cpu_sample(cfg)
+    nreq = small["B"]
+    pool = OraclePool(cfg, xh, nreq)
+    try:
+        for w in range(warmup):
+            pool.step(w)
+        total_rows, total_t = 0, 0.0
+        for s in range(steps):
+            r, t = pool.step(warmup + s)
+            total_rows, total_t = total_rows + r, total_t + t
+    finally:
+        pool.close()
     value = total_rows / total_t
+    sample = (f"{nreq} of {cfg['B']} requests of the workload's recipe drawn on the host (seed {cfg['seed']}); "
+              f"each step: {pool.n} forked processes verify one whole request each, float64 NumPy oracle")
     line = {
         "impl": "reference", "metric": metric_name(cfg), "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
         "ms_per_step": 1e3 * total_t / steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg["workload"], "name": name},
-        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{reqs_per_step} request(s) of {cfg['B']} per step, float64 NumPy "
-                                   f"oracle, one thread"},
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; shapes from the pages, no dataset or weights)",
+        "config": config_dict(cfg, name, world),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": pool.n, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -447,157 +609,6 @@ def run_reference(args, cfg, name):
 
 
 # ------------------------------------------------------------ GPU arm
-
-def run_gpu(args, cfg, name):
-    import torch
-    import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=dev)
-
-    import speculative_decoding_verification_72_gb300 as sv
-    sv.load_library()
-    steps = args.steps if args.steps is not None else 100000
-    warmup = max(3, args.warmup if args.warmup is not None else 200)
-
-    rows, alg_bytes = algorithmic_bytes(cfg)
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20) or (126 << 20)
-    first = make_inputs(cfg, rank_seed(cfg["seed"], rank), dev)
-    set_bytes = input_bytes(first)
-    nsets = max(2, min(64, math.ceil(4 * l2 / set_bytes)))
-    pool = [first] + [make_inputs(cfg, rank_seed(cfg["seed"] + 17 * i, rank), dev) for i in range(1, nsets)]
-    out = call(cfg, pool[0])
-    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
-    need = _workspace_need(cfg)
-    if ws.numel() < need:
-        ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize()
-
-    stream = torch.cuda.Stream(device=dev)
-    per_graph = nsets * max(1, math.ceil(32 / nsets))
-    graphs = {}
-
-    def graph_of(n):
-        if n not in graphs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                for i in range(n):               # warm the capture stream
-                    call(cfg, pool[i % nsets], out=out, ws=ws)
-                stream.synchronize()
-                with torch.cuda.graph(g, stream=stream):
-                    for i in range(n):
-                        call(cfg, pool[i % nsets], out=out, ws=ws)
-            torch.cuda.synchronize()
-            graphs[n] = g
-        return graphs[n]
-
-    full, rem = divmod(steps, per_graph)
-    g_full = graph_of(per_graph) if full else None
-    g_rem = graph_of(rem) if rem else None
-    g_warm = graph_of(per_graph)
-    for _ in range(max(1, math.ceil(warmup / per_graph))):
-        g_warm.replay()
-    torch.cuda.synchronize()
-
-    sampler = ClockSampler(local)
-    time.sleep(0.5)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(full):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    if world > 1:
-        dist.barrier()
-    elapsed = e0.elapsed_time(e1)
-    time.sleep(0.3)
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
-    elapsed = reduce_over_ranks(elapsed, "max", dev, world)
-
-    value = aggregate(elapsed, rows, steps, world)
-    step_s = elapsed / 1e3 / steps
-    peak, peak_kind = measured_peak()
-    read_bytes = None
-    if cfg.get("early"):
-        # Early exit reads only part of the logits: the roofline uses the bytes
-        # each input set's call actually read (mean over the pool), as reported
-        # by the library, while `value` still counts every verified row.
-        tot = 0
-        for x in pool:
-            r = call(cfg, x, out=out, ws=ws)
-            tot += int(r["bytes_read"].item())
-        read_bytes = tot / len(pool)
-    achieved = (read_bytes if read_bytes is not None else alg_bytes) / step_s / 1e9
-
-    e2e = _e2e(cfg, pool[0], dev, steps, out, ws)
-    if world > 1:   # the slowest replica's rate, times the replicas
-        e2e["value"] = reduce_over_ranks(e2e["value"], "min", dev, world) * world
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        xh = host_copy(pool[0])
-        rps, nreq = oracle_rows_per_s(cfg, xh, args.cpu_budget)
-        cpu = {"value": rps, "unit": "rows/s", "cores": 1, "kind": "oracle",
-               "sample": f"{nreq} of {cfg['B']} requests of one input set (~{args.cpu_budget:.0f} s), "
-                         f"float64 NumPy oracle, one thread"}
-
-    line = {
-        "metric": metric_name(cfg), "value": value, "unit": "rows/s", "n_gpus": world,
-        "steps": steps, "warmup": warmup, "ms_per_step": elapsed / steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
-        "data": "synthetic (seeded; shapes from the pages, no dataset or weights)",
-        "config": {"workload": cfg["workload"], "name": name, "B": cfg["B"],
-                   "rows_per_step": rows, "algorithmic_bytes_per_step": alg_bytes,
-                   **({"bytes_read_per_step": read_bytes,
-                       "roofline_bytes": "bytes actually read (library-reported), not all logit bytes"}
-                      if read_bytes is not None else {}),
-                   "l2_policy": f"rotating pool of {nsets} input sets, {nsets * set_bytes / 1e6:.0f} MB "
-                                f"> 4x L2 ({l2 / 1e6:.0f} MB)",
-                   "timing": f"CUDA graphs of {per_graph} calls, events on the launch stream",
-                   "parallelism": f"{world} independent replica(s)"},
-        "hbm_gbs": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": ("one verify call: row_stats_early_kernel (bytes it read) + decide kernel"
-                                if cfg.get("early") else
-                                "one build call: row_topk_kernel (all draft logit bytes) + tree_select_kernel"
-                                if cfg["kind"] == "tree_build" else
-                                "one compaction call: kv_compact_kernel (path rows read + written)"
-                                if cfg["kind"] == "kv_compact" else
-                                "one verify call: row_stats_kernel (all logit bytes) + decide kernel")
-                               + (" + draw kernels (chunk sums, pick)" if _launches_per_call(cfg) == 4 else ""),
-                     "traffic": recorded_traffic(name)},
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": steps * _launches_per_call(cfg),
-        "clocks": clocks,
-    }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
-
-
-def _launches_per_call(cfg):
-    return KERNELS_PER_CALL[cfg["kind"]] + (2 if cfg["kind"] == "tree" and cfg.get("T") else 0)
-
 
 def _workspace_need(cfg):
     import speculative_decoding_verification_72_gb300 as sv
@@ -612,6 +623,146 @@ def _workspace_need(cfg):
     if cfg["kind"] == "kv_compact":
         return 256
     return lib.spec_verify_tree_workspace_size(cfg["B"], cfg["N"], cfg["V"], dt)
+
+
+class GpuWorkload:
+    """One workload on this rank's GPU: a rotating pool of input sets larger
+    than 4x L2, caller-owned outputs and workspace, and CUDA graphs of calls."""
+
+    def __init__(self, cfg, name, dev, rank, stream):
+        import torch
+        self.cfg, self.name, self.dev, self.stream = cfg, name, dev, stream
+        self.rows, self.alg_bytes = algorithmic_bytes(cfg)
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20) or (126 << 20)
+        first = make_inputs(cfg, rank_seed(cfg["seed"], rank), dev)
+        self.set_bytes = input_bytes(first)
+        self.nsets = max(2, min(512, math.ceil(4 * l2 / self.set_bytes)))
+        self.pool = [first] + [make_inputs(cfg, rank_seed(cfg["seed"] + 17 * i, rank), dev)
+                               for i in range(1, self.nsets)]
+        self.out = call(cfg, self.pool[0])
+        self.ws = torch.empty(max(1 << 20, _workspace_need(cfg)), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        self.per_graph = self.nsets * max(1, math.ceil(32 / self.nsets))
+        self.graphs = {}
+        self.pool_desc = (f"{self.nsets} input sets, {self.nsets * self.set_bytes / 1e6:.0f} MB "
+                          f"> 4x L2 ({l2 / 1e6:.0f} MB); graphs of up to {self.per_graph} calls")
+
+    def graph_of(self, n):
+        import torch
+        if n not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                for i in range(n):               # warm the capture stream
+                    call(self.cfg, self.pool[i % self.nsets], out=self.out, ws=self.ws)
+                self.stream.synchronize()
+                with torch.cuda.graph(g, stream=self.stream):
+                    for i in range(n):
+                        call(self.cfg, self.pool[i % self.nsets], out=self.out, ws=self.ws)
+            torch.cuda.synchronize()
+            self.graphs[n] = g
+        return self.graphs[n]
+
+    def replay(self, steps):
+        """Enqueue exactly `steps` calls on self.stream."""
+        full, rem = divmod(steps, self.per_graph)
+        for _ in range(full):
+            self.graph_of(self.per_graph).replay()
+        if rem:
+            self.graph_of(rem).replay()
+
+    def prepare(self, steps, warmup):
+        import torch
+        full, rem = divmod(steps, self.per_graph)
+        if full:
+            self.graph_of(self.per_graph)
+        if rem:
+            self.graph_of(rem)
+        with torch.cuda.stream(self.stream):
+            self.replay(max(3, warmup))
+        torch.cuda.synchronize()
+
+    def bytes_read_per_call(self):
+        """Early exit: logit bytes the library reports it read, mean over the pool."""
+        tot = 0
+        for x in self.pool:
+            r = call(self.cfg, x, out=self.out, ws=self.ws)
+            tot += int(r["bytes_read"].item())
+        return tot / len(self.pool)
+
+
+def time_workload(wl, steps, world, sampler):
+    """Repetitions of exactly `steps` calls, each bracketed by a barrier and a
+    device synchronize and timed with CUDA events on the launch stream (the
+    slowest rank's time per repetition). At least MIN_REPS repetitions, more
+    until they span MIN_WINDOW_S of wall time."""
+    import torch
+    import torch.distributed as dist
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    reps_ms, nreps, t_first, t_last = [], MIN_REPS, None, None
+    while len(reps_ms) < nreps:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        tw0 = time.time()
+        with torch.cuda.stream(wl.stream):
+            e0.record(wl.stream)
+            wl.replay(steps)
+            e1.record(wl.stream)
+        torch.cuda.synchronize()
+        tw1 = time.time()
+        if world > 1:
+            dist.barrier()
+        t_first = tw0 if t_first is None else t_first
+        t_last = tw1
+        reps_ms.append(reduce_over_ranks(e0.elapsed_time(e1), "max", wl.dev, world))
+        if len(reps_ms) == 1:
+            rep_wall = reduce_over_ranks(tw1 - tw0, "max", wl.dev, world)
+            nreps = int(min(MAX_REPS, max(MIN_REPS, math.ceil(MIN_WINDOW_S / max(rep_wall, 1e-6)))))
+    med = float(np.median(reps_ms))
+    return {"ms_per_step": med / steps, "elapsed_ms": med, "steps": steps, "reps": len(reps_ms),
+            "rep_ms": {"min": float(min(reps_ms)), "median": med, "max": float(max(reps_ms))},
+            "window_s": t_last - t_first, "clocks": sampler.summary(t_first, t_last) if sampler else None}
+
+
+def kernel_desc(cfg):
+    if cfg.get("early"):
+        d = "one verify call: row_stats_early_kernel (bytes it read) + decide kernel"
+    elif cfg["kind"] == "tree_build":
+        d = "one build call: row_topk_kernel (all draft logit bytes) + tree_select_kernel"
+    elif cfg["kind"] == "kv_compact":
+        d = "one compaction call: kv_compact_kernel (path rows read + written)"
+    else:
+        d = "one verify call: row_stats_kernel (all logit bytes) + decide kernel"
+    return d + (" + draw kernels (chunk sums, pick)" if launches_per_call(cfg) == 4 else "")
+
+
+def roofline(cfg, name, ms_per_step, read_bytes=None):
+    """Bandwidth roofline of one call: algorithmic bytes (or the bytes an early
+    exit actually read) over the event-timed duration of the whole call, so
+    a lower bound on the row-statistics kernel's own rate."""
+    peak, kind = measured_peak()
+    _, alg = algorithmic_bytes(cfg)
+    achieved = (read_bytes if read_bytes is not None else alg) / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if kind == "measured" else "fallback 6.8 TB/s",
+            "kernel": kernel_desc(cfg), "traffic": recorded_traffic(name)}
+
+
+def per_config_entry(wl, t, world):
+    cfg = wl.cfg
+    rb = wl.bytes_read_per_call() if cfg.get("early") else None
+    e = {"workload": cfg["workload"], "metric": metric_name(cfg),
+         "value": aggregate(t["elapsed_ms"], wl.rows, t["steps"], world), "unit": "rows/s",
+         "ms_per_step": t["ms_per_step"], "steps": t["steps"], "reps": t["reps"], "rep_ms": t["rep_ms"],
+         "rows_per_step": wl.rows, "algorithmic_bytes_per_step": wl.alg_bytes,
+         "roofline": roofline(cfg, wl.name, t["ms_per_step"], rb), "clocks": t["clocks"],
+         "gpu_launches_per_step": launches_per_call(cfg), "pool": wl.pool_desc,
+         "contract": wl.name in CONTRACT_CONFIGS}
+    if rb is not None:
+        e["bytes_read_per_step"] = rb
+        e["roofline_bytes"] = "bytes actually read (library-reported), not all logit bytes"
+    return e
 
 
 def _e2e(cfg, x, dev, steps, out, ws):
@@ -661,6 +812,92 @@ def _e2e(cfg, x, dev, steps, out, ws):
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms}
 
 
+def run_gpu(args, cfg, name):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    steps = args.steps if args.steps is not None else 200
+    warmup = max(3, args.warmup if args.warmup is not None else 20)
+
+    # The CPU oracle legs run first: the all-core leg forks, which must happen
+    # before this process makes any CUDA call.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args.cpu_budget)
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    import speculative_decoding_verification_72_gb300 as sv
+    sv.load_library()
+    stream = torch.cuda.Stream(device=dev)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+
+    # headline workload: exactly `steps` calls per repetition
+    wl = GpuWorkload(cfg, name, dev, rank, stream)
+    wl.prepare(steps, warmup)
+    t = time_workload(wl, steps, world, sampler)
+    value = aggregate(t["elapsed_ms"], wl.rows, steps, world)
+    read_bytes = wl.bytes_read_per_call() if cfg.get("early") else None
+    roof = roofline(cfg, name, t["ms_per_step"], read_bytes)
+    per_config = {}
+    want_per_config = world == 1 and not args.no_per_config
+    if want_per_config:
+        if steps >= PER_CONFIG_MIN_STEPS:
+            per_config[name] = per_config_entry(wl, t, world)
+        else:
+            wl.prepare(PER_CONFIG_MIN_STEPS, 0)
+            per_config[name] = per_config_entry(wl, time_workload(wl, PER_CONFIG_MIN_STEPS, world, sampler), world)
+    e2e = _e2e(cfg, wl.pool[0], dev, steps, wl.out, wl.ws)
+    if world > 1:   # the slowest replica's rate, times the replicas
+        e2e["value"] = reduce_over_ranks(e2e["value"], "min", dev, world) * world
+    pool_desc = wl.pool_desc
+    del wl
+    torch.cuda.empty_cache()
+
+    if want_per_config:
+        for other in CONTRACT_CONFIGS + NEXT_CONFIGS:
+            if other == name:
+                continue
+            ow = GpuWorkload(CONFIGS[other], other, dev, rank, stream)
+            n_steps = max(steps, PER_CONFIG_MIN_STEPS)
+            ow.prepare(n_steps, warmup)
+            per_config[other] = per_config_entry(ow, time_workload(ow, n_steps, world, sampler), world)
+            del ow
+            torch.cuda.empty_cache()
+    time.sleep(0.3)
+    sampler.stop()
+
+    line = {
+        "metric": metric_name(cfg), "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": t["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg["dtype"] == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes from the pages, no dataset or weights)",
+        "config": config_dict(cfg, name, world),
+        "repetitions": {"count": t["reps"], "rep_ms": t["rep_ms"], "reported": "median repetition",
+                        "window_s": t["window_s"], "pool": pool_desc},
+        "hbm_gbs": roof["achieved"],
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": steps * launches_per_call(cfg) * t["reps"],
+        "gpu_launches_per_step": launches_per_call(cfg),
+        "clocks": t["clocks"],
+        "per_config": per_config or None,
+    }
+    if read_bytes is not None:
+        line["config"]["bytes_read_per_step"] = read_bytes
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -668,9 +905,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
-    ap.add_argument("--cpu-budget", type=float, default=10.0,
-                    help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle work for each cpu_baseline leg (one core, all cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time only the --config workload")
     args = ap.parse_args(argv)
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
