@@ -46,6 +46,15 @@
  *   - A device-side problem found in one request sets bits in out_status[b]
  *     (SV_STATUS_*); other requests are unaffected. Kernels never trap; every
  *     wait inside them is bounded (SV_STATUS_TIMEOUT if one gives up).
+ *   - Calls are asynchronous, so a wait that gives up inside a kernel cannot
+ *     be a return code of the call that launched it: it is the per-request bit
+ *     SV_STATUS_TIMEOUT. A caller that reads the status array back can turn it
+ *     into the return code SV_ERR_TIMEOUT with spec_verify_check_status.
+ *     A wait gives up after 20 ms of polling; time the context spends switched
+ *     out (time-slicing, preemption) is not counted beyond 1 ms per gap, so a
+ *     preempted call does not time out spuriously. A request with the bit set
+ *     has unspecified outputs: re-run the call once; a second timeout means
+ *     the device is not making progress and should be treated as failed.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -68,6 +77,8 @@ typedef int32_t sv_status;
 #define SV_ERR_CUDA                4  /* a CUDA launch or attribute call failed */
 #define SV_ERR_NOT_SUPPORTED       5  /* valid request this build does not implement
                                          (no call of this version returns it) */
+#define SV_ERR_TIMEOUT             6  /* a bounded wait inside a kernel gave up (returned
+                                         only by spec_verify_check_status) */
 
 /* Logit element types. */
 #define SV_F32  0
@@ -135,6 +146,16 @@ const char* spec_verify_status_string(sv_status s);
 
 /* Workspace bytes for a call with these sizes; 0 if the sizes are invalid.
  * Pure host functions: they touch no device. */
+
+/* One size for every verification entry point (mini-sglang PR #134,
+ * verify_drafts: one buffer serves any call): bytes that suffice for
+ * spec_verify_greedy / _greedy_ex / _greedy_early with K = rows_per_req - 1,
+ * spec_verify_sample / _sample_ex with K = rows_per_req - 1 (with or without
+ * draft logits, any rule), and spec_verify_tree / _tree_ex with
+ * N = rows_per_req when rows_per_req <= SV_MAX_TREE_NODES. 0 if B < 0,
+ * rows_per_req < 1, V < 1 or dtype is invalid. */
+size_t spec_verify_workspace_size(int32_t B, int32_t rows_per_req, int32_t V, int32_t dtype);
+
 size_t spec_verify_greedy_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype);
 size_t spec_verify_sample_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype,
                                          int32_t has_draft_logits);
@@ -323,6 +344,23 @@ sv_status spec_kv_compact(void* kv, int64_t token_stride_bytes, int32_t row_byte
                           const int32_t* num_accepted, int32_t B, int32_t max_nodes,
                           int32_t* out_len, int32_t* out_status, void* stream);
 
+/* Host-side reduction of a status array the caller has copied back to host
+ * memory (status_host[0..B-1], the out_status of a finished call):
+ * SV_ERR_TIMEOUT if any request has SV_STATUS_TIMEOUT, SV_ERR_INVALID_ARG if
+ * status_host is NULL with B > 0 or B < 0, else SV_OK (the other bits are
+ * per-request outcomes, not errors). Touches no device. */
+sv_status spec_verify_check_status(const int32_t* status_host, int32_t B);
+
+/* Self-test of the kernels' failure path, for health checks: enqueues one
+ * one-thread-block kernel that waits on an mbarrier phase nothing completes,
+ * with the same bounded wait the verification kernels use. The wait gives up
+ * after its limit (about 20 ms), the kernel writes SV_STATUS_TIMEOUT to
+ * out_status[0] (device memory, int32) and returns normally, so the context
+ * stays usable. No bulk copy or other asynchronous work is outstanding when
+ * the kernel exits. Returns SV_ERR_INVALID_ARG for a NULL or misaligned
+ * out_status, SV_ERR_CUDA if the launch fails. */
+sv_status spec_verify_selftest_wait(int32_t* out_status, void* stream);
+
 /* Bytes of the library's static scratch array used by
  * spec_verify_greedy_static (one array per GPU that loads the library). */
 #define SV_STATIC_SCRATCH_BYTES (2u << 20)
@@ -340,7 +378,10 @@ sv_status spec_kv_compact(void* kv, int64_t token_stride_bytes, int32_t row_byte
  * SV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * Set-up: the first call on each device (with that device current) looks up
  * the array's device address once; make that first call before any stream
- * capture. Every call shares the one array per device, and it keeps the last
+ * capture. The address is kept for the life of the process: after
+ * cudaDeviceReset (or anything else that destroys the device's primary
+ * context) it is stale, and this entry point must not be called again on that
+ * device in the same process. Every call shares the one array per device, and it keeps the last
  * call's contents: nothing in it has to start at zero (each call writes all it
  * reads), but two calls whose work overlaps on the GPU (different streams, or
  * concurrent host threads) race on it and must be serialised by the caller. */

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     __syncthreads();
     bool aborted = false;
     for (int g2 = tid; g2 < a.n_cta; g2 += kK2Threads) aborted |= (a.cta_bytes[g2] & kEarlyAbortBit) != 0;
-    if (__syncthreads_or(aborted) && tid == 0) s_status |= 32;   // TIMEOUT
+    if (__syncthreads_or(aborted) && tid == 0) s_status |= SV_STATUS_TIMEOUT;
   }
   int n = -1;
   int base = 0;
@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
         row_partials_merge(a.part, trow, tp, c, m, s, idx, err);
       }
       lp2row = m * c + log2f(s);
-      if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= 4;   // NONFINITE_ROW
-      if (err) st |= 32;                                                     // TIMEOUT
+      if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= SV_STATUS_NONFINITE_ROW;
+      if (err) st |= SV_STATUS_TIMEOUT;
       if (i < K) {
         if (a.greedy) {
           rej = in.bad || in.tok != idx;
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
             int id, ed;
             row_partials_merge(a.part, drow, dp, c, md, sd, id, ed);
             lq2row = md * c + log2f(sd);
-            if (!(fabsf(md) <= FLT_MAX) || !(sd > 0.f && sd <= FLT_MAX)) st |= 4;
-            if (ed) st |= 32;
+            if (!(fabsf(md) <= FLT_MAX) || !(sd > 0.f && sd <= FLT_MAX)) st |= SV_STATUS_NONFINITE_ROW;
+            if (ed) st |= SV_STATUS_TIMEOUT;
             if (!in.bad) {
               const float lq2 = in.y * c - lq2row;
               if (lp2 == -INFINITY && lq2 == -INFINITY) {
@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
       if (i <= nb) {
         int stat = st;
         if (i == nb && i < K) {
-          if (in.bad) stat |= 1;
-          if (zero) stat |= 8;
+          if (in.bad) stat |= SV_STATUS_BAD_TOKEN;
+          if (zero) stat |= SV_STATUS_ZERO_MASS;
         }
         if (stat) atomicOr(&s_status, stat);
       }
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
     const int par = a.parents[row];
     const int tok = a.tokens[row];
     const bool link_ok = (n == 0) ? (par == -1) : (par >= 0 && par < n);
-    if (!link_ok) atomicOr(&s_status, 2);   // BAD_PARENT
+    if (!link_ok) atomicOr(&s_status, SV_STATUS_BAD_PARENT);
     const int p = (n > 0 && link_ok) ? par : -1;
     sm_par[n] = p;
     sm_tok[n] = tok;
@@ -415,8 +415,9 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
     sm_m[n] = m;
     sm_l2[n] = m * c + log2f(s);
     sm_am[n] = idx;
-    sm_bad[n] = static_cast<unsigned char>(((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? 4 : 0) |
-                                           (err ? 32 : 0));
+    sm_bad[n] = static_cast<unsigned char>(
+        ((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? SV_STATUS_NONFINITE_ROW : 0) |
+        (err ? SV_STATUS_TIMEOUT : 0));
   }
   __syncthreads();
   if (tid == 0) {
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
       status |= sm_bad[cur];
       int kid = sm_first[cur];
       if (depth == a.max_depth && kid >= 0) {
-        status |= 16;   // DEPTH_EXCEEDED
+        status |= SV_STATUS_DEPTH_EXCEEDED;
         kid = -1;
       }
       if (a.greedy) {
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
         for (; kid >= 0; kid = sm_next[kid]) {
           const int t = sm_tok[kid];
           if (t < 0 || t >= a.V) {
-            status |= 1;
+            status |= SV_STATUS_BAD_TOKEN;
             continue;
           }
           if (t == am) {
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
         float lp2 = -INFINITY;
         bool counted = false;
         if (t < 0 || t >= a.V) {
-          status |= 1;
+          status |= SV_STATUS_BAD_TOKEN;
         } else {
           bool dup = false;
           for (int r = 0; r < nrej; ++r) dup |= (excl[r] == t);

@@ -48,7 +48,7 @@ constexpr int kK3Req = 8;           // requests whose descriptor and exclusions 
 constexpr int kK3LocalExcl = 64;    // exclusions cached per request
 constexpr int kK3MaxChunks = 256;   // chunk sums the pick kernel stages in shared memory
 constexpr int kK3PickThreads = 1024;
-constexpr int kStatusWaitErr = 32;
+constexpr int kStatusWaitErr = SV_STATUS_TIMEOUT;
 
 template <int ES>
 constexpr int kK3ChunkElems = kK3ChunkBytes / ES;

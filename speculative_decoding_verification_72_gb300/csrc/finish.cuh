@@ -16,8 +16,8 @@
 
 namespace sv {
 
-constexpr int kStatusStopped = 64;
-constexpr int kStatusCapped = 128;
+constexpr int kStatusStopped = SV_STATUS_STOPPED;
+constexpr int kStatusCapped = SV_STATUS_CAPPED;
 constexpr int kMaxStopIds = 16;
 
 struct FinishArgs {

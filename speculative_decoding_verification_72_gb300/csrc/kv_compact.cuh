@@ -26,7 +26,7 @@ namespace sv {
 constexpr int kKvThreads = 256;
 constexpr int kKvChunkBytes = kKvThreads * 16;
 constexpr int kKvStepBatch = 8;
-constexpr int kStatusBadPage = 256;
+constexpr int kStatusBadPage = SV_STATUS_BAD_PAGE;
 
 struct KvCompactArgs {
   uint8_t* kv;

@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
   }
   bad = __syncthreads_or(bad);
   err = __syncthreads_or(err);
-  if (lane == 0 && a.out_status) a.out_status[b] = (bad ? 4 : 0) | (err ? 32 : 0);   // NONFINITE_ROW, TIMEOUT
+  if (lane == 0 && a.out_status) a.out_status[b] = (bad ? SV_STATUS_NONFINITE_ROW : 0) | (err ? SV_STATUS_TIMEOUT : 0);
 }
 
 }  // namespace sv

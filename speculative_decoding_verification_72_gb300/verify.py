@@ -29,6 +29,11 @@ STATUS_NONFINITE_ROW = 4
 STATUS_ZERO_MASS = 8
 STATUS_DEPTH_EXCEEDED = 16
 STATUS_TIMEOUT = 32
+STATUS_STOPPED = 64
+STATUS_CAPPED = 128
+STATUS_BAD_PAGE = 256
+
+SV_ERR_TIMEOUT = 6
 
 _LIB = None
 _LOCK = threading.Lock()
@@ -79,6 +84,9 @@ _SIGS = {
     "spec_verify_greedy_early": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                         _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_tree_build_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "spec_verify_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "spec_verify_check_status": (_I32, [_P, _I32]),
+    "spec_verify_selftest_wait": (_I32, [_P, _P]),
     "spec_tree_build": (_I32, [_P, _I32, _I64, _I32, _I32, _I32, _I32, _I32, _F,
                                _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_kv_compact": (_I32, [_P, _I64, _I32, _P, _I32, _I32, _P, _P, _I32, _P, _I32, _I32, _P, _P, _P]),
@@ -426,4 +434,37 @@ def spec_kv_compact(kv, page_table, seq_base, path_nodes, num_accepted, max_node
                              pn.shape[1], _ptr(na), B, int(max_nodes), _ptr(out["out_len"]), _ptr(out["status"]),
                              ctypes.c_void_p(stream))
     _check(rc)
+    return out
+
+
+def spec_verify_workspace_size(B, rows_per_req, V, dtype):
+    """Workspace bytes that serve every verification entry point for B
+    requests of rows_per_req target rows of V logits (include/spec_verify.h);
+    dtype is torch.float32 or torch.bfloat16."""
+    code = SV_F32 if dtype == torch.float32 else SV_BF16 if dtype == torch.bfloat16 else None
+    if code is None:
+        raise SpecVerifyError(f"dtype must be float32 or bfloat16, got {dtype}")
+    need = load_library().spec_verify_workspace_size(int(B), int(rows_per_req), int(V), code)
+    if need == 0:
+        raise SpecVerifyError("invalid sizes")
+    return need
+
+
+def spec_verify_check_status(status):
+    """SV_OK, or SV_ERR_TIMEOUT if any request's status has STATUS_TIMEOUT
+    (status: int32 tensor, copied to the host)."""
+    h = status.detach().to("cpu", torch.int32).contiguous()
+    return load_library().spec_verify_check_status(_ptr(h), int(h.numel()))
+
+
+def spec_verify_selftest_wait(device=None):
+    """Runs the library's bounded-wait self-test on `device` (default: the
+    current CUDA device) and returns the int32 status it wrote (device
+    tensor [1]): STATUS_TIMEOUT when the wait gave up as designed."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if dev.type != "cuda":
+        raise SpecVerifyError("the self-test needs a CUDA device")
+    out = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(load_library().spec_verify_selftest_wait(_ptr(out), ctypes.c_void_p(stream)))
     return out

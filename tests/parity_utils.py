@@ -9,6 +9,13 @@ Rules (fixed by the verification contract):
     or, when u*S lies within 1e-5*S of a CDF boundary, be one of the tokens
     whose cells meet that band (oracle draw_band); those are counted too;
   * log-probs and mu agree to 1e-4 absolute.
+
+The draw-band exemption goes beyond the contract's stated rules (which name
+only the accept-test near tie): a final draw whose u*S sits within 1e-5*S of
+a CDF boundary has two valid answers at the stated precision. Every
+stochastic comparison therefore also bounds how many requests it exempts
+(max_exempt, default max(2, B // 16)), so a systematic divergence cannot hide
+behind the exemptions.
 """
 
 import numpy as np
@@ -29,8 +36,9 @@ def f64(t):
     return host(t).astype(np.float64)
 
 
-def compare(got, ref, stochastic=False, keys_exact=("tokens",), check_status=True):
-    """Returns the number of requests exempted by a near tie."""
+def compare(got, ref, stochastic=False, keys_exact=("tokens",), check_status=True, max_exempt=None):
+    """Returns the number of requests exempted by a near tie (asserted to be
+    at most max_exempt, default max(2, B // 16), in stochastic comparisons)."""
     tok_g = host(got["tokens"]).astype(np.int64)
     tok_r = ref["tokens"]
     B, W = tok_r.shape
@@ -69,4 +77,7 @@ def compare(got, ref, stochastic=False, keys_exact=("tokens",), check_status=Tru
             if check_status:
                 assert st_g[b] == ref["status"][b], f"{msg}: status {st_g[b]} vs {ref['status'][b]}"
             assert np.array_equal(tok_g[b], tok_r[b]), msg
+    if stochastic:
+        bound = max(2, B // 16) if max_exempt is None else max_exempt
+        assert exempt <= bound, f"{exempt} of {B} requests exempted (bound {bound})"
     return exempt

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "spec_verify.h")
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED_DTYPE = 0, 1, 2
-SV_ERR_WORKSPACE_TOO_SMALL, SV_ERR_NOT_SUPPORTED = 3, 5
+SV_ERR_WORKSPACE_TOO_SMALL, SV_ERR_NOT_SUPPORTED, SV_ERR_TIMEOUT = 3, 5, 6
 FAKE = 0x10000          # 64 KB-aligned stand-in for a device pointer; never dereferenced
 
 
@@ -37,7 +37,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("spec_verify_greedy", "spec_verify_sample", "spec_verify_tree",
               "spec_verify_greedy_ex", "spec_verify_sample_ex", "spec_verify_tree_ex",
-              "spec_verify_status_string", "spec_verify_abi_version"):
+              "spec_verify_status_string", "spec_verify_abi_version", "spec_verify_workspace_size",
+              "spec_verify_check_status", "spec_verify_selftest_wait"):
         assert n in names
 
 
@@ -49,7 +50,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.spec_verify_abi_version() == 2
-    for code in range(6):
+    for code in range(7):
         s = lib.spec_verify_status_string(code).decode()
         assert s and "unknown" not in s
     assert "unknown" in lib.spec_verify_status_string(99).decode()
@@ -65,6 +66,70 @@ def test_workspace_sizes(lib):
     assert lib.spec_verify_greedy_workspace_size(4, 5, 100, 7) == 0    # dtype
     assert lib.spec_verify_tree_workspace_size(4, 2000, 100, 1) == 0   # N too large
     assert lib.spec_verify_greedy_workspace_size(0, 5, 100, 1) > 0
+
+
+def test_one_workspace_size_serves_every_verification_call(lib):
+    for B, R, Vv, dt in ((32, 6, 128256, 1), (64, 5, 151936, 0), (32, 64, 128256, 1), (8, 4096, 50257, 1),
+                         (1, 1, 7, 0), (0, 6, 100, 1)):
+        one = lib.spec_verify_workspace_size(B, R, Vv, dt)
+        assert one > 0 and one % 256 == 0
+        assert one >= lib.spec_verify_greedy_workspace_size(B, R - 1, Vv, dt)
+        assert one >= lib.spec_verify_sample_workspace_size(B, R - 1, Vv, dt, 1)
+        assert one >= lib.spec_verify_sample_workspace_size(B, R - 1, Vv, dt, 0)
+        if R <= 1024:
+            assert one >= lib.spec_verify_tree_workspace_size(B, R, Vv, dt)
+        # and it is the largest of them, not more
+        needs = [lib.spec_verify_greedy_workspace_size(B, R - 1, Vv, dt),
+                 lib.spec_verify_sample_workspace_size(B, R - 1, Vv, dt, 1),
+                 lib.spec_verify_sample_workspace_size(B, R - 1, Vv, dt, 0)]
+        if R <= 1024:
+            needs.append(lib.spec_verify_tree_workspace_size(B, R, Vv, dt))
+        assert one == max(needs)
+    assert lib.spec_verify_workspace_size(4, 0, 100, 1) == 0      # rows_per_req < 1
+    assert lib.spec_verify_workspace_size(-1, 6, 100, 1) == 0
+    assert lib.spec_verify_workspace_size(4, 6, 0, 1) == 0
+    assert lib.spec_verify_workspace_size(4, 6, 100, 5) == 0      # dtype
+
+
+def test_check_status_turns_the_timeout_bit_into_a_return_code(lib):
+    arr = (ctypes.c_int32 * 4)(0, 4, 64, 128)
+    assert lib.spec_verify_check_status(arr, 4) == SV_OK            # per-request outcomes, not errors
+    arr[2] = 64 | 32
+    assert lib.spec_verify_check_status(arr, 4) == SV_ERR_TIMEOUT
+    assert lib.spec_verify_check_status(arr, 2) == SV_OK            # only the first B are read
+    assert lib.spec_verify_check_status(None, 0) == SV_OK
+    assert lib.spec_verify_check_status(None, 3) == SV_ERR_INVALID_ARG
+    assert lib.spec_verify_check_status(arr, -1) == SV_ERR_INVALID_ARG
+    assert "TIMEOUT" in lib.spec_verify_status_string(SV_ERR_TIMEOUT).decode()
+
+
+def test_selftest_rejects_bad_pointers(lib):
+    assert lib.spec_verify_selftest_wait(None, None) == SV_ERR_INVALID_ARG
+    assert lib.spec_verify_selftest_wait(ctypes.c_void_p(FAKE + 2), None) == SV_ERR_INVALID_ARG
+
+
+def test_status_bits_match_the_header():
+    text = open(HEADER).read()
+    for name, val in (("SV_STATUS_BAD_TOKEN", V.STATUS_BAD_TOKEN), ("SV_STATUS_BAD_PARENT", V.STATUS_BAD_PARENT),
+                      ("SV_STATUS_NONFINITE_ROW", V.STATUS_NONFINITE_ROW), ("SV_STATUS_ZERO_MASS", V.STATUS_ZERO_MASS),
+                      ("SV_STATUS_DEPTH_EXCEEDED", V.STATUS_DEPTH_EXCEEDED), ("SV_STATUS_TIMEOUT", V.STATUS_TIMEOUT),
+                      ("SV_STATUS_STOPPED", V.STATUS_STOPPED), ("SV_STATUS_CAPPED", V.STATUS_CAPPED),
+                      ("SV_STATUS_BAD_PAGE", V.STATUS_BAD_PAGE), ("SV_ERR_TIMEOUT", V.SV_ERR_TIMEOUT)):
+        m = re.search(r"#define\s+" + name + r"\s+(\d+)", text)
+        assert m and int(m.group(1)) == val, name
+
+
+def test_kernels_take_status_bits_from_the_header():
+    """No kernel source spells a status bit as a number: each names the
+    header's constant, so kernels and ABI cannot drift apart."""
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_72_gb300", "csrc")
+    pat = re.compile(r"(status\w*\s*(\|=|=)\s*[1-9])|(\bst\s*\|=\s*[1-9])|(stat\s*\|=\s*[1-9])|"
+                     r"(atomicOr\(&s_status,\s*[1-9])|(\?\s*(4|32)\s*:\s*0)")
+    for name in os.listdir(csrc):
+        if name.endswith((".cu", ".cuh")):
+            for i, line in enumerate(open(os.path.join(csrc, name)), 1):
+                code = line.split("//")[0]
+                assert not pat.search(code), f"{name}:{i}: literal status bit: {line.strip()}"
 
 
 def _greedy(lib, **kw):

@@ -221,7 +221,10 @@ def test_relaxed_extremes_and_temperature():
     ci.draft_tokens = W.toy_greedy_drafts(ci.target, p_match=0.5, seed=4)
     got = gpu_sample(ci, O.RULE_RELAXED, 0.0, 1.0, with_draft=False)
     assert (host(got["num_accepted"]) == 4).all()
-    compare(got, oracle_sample(ci, O.RULE_RELAXED, 0.0, 1.0, with_draft=False), stochastic=True)
+    # tau = 0: any draft with p < 1e-5 counts as a near tie of p >= tau although
+    # acceptance is certain (asserted above), so the exemption count is unbounded here
+    compare(got, oracle_sample(ci, O.RULE_RELAXED, 0.0, 1.0, with_draft=False), stochastic=True,
+            max_exempt=ci.target.shape[0])
     got = gpu_sample(ci, O.RULE_RELAXED, 1.5, 1.0, with_draft=False)
     assert (host(got["num_accepted"]) == 0).all()
     ci2 = W.stochastic_chain(B=16, K=3, V=5000, temperature=0.7, seed=12, device=DEV)
