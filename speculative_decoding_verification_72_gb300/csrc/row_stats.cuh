@@ -76,6 +76,13 @@ struct RowStatsArgs {
   int32_t G;           // CTAs
   float c;             // log2(e) / T
   Partial* partials;   // [rows + G]: slot row + cta, one per (CTA, row piece)
+  // L2 retention for a later re-read (stochastic chains, whose draw re-reads
+  // the rows of the first rejected position): rows at chain position
+  // < keep_pos (position = row mod rows_per_req0 in set0, mod rows_per_req1 in
+  // set1) are copied with evict_last, all others with evict_first. keep_pos = 0:
+  // plain copies.
+  int32_t keep_pos;
+  int32_t rows_per_req0, rows_per_req1;
 };
 
 // CTA that owns flattened element e under the equal split of T elements:
@@ -234,13 +241,15 @@ constexpr int kStageFullVecs = kStageVecs * kK1ConsumerThreads;
 // single code path for every stage.
 template <int ES>
 __device__ __forceinline__ void mask_stage(uint4* sv4, int ct, int nvec, int jbase, int j0, int j1,
-                                           int mask_lo_v, int mask_hi_v) {
+                                           int mask_lo_v, int mask_hi_v, int nh = 2) {
   constexpr int N = Elem<ES>::kVec;
   constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;   // -inf in every element
 #pragma unroll
   for (int k = 0; k < kStageVecs; ++k) {
     const int v = ct + k * kK1ConsumerThreads;
-    if (v >= nvec) {
+    if (k >= nh * kGroupVecs) {
+      // a half the warp does not fold (stage_halves): left as the copy wrote it
+    } else if (v >= nvec) {
       sv4[v] = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
     } else if (v == mask_lo_v || v == mask_hi_v) {
       const uint4 q = sv4[v];
@@ -333,6 +342,47 @@ __device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int c
   }
 }
 
+// Halves of a stage that warp cw folds: a short stage (nvec vectors, the last
+// of a piece) holds no data for this warp in half h when the warp's first
+// vector of that half, v = 32 cw + 4 h kK1ConsumerThreads, is past nvec; such
+// halves are neither masked nor folded. Warp-uniform, so no lane diverges.
+__device__ __forceinline__ int stage_halves(int cw, int nvec) {
+  if (cw * 32 >= nvec) return 0;
+  if (cw * 32 + kGroupVecs * kK1ConsumerThreads >= nvec) return 1;
+  return 2;
+}
+
+// fold_stage over the first `nh` halves of the stage (nh from stage_halves):
+// two halves is fold_stage itself; one half folds vectors k = 0..3 only, with
+// the same rescaling, re-summing and argmax bookkeeping.
+template <int ES>
+__device__ __forceinline__ void fold_stage_n(const uint4* sv4, uint4* stash, int ct, int jbase, int sg, float c,
+                                             float& m, float& mc, float& s, GroupCand& cand, int nh) {
+  if (nh == 2) {
+    fold_stage<ES>(sv4, stash, ct, jbase, sg, c, m, mc, s, cand);
+    return;
+  }
+  if (nh == 0) return;
+  uint32_t w[kGroupWords];
+  load_half(sv4, ct, 0, w);
+  const float gsum = group_sum<ES>(w, c, mc);
+  const float gmax = group_max<ES>(w);
+  if (gmax > m) {
+    const float nmc = gmax * c;
+    const float d = mc - nmc;
+    if (gsum <= FLT_MAX && d <= 20.f) {
+      s = (s + gsum) * ex2(d);
+    } else {
+      s = (m == -INFINITY ? 0.f : s * ex2(d)) + group_sum<ES>(w, c, nmc);
+    }
+    m = gmax;
+    mc = nmc;
+    stash_half(sv4, stash, ct, 0, jbase, sg, cand);
+  } else if (gmax > -INFINITY) {
+    s += gsum;
+  }
+}
+
 // Lowest index in [j0, j1) of the thread's candidate holding the value m,
 // read back from its stash (all four vectors loaded before the search);
 // INT_MAX if m is -inf.
@@ -396,8 +446,13 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
       int st = 0, slot = 0;
       uint32_t phase = 0;   // parity of the current use of `slot`
       bool ok = true;
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_drop = l2_policy_evict_first();
       for (int row = row0, j0 = j00; E0 < E1 && ok; ++row, j0 = 0) {
         const Piece p = make_piece<ES>(a, row, j0, E1);
+        bool keep = false;
+        if (a.keep_pos > 0)
+          keep = (row < a.set0.rows ? row % a.rows_per_req0 : (row - a.set0.rows) % a.rows_per_req1) < a.keep_pos;
         for (int s = 0; s < p.nst; ++s, ++st) {
           // the slot's previous use (parity phase ^ 1) must have been released
           if (st >= kK1Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) {
@@ -409,8 +464,12 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
                                      static_cast<uint32_t>(p.cp_hi - p.cp_lo) - off);
           const uint32_t fb = smem_u32(&full_bar[slot]);
           mbar_arrive_expect_tx(fb, bytes);
-          bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off),
-                   bytes, fb);
+          if (a.keep_pos > 0)
+            bulk_g2s_hint(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off),
+                          bytes, fb, keep ? pol_keep : pol_drop);
+          else
+            bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off), bytes,
+                     fb);
           if (++slot == kK1Stages) {
             slot = 0;
             phase ^= 1;
@@ -461,12 +520,13 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
           ok = false;   // stop consuming (and releasing); the producer times out too
         } else {
           uint4* sv4 = reinterpret_cast<uint4*>(ring + slot * kK1StageBytes);
+          const int nh = sg == last ? stage_halves(cw, last_nvec) : 2;
           if ((sg == 0 && first_edge) || (sg == last && last_edge)) {
             const int nvec = sg == last ? last_nvec : kStageFullVecs;
             mask_stage<ES>(sv4, ct, nvec, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,
-                           (sg == last && last_hull) ? nvec - 1 : -1);
+                           (sg == last && last_hull) ? nvec - 1 : -1, nh);
           }
-          fold_stage<ES>(sv4, stash, ct, jbase, sg, c, m, mc, s, cand);
+          fold_stage_n<ES>(sv4, stash, ct, jbase, sg, c, m, mc, s, cand, nh);
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
         }
@@ -483,12 +543,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
 
     // Warp: max, the lowest index among lanes holding it, and the sum
     // rescaled to the warp max (fixed shuffle order).
-    float wm = m;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-    int widx = (m == wm) ? resolve_cand<ES>(cand, stash, ct, m, p.j0, p.j1) : INT_MAX;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) widx = min(widx, __shfl_xor_sync(0xffffffffu, widx, o));
+    const float wm = warp_max(m);
+    const int widx = warp_min_nonneg((m == wm) ? resolve_cand<ES>(cand, stash, ct, m, p.j0, p.j1) : INT_MAX);
     float ws = (m == -INFINITY) ? 0.f : s * ex2((m - wm) * c);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);

@@ -193,12 +193,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
     for (int j = p.tail_begin + ct; j < p.j1; j += kK1ConsumerThreads)
       fold_scalar(Elem<ES>::load(p.rowp, j), j, c, m, mc, s, cand);
     if (m > -INFINITY) ref = mc;
-    float wm = m;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-    int widx = (m == wm) ? resolve_cand<ES>(cand, stash, ct, m, p.j0, p.j1) : INT_MAX;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) widx = min(widx, __shfl_xor_sync(0xffffffffu, widx, o));
+    const float wm = warp_max(m);
+    const int widx = warp_min_nonneg((m == wm) ? resolve_cand<ES>(cand, stash, ct, m, p.j0, p.j1) : INT_MAX);
     float ws = (m == -INFINITY) ? 0.f : s * ex2((m - wm) * c);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);

@@ -12,6 +12,7 @@
 // results after it (the top-k kernel waits first, so a wait on it also
 // covers K1).
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -25,6 +26,7 @@
 #include "rules.cuh"
 #include "tree_build.cuh"
 #include "kv_compact.cuh"
+#include "selftest.cuh"
 
 namespace {
 
@@ -90,17 +92,61 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
   return true;
 }
 
-// SM count of the current device (looked up once per device).
-int sm_count() {
-  static int count[64] = {0};
+// Per-device facts looked up once (SM count, kernel attributes set). Reads
+// take an atomic fast path; the first lookup on a device runs under a mutex,
+// so concurrent first calls from several host threads are safe. Devices past
+// kMaxDevices are not cached (looked up on every call).
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_cache_mu;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<uint32_t> g_attr_done[kMaxDevices];
+
+int current_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (count[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    count[dev] = n;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+// SM count of the current device.
+int sm_count() {
+  const int dev = current_device();
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached) {
+    const int n = g_sm_count[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
   }
-  return count[dev];
+  std::lock_guard<std::mutex> lock(g_dev_cache_mu);
+  if (cached && g_sm_count[dev].load(std::memory_order_relaxed) > 0) return g_sm_count[dev].load();
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (cached) g_sm_count[dev].store(n, std::memory_order_release);
+  return n;
+}
+
+// Runs `set` (kernel attribute calls) once per device for the attribute group
+// `bit`; a failed attempt is retried on the next call.
+enum AttrBit : uint32_t { kAttrK1 = 1, kAttrK1Early = 2, kAttrRowTopk = 4, kAttrDraw = 8 };
+
+template <typename F>
+cudaError_t once_per_device(uint32_t bit, F&& set) {
+  const int dev = current_device();
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && (g_attr_done[dev].load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(g_dev_cache_mu);
+  if (cached && (g_attr_done[dev].load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+  const cudaError_t e = set();
+  if (e == cudaSuccess && cached) g_attr_done[dev].fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+// Largest dynamic shared memory and the largest shared-memory carveout, so
+// two rings fit on one SM.
+template <typename Kern>
+cudaError_t set_smem_attrs(Kern kernel, int smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
 }
 
 // K1 grid for this device: kK1CtasPerSm per SM, fewer for small problems.
@@ -157,36 +203,17 @@ cudaError_t launch(Kern kernel, int grid, int block, size_t smem, cudaStream_t s
 
 template <int ES>
 cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t stream) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(row_stats_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kK1SmemBytes);
-    if (e != cudaSuccess) return e;
-    // The largest shared-memory carveout, so kK1CtasPerSm rings fit on one SM.
-    e = cudaFuncSetAttribute(row_stats_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  const cudaError_t e = once_per_device(kAttrK1 << (ES == 2 ? 0 : 8),
+                                        [] { return set_smem_attrs(row_stats_kernel<ES>, kK1SmemBytes); });
+  if (e != cudaSuccess) return e;
   return launch(row_stats_kernel<ES>, a.G, kK1Threads, kK1SmemBytes, stream, true, a);
 }
 
 template <int ES>
 cudaError_t launch_row_stats_early(const EarlyArgs& e, cudaStream_t stream) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(row_stats_early_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kK1SmemBytes);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(row_stats_early_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
-  }
+  const cudaError_t err = once_per_device(kAttrK1Early << (ES == 2 ? 0 : 8),
+                                          [] { return set_smem_attrs(row_stats_early_kernel<ES>, kK1SmemBytes); });
+  if (err != cudaSuccess) return err;
   return launch(row_stats_early_kernel<ES>, e.rs.G, kK1Threads, kK1SmemBytes, stream, true, e);
 }
 
@@ -228,7 +255,35 @@ RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride,
   r.G = k1_grid(pl.T, es);
   r.c = c;
   r.partials = reinterpret_cast<Partial*>(static_cast<uint8_t*>(ws) + pl.off_part);
+  r.keep_pos = 0;
+  r.rows_per_req0 = 1;
+  r.rows_per_req1 = 1;
   return r;
+}
+
+// L2 bytes of the current device (looked up once per device).
+int64_t l2_bytes() {
+  static std::atomic<int64_t> cached[kMaxDevices];
+  const int dev = current_device();
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int64_t v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) n = 0;
+  if (dev >= 0 && dev < kMaxDevices && n > 0) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Chain positions whose rows a stochastic call keeps in L2 for the draw's
+// re-read: the first rejection is most likely early, so positions 0, 1, ...
+// are kept while their target (and draft) rows fit in 3/4 of L2; 0 keeps none.
+int32_t keep_positions(int64_t B, int64_t K, int64_t V, int es, bool with_draft) {
+  const int64_t per_pos = B * V * es * (with_draft ? 2 : 1);
+  const int64_t budget = l2_bytes() * 3 / 4;
+  if (per_pos <= 0 || budget <= 0) return 0;
+  const int64_t k = budget / per_pos;
+  return static_cast<int32_t>(k > K + 1 ? K + 1 : k);
 }
 
 DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride, int64_t rows_t, const void* dft,
@@ -272,37 +327,19 @@ DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride, int64_t 
 // Draft-tree construction's row pass (a TMA ring of kTbSmemBytes per CTA).
 template <int ES>
 cudaError_t launch_row_topk(const RowTopkArgs& a, int grid, cudaStream_t stream) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(row_topk_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kTbSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(row_topk_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  const cudaError_t e = once_per_device(kAttrRowTopk << (ES == 2 ? 0 : 8),
+                                        [] { return set_smem_attrs(row_topk_kernel<ES>, kTbSmemBytes); });
+  if (e != cudaSuccess) return e;
   return launch(row_topk_kernel<ES>, grid, kTbThreads, kTbSmemBytes, stream, true, a);
 }
 
 // The draw: chunk sums over the drawn rows (K3a), then the pick (K3b).
 template <int ES>
 cudaError_t launch_draw(const DrawArgs& d, cudaStream_t stream) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(draw_sum_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kK3SmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(draw_sum_kernel<ES>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  cudaError_t e = launch(draw_sum_kernel<ES>, d.G, kK3Threads, kK3SmemBytes, stream, true, d);
+  cudaError_t e = once_per_device(kAttrDraw << (ES == 2 ? 0 : 8),
+                                  [] { return set_smem_attrs(draw_sum_kernel<ES>, kK3SmemBytes); });
+  if (e != cudaSuccess) return e;
+  e = launch(draw_sum_kernel<ES>, d.G, kK3Threads, kK3SmemBytes, stream, true, d);
   if (e != cudaSuccess) return e;
   return launch(draw_pick_kernel<ES>, d.B, kK3PickThreads, 0, stream, true, d);
 }
@@ -341,6 +378,7 @@ const char* spec_verify_status_string(sv_status s) {
     case SV_ERR_WORKSPACE_TOO_SMALL: return "SV_ERR_WORKSPACE_TOO_SMALL: workspace_bytes is below the required size";
     case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA launch failed";
     case SV_ERR_NOT_SUPPORTED: return "SV_ERR_NOT_SUPPORTED: valid request not implemented by this build";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded wait inside a kernel gave up (SV_STATUS_TIMEOUT)";
     default: return "unknown sv_status";
   }
 }
@@ -368,6 +406,36 @@ size_t spec_verify_tree_workspace_size(int32_t B, int32_t N, int32_t V, int32_t 
       !make_plan(static_cast<int64_t>(B) * N, 0, B, V, elem_size(dtype), true, N, 0, &pl))
     return 0;
   return pl.total;
+}
+
+size_t spec_verify_workspace_size(int32_t B, int32_t rows_per_req, int32_t V, int32_t dtype) {
+  if (B < 0 || rows_per_req < 1 || V < 1 || elem_size(dtype) == 0) return 0;
+  const int32_t K = rows_per_req - 1;
+  size_t need = spec_verify_greedy_workspace_size(B, K, V, dtype);
+  const size_t with_draft = spec_verify_sample_workspace_size(B, K, V, dtype, 1);
+  const size_t without = spec_verify_sample_workspace_size(B, K, V, dtype, 0);
+  if (need == 0 || with_draft == 0 || without == 0) return 0;
+  need = need > with_draft ? need : with_draft;
+  need = need > without ? need : without;
+  if (rows_per_req <= SV_MAX_TREE_NODES) {
+    const size_t tree = spec_verify_tree_workspace_size(B, rows_per_req, V, dtype);
+    if (tree == 0) return 0;
+    need = need > tree ? need : tree;
+  }
+  return need;
+}
+
+sv_status spec_verify_check_status(const int32_t* status_host, int32_t B) {
+  if (B < 0 || (B > 0 && !status_host)) return SV_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < B; ++b)
+    if (status_host[b] & SV_STATUS_TIMEOUT) return SV_ERR_TIMEOUT;
+  return SV_OK;
+}
+
+sv_status spec_verify_selftest_wait(int32_t* out_status, void* stream) {
+  if (!out_status || !aligned(out_status, 4)) return SV_ERR_INVALID_ARG;
+  const cudaError_t e = launch(selftest_wait_kernel, 1, 32, 0, static_cast<cudaStream_t>(stream), false, out_status);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 sv_status spec_verify_greedy(const void* target_logits, int32_t dtype, int64_t row_stride,
@@ -473,8 +541,11 @@ sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_
   if (workspace_bytes < pl.total) return SV_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float c = kLog2e / temperature;
-  const RowStatsArgs r = row_stats_args(pl, target_logits, row_stride, rows_t, draft_logits,
-                                        draft_row_stride, rows_d, V, es, c, workspace);
+  RowStatsArgs r = row_stats_args(pl, target_logits, row_stride, rows_t, draft_logits, draft_row_stride, rows_d,
+                                  V, es, c, workspace);
+  r.keep_pos = keep_positions(B, K, V, es, draft_logits != nullptr);
+  r.rows_per_req0 = K + 1;
+  r.rows_per_req1 = K > 0 ? K : 1;
   cudaError_t e = es == 2 ? launch_row_stats<2>(r, st) : launch_row_stats<4>(r, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(workspace);

@@ -8,6 +8,10 @@
 #include <cfloat>
 #include <cuda_runtime.h>
 
+// Status bits and return codes are the C ABI's (include/spec_verify.h), so
+// kernels and header cannot drift apart.
+#include "spec_verify.h"
+
 namespace sv {
 
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -97,17 +101,25 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase: gives up after kWaitNs of wall time (or
-// an iteration cap) and returns false; it never spins forever.
-constexpr uint64_t kWaitNs = 20ull * 1000ull * 1000ull;  // 20 ms
+// Bounded wait on an mbarrier phase: gives up and returns false after kWaitNs
+// of polling (or kWaitIters polls); it never spins forever. The time between
+// two polls is counted at most kWaitGapNs, so a context that is switched out
+// while it waits (time-slicing with another process, compute preemption) does
+// not give up early because the global timer ran on meanwhile.
+constexpr uint64_t kWaitNs = 20ull * 1000ull * 1000ull;  // 20 ms of polling
+constexpr uint64_t kWaitGapNs = 1000ull * 1000ull;      // 1 ms
 constexpr uint32_t kWaitIters = 1u << 22;
 
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  uint64_t prev = global_timer_ns(), spent = 0;
   for (uint32_t it = 1; it < kWaitIters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u && global_timer_ns() - t0 > kWaitNs) return false;
+    const uint64_t now = global_timer_ns();
+    const uint64_t gap = now - prev;
+    spent += gap < kWaitGapNs ? gap : kWaitGapNs;
+    prev = now;
+    if (spent > kWaitNs) return false;
   }
   return false;
 }
@@ -121,6 +133,45 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Warp-wide maximum of a float in one instruction (redux.sync, sm_100 and
+// later). NaN inputs are ignored, as with fmaxf.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Warp-wide minimum of a non-negative int in one instruction.
+__device__ __forceinline__ int warp_min_nonneg(int v) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(static_cast<uint32_t>(v)));
+  return static_cast<int>(r);
+}
+
+// 1-D bulk copy global -> shared with an L2 eviction-priority hint (a policy
+// from l2_policy_*).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policies for bulk copies: keep the lines (a later kernel of the call
+// re-reads them), or evict them first (read once).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
