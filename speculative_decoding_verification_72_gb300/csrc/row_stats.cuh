@@ -11,9 +11,9 @@
 // and reusing a stage once all consumer warps have released it on its
 // "empty" mbarrier. Warps 1..7 consume: each thread folds its 16-byte
 // vectors of each stage into a running (max, sum 2^((x - max) c)) and
-// remembers the group holding its first maximum. At the end of every row
+// remembers the vector holding its first maximum. At the end of every row
 // piece the consumers resolve the exact argmax from a per-thread shared-memory
-// stash of that group (copied when the maximum rose) and reduce it within the
+// stash of that vector (copied when the maximum rose) and reduce it within the
 // warp; the last warp to finish the piece merges the warps' results and
 // writes one Partial per (CTA, row piece), so no warp waits for another. The
 // decide kernel merges a row's partials.
@@ -44,11 +44,12 @@ constexpr int kK1MaxRegs = (16384 / (kK1WarpsPerScheduler * 32)) / 8 * 8;
 // Vectors one consumer thread folds per stage, in halves of kGroupVecs.
 constexpr int kStageVecs = 8;
 constexpr int kGroupVecs = 4;
+constexpr int kStageHalves = kStageVecs / kGroupVecs;
 constexpr int kK1StageBytes = kK1ConsumerThreads * kStageVecs * 16;   // 28 KB
 constexpr int kK1Stages = 3;
 constexpr int kK1RingBytes = kK1StageBytes * kK1Stages;
-// Per-thread copy of the half-stage that holds its running maximum (16 words).
-constexpr int kK1StashBytes = kK1ConsumerThreads * kGroupVecs * 16;
+// Per-thread copy of the 16-byte vector that holds its running maximum.
+constexpr int kK1StashBytes = kK1ConsumerThreads * 16;
 constexpr int kK1SmemBytes = kK1RingBytes + kK1StashBytes;
 constexpr int kK1MaxCtas = 4096;                      // bound used to size the workspace
 // Piece-result slots: warps of a CTA are at most kK1Stages pieces apart when
@@ -58,7 +59,7 @@ constexpr int kK1RedBufs = 8;
 static_assert(kK1RedBufs >= kK1Stages + 5 && (kK1RedBufs & (kK1RedBufs - 1)) == 0, "piece-result ring");
 static_assert(kK1Consumers <= 8, "the piece merge reduces lanes 0..7");
 constexpr int kK1MinBytesPerCta = 16384;
-static_assert(kStageVecs == 2 * kGroupVecs, "a stage is folded as two groups per thread");
+static_assert(kStageHalves == 1 || kStageHalves == 2, "a stage is folded as one or two groups per thread");
 
 struct RowSet {
   const uint8_t* base;   // first row
@@ -149,11 +150,11 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }
 
 // Where a thread's running maximum first appeared: a scalar element
-// (stage -1, exact index j) or one half of one stage of the current row piece,
-// whose 16 words the thread has copied to its shared-memory stash.
+// (stage -1, exact index j) or one 16-byte vector of one stage of the current
+// row piece, which the thread has copied to its shared-memory stash.
 struct GroupCand {
   int stage;   // stage index within the piece, or -1 for a scalar element
-  int half;    // vectors k = 4*half .. 4*half + 3 of the thread's stage share
+  int vec;     // the vector's k in the thread's stage share (v = ct + k kK1ConsumerThreads)
   int j;       // exact index of a scalar candidate
   int jbase;   // row index of the candidate stage's first element
 };
@@ -239,13 +240,13 @@ constexpr int kStageFullVecs = kStageVecs * kK1ConsumerThreads;
 // all -inf, and the vectors that may hold elements outside [j0, j1)
 // (mask_lo_v, mask_hi_v) get -inf in those elements. The fold then has a
 // single code path for every stage.
-template <int ES>
+template <int ES, int SV = kStageVecs>
 __device__ __forceinline__ void mask_stage(uint4* sv4, int ct, int nvec, int jbase, int j0, int j1,
-                                           int mask_lo_v, int mask_hi_v, int nh = 2) {
+                                           int mask_lo_v, int mask_hi_v, int nh = SV / kGroupVecs) {
   constexpr int N = Elem<ES>::kVec;
   constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;   // -inf in every element
 #pragma unroll
-  for (int k = 0; k < kStageVecs; ++k) {
+  for (int k = 0; k < SV; ++k) {
     const int v = ct + k * kK1ConsumerThreads;
     if (k >= nh * kGroupVecs) {
       // a half the warp does not fold (stage_halves): left as the copy wrote it
@@ -271,6 +272,7 @@ __device__ __forceinline__ void mask_stage(uint4* sv4, int ct, int nvec, int jba
     }
   }
   // These generic-proxy writes precede the next bulk copy into the slot.
+  // (Fencing only in the threads that wrote was measured slower.)
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
@@ -287,15 +289,37 @@ __device__ __forceinline__ void load_half(const uint4* sv4, int ct, int h, uint3
   }
 }
 
-// Record half h of this stage as the thread's candidate: its 16 words go to
-// the thread's stash, vector k at stash[k * kK1ConsumerThreads + ct].
-__device__ __forceinline__ void stash_half(const uint4* sv4, uint4* stash, int ct, int h, int jbase, int sg,
-                                           GroupCand& cand) {
+// Maximum of one 16-byte vector (NaN ignored, as in group_max).
+template <int ES>
+__device__ __forceinline__ float vec_max(const uint4& q) {
+  if constexpr (ES == 2) {
+    const uint32_t t = max_bf16x2(max_bf16x2(q.x, q.y), max_bf16x2(q.z, q.w));
+    return fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xffff0000u));
+  } else {
+    return fmaxf(max3f(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z)), __uint_as_float(q.w));
+  }
+}
+
+// Record where the thread's new maximum gmax first appears in half h of this
+// stage: the lowest vector of the half whose maximum equals gmax (a half's
+// vectors follow in increasing index order), copied to the thread's stash
+// slot stash[ct]; resolve_cand later finds the element inside it.
+template <int ES>
+__device__ __forceinline__ void stash_first(const uint4* sv4, uint4* stash, int ct, int h, float gmax, int jbase,
+                                            int sg, GroupCand& cand) {
+  int kf = h * kGroupVecs + kGroupVecs - 1;
+  uint4 qf = sv4[ct + kf * kK1ConsumerThreads];
 #pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k)
-    stash[k * kK1ConsumerThreads + ct] = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
+  for (int k = kGroupVecs - 2; k >= 0; --k) {
+    const uint4 q = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
+    if (vec_max<ES>(q) == gmax) {
+      kf = h * kGroupVecs + k;
+      qf = q;
+    }
+  }
+  stash[ct] = qf;
   cand.stage = sg;
-  cand.half = h;
+  cand.vec = kf;
   cand.jbase = jbase;
 }
 
@@ -308,9 +332,9 @@ __device__ __forceinline__ void stash_half(const uint4* sv4, uint4* stash, int c
 // halves are re-summed against the new maximum from shared memory only if the
 // stage sum overflowed or the new maximum sat more than 2^20 below the old
 // reference (where flushed small terms could matter). The argmax keeps the
-// half where the maximum first rose: stages and halves arrive in increasing
-// index order, so a strict '>' (and the lower half on a tie) keeps the
-// lowest index.
+// vector where the maximum first rose: stages, halves and vectors arrive in
+// increasing index order, so a strict '>' (and the lower half and vector on
+// a tie) keeps the lowest index.
 template <int ES>
 __device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int ct, int jbase, int sg,
                                            float c, float& m, float& mc, float& s, GroupCand& cand) {
@@ -336,7 +360,7 @@ __device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int c
     }
     m = gmax;
     mc = nmc;
-    stash_half(sv4, stash, ct, ga >= gb ? 0 : 1, jbase, sg, cand);
+    stash_first<ES>(sv4, stash, ct, ga >= gb ? 0 : 1, gmax, jbase, sg, cand);
   } else if (gmax > -INFINITY) {
     s += gsum;
   }
@@ -348,7 +372,7 @@ __device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int c
 // halves are neither masked nor folded. Warp-uniform, so no lane diverges.
 __device__ __forceinline__ int stage_halves(int cw, int nvec) {
   if (cw * 32 >= nvec) return 0;
-  if (cw * 32 + kGroupVecs * kK1ConsumerThreads >= nvec) return 1;
+  if (kStageHalves == 1 || cw * 32 + kGroupVecs * kK1ConsumerThreads >= nvec) return 1;
   return 2;
 }
 
@@ -377,34 +401,27 @@ __device__ __forceinline__ void fold_stage_n(const uint4* sv4, uint4* stash, int
     }
     m = gmax;
     mc = nmc;
-    stash_half(sv4, stash, ct, 0, jbase, sg, cand);
+    stash_first<ES>(sv4, stash, ct, 0, gmax, jbase, sg, cand);
   } else if (gmax > -INFINITY) {
     s += gsum;
   }
 }
 
 // Lowest index in [j0, j1) of the thread's candidate holding the value m,
-// read back from its stash (all four vectors loaded before the search);
-// INT_MAX if m is -inf.
+// read back from its stashed vector; INT_MAX if m is -inf.
 template <int ES>
 __device__ __forceinline__ int resolve_cand(const GroupCand& cand, const uint4* stash, int ct, float m,
                                             int j0, int j1) {
   if (!(m > -INFINITY)) return INT_MAX;
   if (cand.stage < 0) return cand.j;
   constexpr int N = Elem<ES>::kVec;
-  uint4 q[kGroupVecs];
-#pragma unroll
-  for (int k = 0; k < kGroupVecs; ++k) q[k] = stash[k * kK1ConsumerThreads + ct];
+  float f[N];
+  Elem<ES>::unpack(stash[ct], f);
+  const int jv = cand.jbase + (ct + cand.vec * kK1ConsumerThreads) * N;
   int best = INT_MAX;
 #pragma unroll
-  for (int k = kGroupVecs - 1; k >= 0; --k) {
-    float f[N];
-    Elem<ES>::unpack(q[k], f);
-    const int jv = cand.jbase + (ct + (cand.half * kGroupVecs + k) * kK1ConsumerThreads) * N;
-#pragma unroll
-    for (int e = N - 1; e >= 0; --e)
-      if (f[e] == m && jv + e >= j0 && jv + e < j1) best = jv + e;
-  }
+  for (int e = N - 1; e >= 0; --e)
+    if (f[e] == m && jv + e >= j0 && jv + e < j1) best = jv + e;
   return best;
 }
 
@@ -499,7 +516,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
     float m = -INFINITY, mc = ref, s = 0.f;
     GroupCand cand;
     cand.stage = -1;
-    cand.half = 0;
+    cand.vec = 0;
     cand.j = INT_MAX;
     cand.jbase = 0;
     for (int j = p.j0 + ct; j < p.head_end; j += kK1ConsumerThreads)
@@ -520,7 +537,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
           ok = false;   // stop consuming (and releasing); the producer times out too
         } else {
           uint4* sv4 = reinterpret_cast<uint4*>(ring + slot * kK1StageBytes);
-          const int nh = sg == last ? stage_halves(cw, last_nvec) : 2;
+          const int nh = sg == last ? stage_halves(cw, last_nvec) : kStageHalves;
           if ((sg == 0 && first_edge) || (sg == last && last_edge)) {
             const int nvec = sg == last ? last_nvec : kStageFullVecs;
             mask_stage<ES>(sv4, ct, nvec, jbase, p.j0, p.j1, (sg == 0 && first_edge) ? 0 : -1,

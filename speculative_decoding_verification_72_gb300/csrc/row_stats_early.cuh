@@ -159,7 +159,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
       mc = ref;
       s = 0.f;
       cand.stage = -1;
-      cand.half = 0;
+      cand.vec = 0;
       cand.j = INT_MAX;
       cand.jbase = 0;
       jbase = p.j0 - static_cast<int>((p.lo - p.cp_lo) / ES);
@@ -173,12 +173,13 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
       const bool last_hull = p.cp_hi > p.hi;
       const int last_nvec = static_cast<int>((p.cp_hi - p.cp_lo - static_cast<uintptr_t>(last) * kK1StageBytes) / 16u);
       const bool last_edge = last_hull || last_nvec != kStageFullVecs;
+      const int nh = msg == last ? stage_halves(warp - 1, last_nvec) : kStageHalves;
       if ((msg == 0 && first_edge) || (msg == last && last_edge)) {
         const int nvec = msg == last ? last_nvec : kStageFullVecs;
         mask_stage<ES>(sv4, ct, nvec, jbase, p.j0, p.j1, (msg == 0 && first_edge) ? 0 : -1,
-                       (msg == last && last_hull) ? nvec - 1 : -1);
+                       (msg == last && last_hull) ? nvec - 1 : -1, nh);
       }
-      fold_stage<ES>(sv4, stash, ct, jbase, msg, c, m, mc, s, cand);
+      fold_stage_n<ES>(sv4, stash, ct, jbase, msg, c, m, mc, s, cand, nh);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));

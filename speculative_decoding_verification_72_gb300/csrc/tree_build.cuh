@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
     // fp32x2 exponential sums against the reference from before the group),
     // plus the list: a half whose maximum reaches the bound is offered
     // element by element.
-    static_assert(kTbStageVecs == kStageVecs && kTbConsumerThreads == kK1ConsumerThreads, "verify-pass stage layout");
+    static_assert(kTbStageVecs == 2 * kGroupVecs && kTbConsumerThreads == kK1ConsumerThreads, "verify-pass group layout");
+    constexpr int kTbFullVecs = kTbStageVecs * kTbConsumerThreads;
     const int ct = tid - 32;
     float mc = 0.f;   // exponent reference of s
     // the head the copy misses, first: each thread visits its indices in increasing order
@@ -296,8 +297,8 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
         const int nvec = static_cast<int>(min(static_cast<uint32_t>(kTbStageBytes), nbytes - st * kTbStageBytes) / 16);
         const bool first_edge = st == 0 && e0 < 0;
         const bool last_hull = st == nst - 1 && e0 + static_cast<int>(nbytes / ES) > Vp;
-        if (first_edge || last_hull || nvec != kStageFullVecs)
-          mask_stage<ES>(sv4, ct, nvec, jbase, 0, Vp, first_edge ? 0 : -1, last_hull ? nvec - 1 : -1);
+        if (first_edge || last_hull || nvec != kTbFullVecs)
+          mask_stage<ES, kTbStageVecs>(sv4, ct, nvec, jbase, 0, Vp, first_edge ? 0 : -1, last_hull ? nvec - 1 : -1);
         uint32_t w[kGroupWords];
         load_half(sv4, ct, 0, w);
         const float sa = group_sum<ES>(w, c, mc);

@@ -4,8 +4,11 @@ no allocator, or must not allocate once serving has started). It takes no
 workspace; its scratch is the library's static device array.
 
 Checked through the raw C ABI against spec_verify_greedy with a caller
-workspace, on two calls in a row with different inputs (the static array
-keeps the previous call's contents), plus the size limit. This file is
+workspace, on two calls in a row with different inputs. The static array
+keeps the previous call's contents, so the larger call runs first: the
+second, smaller call then reads its partials from an array still holding
+the first call's (more) partials, and must ignore them. Plus the size
+limit. This file is
 collected last so that a run stopping at the first failure has already run
 every other test.
 """
@@ -50,7 +53,9 @@ def test_static_scratch_matches_workspace_path_on_two_calls():
     assert torch.cuda.is_available()
     lib = sv.load_library()
     dev = torch.device("cuda:0")
-    for seed, (B, K, V) in ((11, (32, 5, 128256)), (12, (8, 300, 50257))):
+    # larger call first (2408 rows + one partial per CTA), then a smaller one
+    # (192 rows) over the leftovers
+    for seed, (B, K, V) in ((12, (8, 300, 50257)), (11, (32, 5, 128256))):
         ci = W.greedy_chain(B=B, K=K, V=V, dtype=torch.bfloat16, p_match=0.9, seed=seed, device=dev)
         need = lib.spec_verify_greedy_workspace_size(B, K, V, SV_BF16)
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
