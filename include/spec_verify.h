@@ -363,7 +363,7 @@ sv_status spec_verify_selftest_wait(int32_t* out_status, void* stream);
 
 /* Bytes of the library's static scratch array used by
  * spec_verify_greedy_static (one array per GPU that loads the library). */
-#define SV_STATIC_SCRATCH_BYTES (2u << 20)
+#define SV_STATIC_SCRATCH_BYTES (4u << 20)
 
 /* Greedy chain verification that allocates nothing and takes no workspace.
  * The pages have no counterpart to this entry point: it exists for callers
@@ -374,7 +374,7 @@ sv_status spec_verify_selftest_wait(int32_t* out_status, void* stream);
  * while another component owns the allocator.
  * Arguments, outputs and results are exactly those of spec_verify_greedy; the
  * scratch is a file-scope static device array of SV_STATIC_SCRATCH_BYTES,
- * which holds B*(K+1) <= 126976 rows. Larger requests return
+ * which holds B*(K+1) <= 33353 rows. Larger requests return
  * SV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
  * Set-up: the first call on each device (with that device current) looks up
  * the array's device address once; make that first call before any stream

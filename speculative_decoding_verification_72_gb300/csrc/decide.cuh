@@ -31,6 +31,16 @@
 namespace sv {
 
 constexpr int kK2Threads = 256;
+// Registers sized for three decide blocks per SM, so the draw kernels launched
+// behind a stochastic call's decide kernel (programmatic dependent launch)
+// still find room for their blocks on the SMs that hold a decide block.
+constexpr int kK2MinBlocks = 3;
+// Row-piece slots a decide block stages in shared memory per row set (one
+// merged Partial each); a larger range falls back to per-thread merges.
+constexpr int kStageSlots = 640;
+// Requests whose target plus draft rows number at most kHalfRows are merged
+// by one half-warp per row instead (no staging pass).
+constexpr int kHalfRows = kK2Threads / 16;
 constexpr unsigned long long kEarlyAbortBit = 1ull << 63;   // set in a K1 CTA's byte count
 constexpr int kMaxTreeNodes = 1024;
 
@@ -135,18 +145,21 @@ __device__ __forceinline__ float row_thr(const ChainArgs& a, int b, int i) {
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArgs a) {
+__global__ void __launch_bounds__(kK2Threads, kK2MinBlocks) chain_decide_kernel(const ChainArgs a) {
   __shared__ int s_first;
   __shared__ int s_status;
   __shared__ int s_fin[2];
   __shared__ int s_stop[kMaxStopIds];
+  __shared__ Partial s_tslots[kStageSlots];   // this block's target rows, one merged Partial per slot
+  __shared__ Partial s_dslots[kStageSlots];   // and draft rows
+  __shared__ Partial s_rows[kHalfRows];       // short requests: merged target rows, then draft rows
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int K = a.K, R = a.K + 1;
   const float c = a.c;
   const ChainIn pre = load_chain_in<ES>(a, b, tid < R ? tid : R);
   const float u_final = a.greedy ? 0.f : a.uniforms[static_cast<int64_t>(b) * R + K];
-  FinishPre fpre;
+  __shared__ FinishPre fpre;   // written by thread 0, read by thread 0 in finish_request
   finish_prefetch(a.fin, b, s_stop, fpre);
 
   grid_dep_wait();
@@ -168,6 +181,48 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     __syncthreads();   // every thread has read the previous block's s_first
     if (tid == 0) s_first = INT_MAX;
     __syncthreads();
+    // Merge this block's rows: a half-warp per row for short requests, else
+    // stage the row-piece slots (one merged Partial per slot).
+    const int nr = min(kK2Threads, R - base);
+    const int nd = min(nr, K - base);   // draft rows of positions base .. base + nd - 1
+    const bool with_dft = !a.greedy && a.dft;
+    const bool halves = !a.row_partials && base == 0 && R + (with_dft ? K : 0) <= kHalfRows;
+    SlotRange tsr, dsr;
+    tsr.lo = dsr.lo = 0;
+    tsr.n = dsr.n = 0;
+    bool tstaged = false, dstaged = false;
+    if (halves) {
+      const int h = tid >> 4;
+      const bool draft_row = h >= R;
+      const bool valid = h < R + (with_dft ? K : 0);
+      const int64_t row = draft_row ? static_cast<int64_t>(a.B) * R + static_cast<int64_t>(b) * K + (h - R)
+                                    : static_cast<int64_t>(b) * R + h;
+      float hm, hs;
+      int hi, he;
+      merge_row_half(a.part, row, valid, a.V, a.T, a.G, c, tid & 15, hm, hs, hi, he);
+      if (valid && (tid & 15) == 0) {
+        Partial o;
+        o.m = hm;
+        o.s = hs;
+        o.idx = hi;
+        o.err = he;
+        s_rows[h] = o;
+      }
+      __syncthreads();
+    } else if (!a.row_partials) {
+      tsr = slot_range(static_cast<int64_t>(b) * R + base, static_cast<int64_t>(b) * R + base + nr - 1, a.V, a.T, a.G);
+      tstaged = tsr.n <= kStageSlots;
+      if (!a.greedy && a.dft && nd > 0) {
+        const int64_t d0 = static_cast<int64_t>(a.B) * R + static_cast<int64_t>(b) * K + base;
+        dsr = slot_range(d0, d0 + nd - 1, a.V, a.T, a.G);
+        dstaged = dsr.n <= kStageSlots;
+      }
+      SlotRange none;
+      none.lo = 0;
+      none.n = 0;
+      stage_slots(a.part, tstaged ? tsr : none, s_tslots, dstaged ? dsr : none, s_dslots, c);
+      __syncthreads();
+    }
     const int i = base + tid;
     const bool active = i < R;
     float m = -INFINITY, s = 0.f, lp2row = 0.f, lq2row = 0.f, lp2 = 0.f, acc = 0.f;
@@ -177,19 +232,16 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
     if (active) {
       const int64_t trow = static_cast<int64_t>(b) * R + i;
       const int64_t drow = static_cast<int64_t>(a.B) * R + static_cast<int64_t>(b) * K + i;
-      const bool with_draft = !a.greedy && a.dft && i < K;
-      // both rows' partial loads in flight together
-      RowPartials tp, dp;
-      if (!a.row_partials) row_partials_load(a.part, trow, a.V, a.T, a.G, tp);
-      if (with_draft) row_partials_load(a.part, drow, a.V, a.T, a.G, dp);
-      if (a.row_partials) {
-        const Partial v = a.part[trow];
+      if (a.row_partials || halves) {
+        const Partial v = halves ? s_rows[i] : a.part[trow];
         m = v.m;
         s = v.s;
         idx = v.idx;
         err = v.err;
+      } else if (tstaged) {
+        merge_row_staged(s_tslots, tsr, trow, a.V, a.T, a.G, c, m, s, idx, err);
       } else {
-        row_partials_merge(a.part, trow, tp, c, m, s, idx, err);
+        merge_row_serial(a.part, trow, a.V, a.T, a.G, c, m, s, idx, err);
       }
       lp2row = m * c + log2f(s);
       if (!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) st |= SV_STATUS_NONFINITE_ROW;
@@ -202,7 +254,17 @@ __global__ void __launch_bounds__(kK2Threads) chain_decide_kernel(const ChainArg
           if (a.dft) {
             float md, sd;
             int id, ed;
-            row_partials_merge(a.part, drow, dp, c, md, sd, id, ed);
+            if (halves) {
+              const Partial v = s_rows[R + i];
+              md = v.m;
+              sd = v.s;
+              id = v.idx;
+              ed = v.err;
+            } else if (dstaged) {
+              merge_row_staged(s_dslots, dsr, drow, a.V, a.T, a.G, c, md, sd, id, ed);
+            } else {
+              merge_row_serial(a.part, drow, a.V, a.T, a.G, c, md, sd, id, ed);
+            }
             lq2row = md * c + log2f(sd);
             if (!(fabsf(md) <= FLT_MAX) || !(sd > 0.f && sd <= FLT_MAX)) st |= SV_STATUS_NONFINITE_ROW;
             if (ed) st |= SV_STATUS_TIMEOUT;
@@ -367,6 +429,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   __shared__ int s_status;
   __shared__ int s_n, s_fin[2];
   __shared__ int s_stop[kMaxStopIds];
+  __shared__ Partial s_slots[kStageSlots];  // the request's row-piece slots, one merged Partial each
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -393,7 +456,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
     sm_first[n] = -1;
   }
   __syncthreads();
-  FinishPre fpre;
+  __shared__ FinishPre fpre;   // written by thread 0, read by thread 0 in finish_request
   finish_prefetch(a.fin, b, s_stop, fpre);
   if (tid == 0) {
     for (int n = N - 1; n >= 1; --n) {   // reverse insertion: lists in increasing index
@@ -408,10 +471,20 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
   grid_dep_wait();
   grid_dep_launch();
 
+  const SlotRange sr = slot_range(static_cast<int64_t>(b) * N, static_cast<int64_t>(b) * N + N - 1, a.V, a.T, a.G);
+  const bool staged = sr.n <= kStageSlots;
+  if (staged) {
+    SlotRange none;
+    none.lo = 0;
+    none.n = 0;
+    stage_slots(a.part, sr, s_slots, none, nullptr, c);
+    __syncthreads();
+  }
   for (int n = tid; n < N; n += kK2Threads) {
     float m, s;
     int idx, err;
-    merge_row(a.part, static_cast<int64_t>(b) * N + n, a.V, a.T, a.G, c, m, s, idx, err);
+    if (staged) merge_row_staged(s_slots, sr, static_cast<int64_t>(b) * N + n, a.V, a.T, a.G, c, m, s, idx, err);
+    else merge_row_serial(a.part, static_cast<int64_t>(b) * N + n, a.V, a.T, a.G, c, m, s, idx, err);
     sm_m[n] = m;
     sm_l2[n] = m * c + log2f(s);
     sm_am[n] = idx;

@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kK3PickThreads) draw_pick_kernel(const DrawArg
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
-  FinishPre fpre;
+  __shared__ FinishPre fpre;   // written by thread 0, read by thread 0 in finish_request
   if (a.fin_here) finish_prefetch(a.fin, b, s_stop_pre, fpre);
   grid_dep_wait();
   grid_dep_launch();

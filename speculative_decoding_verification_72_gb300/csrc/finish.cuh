@@ -31,8 +31,9 @@ struct FinishArgs {
 
 // The finish step's inputs for request b, read at kernel start (before the
 // dependency wait: they are call inputs, and only this step writes the
-// counters, once per call at its end). Stop ids go to shared memory; the cap
-// and the counters to thread 0's registers.
+// counters, once per call at its end). Stop ids go to shared memory; thread 0
+// writes the cap and the counters into `pre`, which the kernels keep in
+// shared memory (so no thread holds them in registers for the whole kernel).
 struct FinishPre {
   int cap;            // INT_MAX when there is no cap
   long long c[4];

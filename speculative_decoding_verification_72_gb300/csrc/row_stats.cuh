@@ -13,10 +13,9 @@
 // vectors of each stage into a running (max, sum 2^((x - max) c)) and
 // remembers the vector holding its first maximum. At the end of every row
 // piece the consumers resolve the exact argmax from a per-thread shared-memory
-// stash of that vector (copied when the maximum rose) and reduce it within the
-// warp; the last warp to finish the piece merges the warps' results and
-// writes one Partial per (CTA, row piece), so no warp waits for another. The
-// decide kernel merges a row's partials.
+// stash of that vector (copied when the maximum rose), reduce it within the
+// warp and write one Partial per (warp, row piece), so no warp waits for,
+// counts or merges another. The decide kernel merges a row's partials.
 //
 // Copies cover the 16-byte-aligned hull of each row piece when it lies inside
 // the logit buffer, and elements outside the piece are masked in the first
@@ -52,9 +51,10 @@ constexpr int kK1RingBytes = kK1StageBytes * kK1Stages;
 constexpr int kK1StashBytes = kK1ConsumerThreads * 16;
 constexpr int kK1SmemBytes = kK1RingBytes + kK1StashBytes;
 constexpr int kK1MaxCtas = 4096;                      // bound used to size the workspace
-// Piece-result slots: warps of a CTA are at most kK1Stages pieces apart when
-// every piece has a copied stage, plus one piece per buffer edge handled by
-// scalar loads alone (two per row set, two row sets).
+// Piece-result slots of the early-exit row pass (row_stats_early.cuh), which
+// merges a row's warp results in the CTA: warps are at most kK1Stages pieces
+// apart when every piece has a copied stage, plus one piece per buffer edge
+// handled by scalar loads alone (two per row set, two row sets).
 constexpr int kK1RedBufs = 8;
 static_assert(kK1RedBufs >= kK1Stages + 5 && (kK1RedBufs & (kK1RedBufs - 1)) == 0, "piece-result ring");
 static_assert(kK1Consumers <= 8, "the piece merge reduces lanes 0..7");
@@ -76,7 +76,7 @@ struct RowStatsArgs {
   int64_t T;           // (set0.rows + set1.rows) * V
   int32_t G;           // CTAs
   float c;             // log2(e) / T
-  Partial* partials;   // [rows + G]: slot row + cta, one per (CTA, row piece)
+  Partial* partials;   // [(rows + G) * kK1Consumers]: slot (row + cta) * kK1Consumers + warp
   // L2 retention for a later re-read (stochastic chains, whose draw re-reads
   // the rows of the first rejected position): rows at chain position
   // < keep_pos (position = row mod rows_per_req0 in set0, mod rows_per_req1 in
@@ -430,8 +430,6 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full_bar[kK1Stages];
   __shared__ __align__(8) uint64_t empty_bar[kK1Stages];
-  __shared__ Partial red[kK1RedBufs][kK1Consumers];
-  __shared__ int red_cnt[kK1RedBufs];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -442,7 +440,6 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   const int j00 = static_cast<int>(E0 - static_cast<int64_t>(row0) * a.V);
 
   // Shared-memory setup overlaps the previous kernel's tail.
-  if (tid < kK1RedBufs) red_cnt[tid] = 0;
   if (tid == 0) {
     for (int i = 0; i < kK1Stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
@@ -507,11 +504,11 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   const int ct = tid - 32;
   const int cw = warp - 1;
   const float c = a.c;
-  int slot = 0, npiece = 0;
+  int slot = 0;
   uint32_t phase = 0;
   bool ok = true;
   float ref = 0.f;   // exponent reference a piece starts from (log2 domain)
-  for (int row = row0, j0 = j00; E0 < E1; ++npiece, ++row, j0 = 0) {
+  for (int row = row0, j0 = j00; E0 < E1; ++row, j0 = 0) {
     const Piece p = make_piece<ES>(a, row, j0, E1);
     float m = -INFINITY, mc = ref, s = 0.f;
     GroupCand cand;
@@ -566,103 +563,166 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
 
-    // CTA: each warp leaves its result in the piece's slot of a small ring
-    // and counts itself in; the last warp to arrive merges the slot (lanes
-    // 0..7, a fixed shuffle tree, so the result does not depend on which warp
-    // was last) and writes the Partial. No warp waits for another here.
-    const int buf = npiece & (kK1RedBufs - 1);
-    int merger = 0;
+    // One partial per warp and piece, at slot (row + g) * kK1Consumers + cw:
+    // the decide kernel merges a row's partials, so no warp waits for,
+    // counts or merges another warp's result here.
     if (lane == 0) {
-      Partial mine;
-      mine.m = wm;
-      mine.s = ws;
-      mine.idx = widx;
-      mine.err = ok ? 0 : 1;
-      red[buf][cw] = mine;
-      __threadfence_block();
-      merger = atomicAdd(&red_cnt[buf], 1) == kK1Consumers - 1;
-    }
-    if (__shfl_sync(0xffffffffu, merger, 0)) {
-      __threadfence_block();
-      float rm = -INFINITY, rs = 0.f;
-      int ri = INT_MAX, re = 0;
-      if (lane < kK1Consumers) {
-        const Partial v = red[buf][lane];
-        rm = v.m;
-        rs = v.s;
-        ri = v.idx;
-        re = v.err;
-      }
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, rm, o);
-        const float os = __shfl_xor_sync(0xffffffffu, rs, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, ri, o);
-        re |= __shfl_xor_sync(0xffffffffu, re, o);
-        merge_stats(rm, rs, ri, om, os, oi, c);
-      }
-      if (lane == 0) {
-        atomicExch(&red_cnt[buf], 0);
-        Partial out;
-        out.m = rm;
-        out.s = rs;
-        out.idx = ri;
-        out.err = re;
-        a.partials[static_cast<int64_t>(p.row) + g] = out;
-      }
+      Partial out;
+      out.m = wm;
+      out.s = ws;
+      out.idx = widx;
+      out.err = ok ? 0 : 1;
+      a.partials[(static_cast<int64_t>(p.row) + g) * kK1Consumers + cw] = out;
     }
     if (static_cast<int64_t>(row) * a.V + p.j1 >= E1) break;
   }
 }
 
-// One row's partials (one per CTA whose range meets the row): the first four
-// are loaded by row_partials_load (so several rows' loads can be in flight
-// together), then row_partials_merge folds them in CTA order, loading any
-// further ones itself.
-struct RowPartials {
-  Partial v[4];
-  int g_lo, g_hi;
-};
-
-__device__ __forceinline__ void row_partials_load(const Partial* __restrict__ parts, int64_t row, int V, int64_t T,
-                                                  int G, RowPartials& rp) {
-  const int64_t e0 = row * V;
-  rp.g_lo = cta_of(e0, T, G);
-  rp.g_hi = cta_of(e0 + V - 1, T, G);
+// One row's partials: kK1Consumers per CTA whose range meets the row, at
+// slots (row + g) * kK1Consumers + w, contiguous for one CTA. A CTA's
+// partials are folded as a pairwise tree, and the CTAs in increasing order;
+// the order is fixed, so the result is deterministic.
+__device__ __forceinline__ void load_cta_partials(const Partial* __restrict__ parts, int64_t row, int g,
+                                                  Partial (&v)[kK1Consumers]) {
+  const Partial* p = parts + (row + g) * kK1Consumers;
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    if (rp.g_lo + k <= rp.g_hi) rp.v[k] = parts[row + rp.g_lo + k];
+  for (int w = 0; w < kK1Consumers; ++w) v[w] = p[w];
 }
 
-__device__ __forceinline__ void row_partials_merge(const Partial* __restrict__ parts, int64_t row,
-                                                   const RowPartials& rp, float c, float& m, float& s, int& idx,
-                                                   int& err) {
+// Pairwise merge of one CTA's warp partials (w, w + 1), (w, w + 2), ...
+__device__ __forceinline__ void merge_cta_partials(const Partial (&v)[kK1Consumers], float c, float& m, float& s,
+                                                   int& idx, int& err) {
+  float tm[kK1Consumers], ts[kK1Consumers];
+  int ti[kK1Consumers];
+  err = 0;
+#pragma unroll
+  for (int w = 0; w < kK1Consumers; ++w) {
+    tm[w] = v[w].m;
+    ts[w] = v[w].s;
+    ti[w] = v[w].idx;
+    err |= v[w].err;
+  }
+#pragma unroll
+  for (int step = 1; step < kK1Consumers; step <<= 1)
+#pragma unroll
+    for (int w = 0; w + step < kK1Consumers; w += 2 * step) merge_stats(tm[w], ts[w], ti[w], tm[w + step], ts[w + step], ti[w + step], c);
+  m = tm[0];
+  s = ts[0];
+  idx = ti[0];
+}
+
+// Block-cooperative staging. The slots (row + g) of consecutive rows are
+// consecutive (a CTA's range continues into the next row), so rows
+// [r0, r1] own the dense slot range [r0 + g_lo(r0), r1 + g_hi(r1)]. Each
+// thread of the block merges the kK1Consumers warp partials of one slot into
+// one Partial in shared memory; a row's thread then merges its few slots with
+// merge_row_staged. Same merge order as merge_row_serial, so the results
+// are identical.
+struct SlotRange {
+  int64_t lo;   // first slot
+  int n;        // slots
+};
+
+__device__ __forceinline__ SlotRange slot_range(int64_t r0, int64_t r1, int V, int64_t T, int G) {
+  SlotRange sr;
+  sr.lo = r0 + cta_of(r0 * V, T, G);
+  const int64_t hi = r1 + cta_of(r1 * V + V - 1, T, G);
+  sr.n = static_cast<int>(hi - sr.lo + 1);
+  return sr;
+}
+
+// Stages two slot ranges in one pass (a second range of n = 0 is skipped), so
+// the loads of both are in flight together.
+__device__ __forceinline__ void stage_slots(const Partial* __restrict__ parts, const SlotRange& sa, Partial* staged_a,
+                                            const SlotRange& sb, Partial* staged_b, float c) {
+  const int n = sa.n + sb.n;
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const bool first = q < sa.n;
+    const int k = first ? q : q - sa.n;
+    Partial v[kK1Consumers];
+    const Partial* p = parts + ((first ? sa.lo : sb.lo) + k) * kK1Consumers;
+#pragma unroll
+    for (int w = 0; w < kK1Consumers; ++w) v[w] = p[w];
+    Partial o;
+    merge_cta_partials(v, c, o.m, o.s, o.idx, o.err);
+    (first ? staged_a : staged_b)[k] = o;
+  }
+}
+
+__device__ __forceinline__ void merge_row_staged(const Partial* staged, const SlotRange& sr, int64_t row, int V,
+                                                 int64_t T, int G, float c, float& m, float& s, int& idx, int& err) {
+  const int64_t e0 = row * V;
+  const int q0 = static_cast<int>(row + cta_of(e0, T, G) - sr.lo);
+  const int q1 = static_cast<int>(row + cta_of(e0 + V - 1, T, G) - sr.lo);
   m = -INFINITY;
   s = 0.f;
   idx = INT_MAX;
   err = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (rp.g_lo + k <= rp.g_hi) {
-      merge_stats(m, s, idx, rp.v[k].m, rp.v[k].s, rp.v[k].idx, c);
-      err |= rp.v[k].err;
-    }
-  }
-  for (int g = rp.g_lo + 4; g <= rp.g_hi; ++g) {
-    const Partial w = parts[row + g];
-    merge_stats(m, s, idx, w.m, w.s, w.idx, c);
-    err |= w.err;
+  for (int q = q0; q <= q1; ++q) {
+    const Partial v = staged[q];
+    merge_stats(m, s, idx, v.m, v.s, v.idx, c);
+    err |= v.err;
   }
   if (m == -INFINITY) idx = 0;   // every element is -inf: the lowest index attains the max
 }
 
-// Merge one row's partials.
-__device__ __forceinline__ void merge_row(const Partial* __restrict__ parts, int64_t row, int V,
-                                          int64_t T, int G, float c, float& m, float& s, int& idx,
-                                          int& err) {
-  RowPartials rp;
-  row_partials_load(parts, row, V, T, G, rp);
-  row_partials_merge(parts, row, rp, c, m, s, idx, err);
+// One row's statistics merged by a half-warp (lane16 = lane & 15): lane l
+// takes partials l, l + 16, ... of the row's (g_hi - g_lo + 1) * kK1Consumers
+// (in slot order), merges them, and four xor-shuffle levels within the half
+// merge the lanes, so every lane of the half ends with the row's statistics.
+// All 32 lanes of the warp must call it (valid = false: a half with no row,
+// which contributes nothing); merge_stats is symmetric, so both partners of a
+// shuffle compute the same value and the result is deterministic.
+__device__ __forceinline__ void merge_row_half(const Partial* __restrict__ parts, int64_t row, bool valid, int V,
+                                               int64_t T, int G, float c, int lane16, float& m, float& s, int& idx,
+                                               int& err) {
+  m = -INFINITY;
+  s = 0.f;
+  idx = INT_MAX;
+  err = 0;
+  if (valid) {
+    const int64_t e0 = row * V;
+    const int g_lo = cta_of(e0, T, G), g_hi = cta_of(e0 + V - 1, T, G);
+    const int n = (g_hi - g_lo + 1) * kK1Consumers;
+    const Partial* p = parts + (row + g_lo) * kK1Consumers;
+    for (int k = lane16; k < n; k += 16) {
+      const Partial v = p[k];
+      merge_stats(m, s, idx, v.m, v.s, v.idx, c);
+      err |= v.err;
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, s, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    err |= __shfl_xor_sync(0xffffffffu, err, o);
+    merge_stats(m, s, idx, om, os, oi, c);
+  }
+  if (m == -INFINITY) idx = 0;   // every element is -inf: the lowest index attains the max
 }
+
+// Merge one row's partials CTA by CTA (few registers). The decide kernels
+// use it when a block's slots exceed their staging area; the mu pass always.
+__device__ __noinline__ void merge_row_serial(const Partial* __restrict__ parts, int64_t row, int V, int64_t T,
+                                              int G, float c, float& m, float& s, int& idx, int& err) {
+  const int64_t e0 = row * V;
+  const int g_lo = cta_of(e0, T, G), g_hi = cta_of(e0 + V - 1, T, G);
+  m = -INFINITY;
+  s = 0.f;
+  idx = INT_MAX;
+  err = 0;
+  for (int g = g_lo; g <= g_hi; ++g) {
+    Partial v[kK1Consumers];
+    load_cta_partials(parts, row, g, v);
+    float cm, cs;
+    int ci, ce;
+    merge_cta_partials(v, c, cm, cs, ci, ce);
+    merge_stats(m, s, idx, cm, cs, ci, c);
+    err |= ce;
+  }
+  if (m == -INFINITY) idx = 0;   // every element is -inf: the lowest index attains the max
+}
+
 
 }  // namespace sv

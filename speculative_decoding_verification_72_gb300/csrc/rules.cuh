@@ -218,9 +218,9 @@ template <int ES>
 __device__ __forceinline__ void row_lse2(const MuArgs& a, int b, int j, float& lp2, float& lq2) {
   float m, s;
   int idx, err;
-  merge_row(a.part, static_cast<int64_t>(b) * (a.K + 1) + j, a.V, a.T, a.G, a.c, m, s, idx, err);
+  merge_row_serial(a.part, static_cast<int64_t>(b) * (a.K + 1) + j, a.V, a.T, a.G, a.c, m, s, idx, err);
   lp2 = m * a.c + log2f(s);
-  merge_row(a.part, static_cast<int64_t>(a.B) * (a.K + 1) + static_cast<int64_t>(b) * a.K + j, a.V, a.T,
+  merge_row_serial(a.part, static_cast<int64_t>(a.B) * (a.K + 1) + static_cast<int64_t>(b) * a.K + j, a.V, a.T,
             a.G, a.c, m, s, idx, err);
   lq2 = m * a.c + log2f(s);
 }
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kMuThreads) mu_pass_kernel(const MuArgs a) {
   __shared__ int s_last, s_fin[2];
   __shared__ int s_stop[kMaxStopIds];
   const int per_req = a.K * a.P;
-  FinishPre fpre;
+  __shared__ FinishPre fpre;   // written by thread 0, read by thread 0 in finish_request
   finish_prefetch(a.fin, blockIdx.x / per_req, s_stop, fpre);
   grid_dep_wait();
   grid_dep_launch();

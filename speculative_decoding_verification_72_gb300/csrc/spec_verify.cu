@@ -71,7 +71,8 @@ bool make_plan(int64_t rows_t, int64_t rows_d, int64_t B, int64_t V, int es, boo
   pl->excl_stride = static_cast<int32_t>(excl_stride < 1 ? 1 : excl_stride);
   size_t off = 0;
   pl->off_part = off;
-  off += align_up(static_cast<size_t>(pl->rows_total + kK1MaxCtas) * sizeof(Partial), kAlign);
+  // one partial per (row piece, consumer warp): (rows + G) * kK1Consumers slots
+  off += align_up(static_cast<size_t>(pl->rows_total + kK1MaxCtas) * kK1Consumers * sizeof(Partial), kAlign);
   if (draw) {
     pl->off_draw = off;
     off += align_up(static_cast<size_t>(B) * sizeof(DrawDesc), kAlign);

@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 SV_BF16 = 1
 SV_ERR_WORKSPACE_TOO_SMALL = 3
 ATOL = 1e-4
-MAX_STATIC_ROWS = 126976          # rows that fit the 2 MiB static scratch array
+MAX_STATIC_ROWS = 33353           # rows that fit the 4 MiB static scratch array
 P = ctypes.c_void_p
 
 
