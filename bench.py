@@ -92,8 +92,11 @@ CONTRACT_CONFIGS = ("long_chain", "llama_greedy", "llama_greedy_b8", "llama_gree
                     "eagle_tree_greedy", "eagle_tree_power", "eagle_tree_relaxed")
 NEXT_CONFIGS = ("llama_greedy_finish", "long_chain_early", "eagle_tree_build", "kv_compact")
 DEFAULT_CONFIG = "long_chain"
-# K1 + K2, plus the draw's two kernels (chunk sums, pick) when a call samples
+# row pass + decide, plus the draw's two kernels (chunk sums, pick) when a
+# call samples; a stochastic chain of at most 16 rows with draft logits and
+# the exact rule decides inside the chunk-sum kernel (no decide kernel)
 KERNELS_PER_CALL = {"greedy": 2, "sample": 4, "tree": 2, "tree_build": 2, "kv_compact": 1}
+FUSED_MAX_ROWS = 16
 FALLBACK_HBM_GBS = 6800.0
 MIN_REPS = 5                 # timed repetitions per workload (median reported)
 MAX_REPS = 2000
@@ -247,6 +250,8 @@ def algorithmic_bytes(cfg):
 
 
 def launches_per_call(cfg):
+    if cfg["kind"] == "sample" and cfg["K"] + 1 <= FUSED_MAX_ROWS:
+        return 3
     return KERNELS_PER_CALL[cfg["kind"]] + (2 if cfg["kind"] == "tree" and cfg.get("T") else 0)
 
 
@@ -732,6 +737,8 @@ def kernel_desc(cfg):
         d = "one build call: row_topk_kernel (all draft logit bytes) + tree_select_kernel"
     elif cfg["kind"] == "kv_compact":
         d = "one compaction call: kv_compact_kernel (path rows read + written)"
+    elif launches_per_call(cfg) == 3:
+        d = "one verify call: row_stats_kernel (all logit bytes) + draw kernels (chunk sums with the decision, pick)"
     else:
         d = "one verify call: row_stats_kernel (all logit bytes) + decide kernel"
     return d + (" + draw kernels (chunk sums, pick)" if launches_per_call(cfg) == 4 else "")

@@ -32,6 +32,7 @@
 #pragma once
 
 #include "finish.cuh"
+#include "row_stats.cuh"
 #include "sv_common.cuh"
 
 namespace sv {
@@ -49,6 +50,9 @@ constexpr int kK3LocalExcl = 64;    // exclusions cached per request
 constexpr int kK3MaxChunks = 256;   // chunk sums the pick kernel stages in shared memory
 constexpr int kK3PickThreads = 1024;
 constexpr int kStatusWaitErr = SV_STATUS_TIMEOUT;
+// Fused decision: chains of at most kFusedMaxRows positions (K + 1).
+constexpr int kFusedMaxRows = 16;
+constexpr int kFusedRowsPerReq = 2 * kFusedMaxRows - 1;   // target rows 0..K, draft rows 0..K-1
 
 template <int ES>
 constexpr int kK3ChunkElems = kK3ChunkBytes / ES;
@@ -79,6 +83,21 @@ struct DrawArgs {
   int32_t* out_status;
   FinishArgs fin;        // applied by the pick kernel when fin_here
   int32_t fin_here;
+  // Fused decision (stochastic chain, draft logits, exact rule, K + 1 <=
+  // kFusedMaxRows): draw_sum_kernel decides its own requests from the row
+  // pass's partials (the same half-warp merges and acceptance tests as the
+  // decide kernel) instead of reading a decide kernel's descriptors. The CTA
+  // whose range holds a request's first chunk writes that request's
+  // accepted outputs, count, status and draw descriptor (for the pick).
+  int32_t fused;
+  const Partial* k1_part;
+  int64_t k1_T;
+  int32_t k1_G;
+  int32_t K;
+  const int32_t* drafts;     // [B, K]
+  const float* uniforms;     // [B, K + 1]
+  int32_t* out_num;          // [B]
+  DrawDesc* draws_out;       // [B]: the same array as draws
 };
 
 // Weights of one element from its logits: p = 2^(x c - lp2), w = relu(p - q)
@@ -306,6 +325,100 @@ __device__ __forceinline__ void sum_stage(const StageDesc& ts, const StageDesc& 
   }
 }
 
+// Fused decision for the requests b_first .. b_first + nreq - 1 of a draw-sum
+// CTA (stochastic chain, draft logits, exact rule; spec-decode README, "How
+// it works"): accept draft i with probability min(1, p(d_i)/q(d_i)), stop at
+// the first rejection n (residual draw from normalize(relu(p - q)) at row n),
+// else a bonus draw from p at row K. The same arithmetic, merge order and
+// status bits as the decide kernel's stochastic path, so the outputs are
+// identical. Block-cooperative: every thread calls it.
+template <int ES>
+__device__ __forceinline__ void fused_decide(const DrawArgs& a, int b_first, int nreq, int64_t i0, int64_t i1,
+                                             int tok, bool bad, float x, float y, float u, float uK, Partial* s_rs,
+                                             DrawDesc* s_desc) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = a.K, R = K + 1, per = 2 * K + 1;
+  const float c = a.c;
+  // Row statistics, one half-warp per row (the decide kernel's merge).
+  const int rows_all = nreq * per;
+  for (int q0 = 0; q0 < rows_all; q0 += kK3Threads / 16) {
+    const int q = q0 + (tid >> 4);
+    const bool valid = q < rows_all;
+    const int r = valid ? q / per : 0, j = valid ? q - r * per : 0;
+    const int64_t bq = b_first + r;
+    const int64_t row = j <= K ? bq * R + j : static_cast<int64_t>(a.B) * R + bq * K + (j - K - 1);
+    float m, s;
+    int idx, err;
+    merge_row_half(a.k1_part, row, valid, a.V, a.k1_T, a.k1_G, c, tid & 15, m, s, idx, err);
+    if (valid && (tid & 15) == 0) {
+      Partial o;
+      o.m = m;
+      o.s = s;
+      o.idx = idx;
+      o.err = err;
+      s_rs[q] = o;
+    }
+  }
+  __syncthreads();
+  if (warp >= nreq) return;
+  const int b = b_first + warp;
+  const Partial tr = s_rs[warp * per + min(lane, K)];
+  const float lp2row = tr.m * c + log2f(tr.s);
+  int st = 0;
+  if (!(fabsf(tr.m) <= FLT_MAX) || !(tr.s > 0.f && tr.s <= FLT_MAX)) st |= SV_STATUS_NONFINITE_ROW;
+  if (tr.err) st |= SV_STATUS_TIMEOUT;
+  float lq2row = 0.f, lp2 = 0.f, acc = 0.f;
+  bool zero = false, rej = false;
+  if (lane < K) {
+    const Partial dr = s_rs[warp * per + K + 1 + lane];
+    lq2row = dr.m * c + log2f(dr.s);
+    if (!(fabsf(dr.m) <= FLT_MAX) || !(dr.s > 0.f && dr.s <= FLT_MAX)) st |= SV_STATUS_NONFINITE_ROW;
+    if (dr.err) st |= SV_STATUS_TIMEOUT;
+    if (!bad) {
+      lp2 = x * c - lp2row;   // log2 p(t)
+      const float lq2 = y * c - lq2row;
+      if (lp2 == -INFINITY && lq2 == -INFINITY) zero = true;
+      else acc = ex2(fminf(0.f, lp2 - lq2));   // min(1, p/q)
+    }
+    rej = bad || zero || !(u < acc);
+  }
+  const unsigned rm = __ballot_sync(0xffffffffu, lane < K && rej);
+  const int n = rm ? __ffs(rm) - 1 : K;
+  int stat = lane <= n ? st : 0;
+  if (lane == n && n < K) {
+    if (bad) stat |= SV_STATUS_BAD_TOKEN;
+    if (zero) stat |= SV_STATUS_ZERO_MASS;
+  }
+  stat = __reduce_or_sync(0xffffffffu, stat);
+  DrawDesc d;
+  d.type = n == K ? kDrawP : kDrawResid;
+  d.t_row = b * R + n;
+  d.d_row = b * K + n;
+  d.pos = n;
+  d.u = uK;
+  d.lp2 = __shfl_sync(0xffffffffu, lp2row, n);
+  d.lq2 = n < K ? __shfl_sync(0xffffffffu, lq2row, n) : 0.f;
+  d.scale = 1.f;
+  d.n_excl = 0;
+  d.pad0 = d.pad1 = d.pad2 = 0;
+  if (lane == 0) s_desc[warp] = d;
+  // The CTA holding the request's first chunk writes its outputs once.
+  const int64_t first_item = static_cast<int64_t>(b) * a.P;
+  if (first_item >= i0 && first_item < i1) {
+    if (lane == 0) {
+      a.draws_out[b] = d;
+      a.out_num[b] = n;
+      if (a.out_status) a.out_status[b] = stat;
+    }
+    if (lane < R && lane != n) {   // the pick kernel writes position n
+      const int64_t o = static_cast<int64_t>(b) * a.out_cols + lane;
+      a.out_tokens[o] = lane < n ? tok : -1;
+      if (a.out_logprob) a.out_logprob[o] = lane < n ? lp2 * kLn2 : 0.f;
+      if (a.out_mu) a.out_mu[o] = lane < n ? ex2(lp2) : 0.f;
+    }
+  }
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(const DrawArgs a) {
   extern __shared__ __align__(128) uint8_t ring[];
@@ -317,6 +430,7 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
   __shared__ DrawDesc s_desc[kK3Req];
   __shared__ int s_ex[kK3Req][kK3LocalExcl];
   __shared__ int s_err;
+  __shared__ Partial s_rs[kK3Req * kFusedRowsPerReq];   // fused decision: row statistics
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -324,6 +438,28 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
   const int64_t i0 = n_items * blockIdx.x / a.G;
   const int64_t i1 = n_items * (blockIdx.x + 1) / a.G;
   const int b_first = static_cast<int>(i0 / a.P);
+
+  // Fused decision: warp w decides request b_first + w, lane i position i.
+  // Its call inputs (draft tokens, uniforms, the draft tokens' logits) are
+  // read before the dependency wait.
+  const int R = a.K + 1;
+  const int nreq_f = a.fused ? min(kK3Req, static_cast<int>((i1 - 1) / a.P) - b_first + 1) : 0;
+  int f_tok = -1;
+  bool f_bad = false;
+  float f_x = -INFINITY, f_y = -INFINITY, f_u = 0.f, f_uK = 0.f;
+  if (warp < nreq_f) {
+    const int64_t bq = b_first + warp;
+    f_uK = a.uniforms[bq * R + a.K];
+    if (lane < a.K) {
+      f_tok = a.drafts[bq * a.K + lane];
+      f_bad = f_tok < 0 || f_tok >= a.V;
+      f_u = a.uniforms[bq * R + lane];
+      if (!f_bad) {
+        f_x = Elem<ES>::load(a.tgt + (bq * R + lane) * a.tgt_stride, f_tok);
+        f_y = Elem<ES>::load(a.dft + (bq * a.K + lane) * a.dft_stride, f_tok);
+      }
+    }
+  }
 
   // Shared-memory setup overlaps the decide kernel's tail.
   if (tid < kK3Stages) red_cnt[tid] = 0;
@@ -335,15 +471,19 @@ __global__ void __launch_bounds__(kK3Threads, kK3CtasPerSm) draw_sum_kernel(cons
     }
     fence_barrier_init();
   }
-  grid_dep_wait();   // the draw descriptors come from the decide kernel
+  grid_dep_wait();   // the draw descriptors come from the decide kernel (or the row pass, fused)
   grid_dep_launch();
 
-  // Descriptors and exclusion lists of the first kK3Req requests of the range.
-  const int nreq = min(kK3Req, static_cast<int>((i1 - 1) / a.P) - b_first + 1);
-  if (tid < nreq) s_desc[tid] = a.draws[b_first + tid];
-  for (int x = tid; x < nreq * kK3LocalExcl; x += kK3Threads) {
-    const int r = x / kK3LocalExcl, e = x - r * kK3LocalExcl;
-    if (e < a.excl_stride) s_ex[r][e] = a.excl[static_cast<int64_t>(b_first + r) * a.excl_stride + e];
+  if (a.fused) {
+    fused_decide<ES>(a, b_first, nreq_f, i0, i1, f_tok, f_bad, f_x, f_y, f_u, f_uK, s_rs, s_desc);
+  } else {
+    // Descriptors and exclusion lists of the first kK3Req requests of the range.
+    const int nreq = min(kK3Req, static_cast<int>((i1 - 1) / a.P) - b_first + 1);
+    if (tid < nreq) s_desc[tid] = a.draws[b_first + tid];
+    for (int x = tid; x < nreq * kK3LocalExcl; x += kK3Threads) {
+      const int r = x / kK3LocalExcl, e = x - r * kK3LocalExcl;
+      if (e < a.excl_stride) s_ex[r][e] = a.excl[static_cast<int64_t>(b_first + r) * a.excl_stride + e];
+    }
   }
   __syncthreads();
 

@@ -575,6 +575,14 @@ sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_
   }
   const bool mu_pass = draft_logits && a.rule.rule != SV_RULE_EXACT && K > 0;
   a.mu_counters = mu_pass ? reinterpret_cast<uint32_t*>(w + pl.off_mucnt) : nullptr;
+  DrawArgs d = draw_args(pl, target_logits, row_stride, rows_t, draft_logits, draft_logits ? draft_row_stride : 0,
+                         rows_d, B, V, es, c, workspace, K + 1, out_tokens, out_logprob, out_mu);
+  // The exact rule with draft logits and short chains decides inside the
+  // draw's chunk-sum kernel (no decide kernel), when no chunk-sum CTA's item
+  // range spans more requests than it decides.
+  const int64_t items_per_cta = (static_cast<int64_t>(B) * pl.P + d.G - 1) / d.G;
+  const bool fuse = draft_logits && a.rule.rule == SV_RULE_EXACT && a.rule.top_k == 0 && K + 1 <= kFusedMaxRows &&
+                    (items_per_cta + pl.P - 1) / pl.P + 1 <= kK3Req;
   a.out_tokens = out_tokens;
   a.out_num = out_num_accepted;
   a.out_logprob = out_logprob;
@@ -583,11 +591,21 @@ sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_
   a.draws = reinterpret_cast<DrawDesc*>(w + pl.off_draw);
   a.excl = reinterpret_cast<int32_t*>(w + pl.off_excl);
   a.excl_stride = pl.excl_stride;
-  e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
-              : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
-  if (e != cudaSuccess) return SV_ERR_CUDA;
-  DrawArgs d = draw_args(pl, target_logits, row_stride, rows_t, draft_logits, draft_logits ? draft_row_stride : 0,
-                         rows_d, B, V, es, c, workspace, K + 1, out_tokens, out_logprob, out_mu);
+  if (fuse) {
+    d.fused = 1;
+    d.k1_part = r.partials;
+    d.k1_T = r.T;
+    d.k1_G = r.G;
+    d.K = K;
+    d.drafts = draft_tokens;
+    d.uniforms = uniforms;
+    d.out_num = out_num_accepted;
+    d.draws_out = a.draws;
+  } else {
+    e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
+                : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+  }
   d.out_status = out_status;
   d.fin = fa;
   d.fin_here = (fa.out_len && !mu_pass) ? 1 : 0;

@@ -117,3 +117,17 @@ def test_more_chunks_than_the_pick_stages():
     got = sv.spec_verify_sample(ci.target, ci.draft_tokens, ci.uniforms, draft_logits=ci.draft_logits,
                                 temperature=ci.temperature)
     compare(got, _oracle_sample(ci), stochastic=True)
+
+
+def test_exact_rule_chains_past_the_fused_length():
+    # K + 1 > 16: the stochastic exact rule with draft logits runs the decide
+    # kernel (the chunk-sum kernel decides only chains of up to 16 rows)
+    ci = W.stochastic_chain(B=16, K=20, V=5000, seed=7950, device=DEV)
+    got = sv.spec_verify_sample(ci.target, ci.draft_tokens, ci.uniforms, draft_logits=ci.draft_logits,
+                                temperature=ci.temperature)
+    compare(got, _oracle_sample(ci), stochastic=True)
+    # and the fused length itself (K + 1 = 16)
+    ci = W.stochastic_chain(B=16, K=15, V=5000, seed=7951, device=DEV)
+    got = sv.spec_verify_sample(ci.target, ci.draft_tokens, ci.uniforms, draft_logits=ci.draft_logits,
+                                temperature=ci.temperature)
+    compare(got, _oracle_sample(ci), stochastic=True)
