@@ -753,7 +753,8 @@ def roofline(cfg, name, ms_per_step, read_bytes=None):
     achieved = (read_bytes if read_bytes is not None else alg) / (ms_per_step / 1e3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if kind == "measured" else "fallback 6.8 TB/s",
-            "kernel": kernel_desc(cfg), "traffic": recorded_traffic(name)}
+            "kernel": kernel_desc(cfg),
+            "traffic": recorded_traffic(name) if cfg["B"] == CONFIGS[name]["B"] else None}
 
 
 def per_config_entry(wl, t, world):
@@ -916,8 +917,15 @@ def main(argv=None):
                     help="seconds of oracle work for each cpu_baseline leg (one core, all cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time only the --config workload")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests per call for the --config workload (a smaller case for profiling; "
+                         "the workload string records it)")
     args = ap.parse_args(argv)
     cfg = CONFIGS[args.config]
+    if args.batch is not None:
+        if args.batch < 1:
+            ap.error("--batch must be >= 1")
+        cfg = dict(cfg, B=args.batch, workload=f"{cfg['workload']} [batch overridden: B={args.batch}]")
     if args.impl == "reference":
         return run_reference(args, cfg, args.config)
     return run_gpu(args, cfg, args.config)

@@ -77,13 +77,6 @@ struct RowStatsArgs {
   int32_t G;           // CTAs
   float c;             // log2(e) / T
   Partial* partials;   // [(rows + G) * kK1Consumers]: slot (row + cta) * kK1Consumers + warp
-  // L2 retention for a later re-read (stochastic chains, whose draw re-reads
-  // the rows of the first rejected position): rows at chain position
-  // < keep_pos (position = row mod rows_per_req0 in set0, mod rows_per_req1 in
-  // set1) are copied with evict_last, all others with evict_first. keep_pos = 0:
-  // plain copies.
-  int32_t keep_pos;
-  int32_t rows_per_req0, rows_per_req1;
 };
 
 // CTA that owns flattened element e under the equal split of T elements:
@@ -460,13 +453,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
       int st = 0, slot = 0;
       uint32_t phase = 0;   // parity of the current use of `slot`
       bool ok = true;
-      const uint64_t pol_keep = l2_policy_evict_last();
-      const uint64_t pol_drop = l2_policy_evict_first();
       for (int row = row0, j0 = j00; E0 < E1 && ok; ++row, j0 = 0) {
         const Piece p = make_piece<ES>(a, row, j0, E1);
-        bool keep = false;
-        if (a.keep_pos > 0)
-          keep = (row < a.set0.rows ? row % a.rows_per_req0 : (row - a.set0.rows) % a.rows_per_req1) < a.keep_pos;
         for (int s = 0; s < p.nst; ++s, ++st) {
           // the slot's previous use (parity phase ^ 1) must have been released
           if (st >= kK1Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) {
@@ -478,12 +466,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
                                      static_cast<uint32_t>(p.cp_hi - p.cp_lo) - off);
           const uint32_t fb = smem_u32(&full_bar[slot]);
           mbar_arrive_expect_tx(fb, bytes);
-          if (a.keep_pos > 0)
-            bulk_g2s_hint(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off),
-                          bytes, fb, keep ? pol_keep : pol_drop);
-          else
-            bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off), bytes,
-                     fb);
+          bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off), bytes, fb);
           if (++slot == kK1Stages) {
             slot = 0;
             phase ^= 1;

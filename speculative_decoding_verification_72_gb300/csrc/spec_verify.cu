@@ -256,35 +256,7 @@ RowStatsArgs row_stats_args(const Plan& pl, const void* tgt, int64_t tgt_stride,
   r.G = k1_grid(pl.T, es);
   r.c = c;
   r.partials = reinterpret_cast<Partial*>(static_cast<uint8_t*>(ws) + pl.off_part);
-  r.keep_pos = 0;
-  r.rows_per_req0 = 1;
-  r.rows_per_req1 = 1;
   return r;
-}
-
-// L2 bytes of the current device (looked up once per device).
-int64_t l2_bytes() {
-  static std::atomic<int64_t> cached[kMaxDevices];
-  const int dev = current_device();
-  if (dev >= 0 && dev < kMaxDevices) {
-    const int64_t v = cached[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
-  int n = 0;
-  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) n = 0;
-  if (dev >= 0 && dev < kMaxDevices && n > 0) cached[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
-
-// Chain positions whose rows a stochastic call keeps in L2 for the draw's
-// re-read: the first rejection is most likely early, so positions 0, 1, ...
-// are kept while their target (and draft) rows fit in 3/4 of L2; 0 keeps none.
-int32_t keep_positions(int64_t B, int64_t K, int64_t V, int es, bool with_draft) {
-  const int64_t per_pos = B * V * es * (with_draft ? 2 : 1);
-  const int64_t budget = l2_bytes() * 3 / 4;
-  if (per_pos <= 0 || budget <= 0) return 0;
-  const int64_t k = budget / per_pos;
-  return static_cast<int32_t>(k > K + 1 ? K + 1 : k);
 }
 
 DrawArgs draw_args(const Plan& pl, const void* tgt, int64_t tgt_stride, int64_t rows_t, const void* dft,
@@ -544,9 +516,6 @@ sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_
   const float c = kLog2e / temperature;
   RowStatsArgs r = row_stats_args(pl, target_logits, row_stride, rows_t, draft_logits, draft_row_stride, rows_d,
                                   V, es, c, workspace);
-  r.keep_pos = keep_positions(B, K, V, es, draft_logits != nullptr);
-  r.rows_per_req0 = K + 1;
-  r.rows_per_req1 = K > 0 ? K : 1;
   cudaError_t e = es == 2 ? launch_row_stats<2>(r, st) : launch_row_stats<4>(r, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(workspace);
