@@ -227,43 +227,48 @@ __device__ __forceinline__ float group_sum(const uint32_t (&w)[kGroupWords], flo
 constexpr int kStageFullVecs = kStageVecs * kK1ConsumerThreads;
 
 // Edge stages (the first and last of a piece whose copy hull reaches past the
-// piece, or a short last stage) are masked in place before the fold: each
-// thread rewrites only its own vectors v = ct + k * kK1ConsumerThreads, so no
-// other thread is involved. Vectors past nvec (not written by the copy) become
-// all -inf, and the vectors that may hold elements outside [j0, j1)
-// (mask_lo_v, mask_hi_v) get -inf in those elements. The fold then has a
-// single code path for every stage.
+// piece, or a short last stage) are masked in place before the fold. Vectors
+// past nvec (not written by the copy) become all -inf; each thread rewrites
+// only its own such vectors v = ct + k * kK1ConsumerThreads. The elements
+// outside [j0, j1) can only sit in vectors mask_lo_v and mask_hi_v (the
+// hull's first and last); each is rewritten by the one thread that folds it,
+// so the other threads do no per-element work. The fold then has a single
+// code path for every stage.
+template <int ES>
+__device__ __forceinline__ void mask_vec(uint4* sv4, int v, int jbase, int j0, int j1) {
+  constexpr int N = Elem<ES>::kVec;
+  const uint4 q = sv4[v];
+  uint32_t word[4] = {q.x, q.y, q.z, q.w};
+  const int jv = jbase + v * N;
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    if (jv + e < j0 || jv + e >= j1) {
+      if constexpr (ES == 2) {
+        const int wi = e >> 1;
+        word[wi] = (e & 1) ? ((word[wi] & 0x0000ffffu) | 0xff800000u) : ((word[wi] & 0xffff0000u) | 0x0000ff80u);
+      } else {
+        word[e] = 0xff800000u;
+      }
+    }
+  }
+  sv4[v] = make_uint4(word[0], word[1], word[2], word[3]);
+}
+
 template <int ES, int SV = kStageVecs>
 __device__ __forceinline__ void mask_stage(uint4* sv4, int ct, int nvec, int jbase, int j0, int j1,
                                            int mask_lo_v, int mask_hi_v, int nh = SV / kGroupVecs) {
-  constexpr int N = Elem<ES>::kVec;
   constexpr uint32_t kNegInfWord = ES == 2 ? 0xff80ff80u : 0xff800000u;   // -inf in every element
+  if (nvec < SV * kK1ConsumerThreads) {   // a short stage (uniform over the CTA)
 #pragma unroll
-  for (int k = 0; k < SV; ++k) {
-    const int v = ct + k * kK1ConsumerThreads;
-    if (k >= nh * kGroupVecs) {
-      // a half the warp does not fold (stage_halves): left as the copy wrote it
-    } else if (v >= nvec) {
-      sv4[v] = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
-    } else if (v == mask_lo_v || v == mask_hi_v) {
-      const uint4 q = sv4[v];
-      uint32_t word[4] = {q.x, q.y, q.z, q.w};
-      const int jv = jbase + v * N;
-#pragma unroll
-      for (int e = 0; e < N; ++e) {
-        if (jv + e < j0 || jv + e >= j1) {
-          if constexpr (ES == 2) {
-            const int wi = e >> 1;
-            word[wi] = (e & 1) ? ((word[wi] & 0x0000ffffu) | 0xff800000u)
-                               : ((word[wi] & 0xffff0000u) | 0x0000ff80u);
-          } else {
-            word[e] = kNegInfWord;
-          }
-        }
-      }
-      sv4[v] = make_uint4(word[0], word[1], word[2], word[3]);
+    for (int k = 0; k < SV; ++k) {
+      // a half the warp does not fold (stage_halves) is left as the copy wrote it
+      const int v = ct + k * kK1ConsumerThreads;
+      if (k < nh * kGroupVecs && v >= nvec) sv4[v] = make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
     }
   }
+  if (mask_lo_v >= 0 && ct == mask_lo_v % kK1ConsumerThreads) mask_vec<ES>(sv4, mask_lo_v, jbase, j0, j1);
+  if (mask_hi_v >= 0 && mask_hi_v != mask_lo_v && ct == mask_hi_v % kK1ConsumerThreads)
+    mask_vec<ES>(sv4, mask_hi_v, jbase, j0, j1);
   // These generic-proxy writes precede the next bulk copy into the slot.
   // (Fencing only in the threads that wrote was measured slower.)
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
