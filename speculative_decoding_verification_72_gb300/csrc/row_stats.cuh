@@ -176,26 +176,46 @@ __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Maximum of a group (NaN ignored: max.bf16x2 and max.f32 return the other
+// operand). vm[k] receives vector k's maximum as computed on the way: for
+// bf16 the packed pair max of its 8 elements, for fp32 the float's bits
+// (vec_max_of turns either into a float). The vectors' maxima come free from
+// the reduction tree, so locating the vector that holds a new maximum needs
+// no second pass over the stage.
 template <int ES>
-__device__ __forceinline__ float group_max(const uint32_t (&w)[kGroupWords]) {
+__device__ __forceinline__ float group_max(const uint32_t (&w)[kGroupWords], uint32_t (&vm)[kGroupVecs]) {
   if constexpr (ES == 2) {
     uint32_t a[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) a[i] = max_bf16x2(w[2 * i], w[2 * i + 1]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = max_bf16x2(a[2 * i], a[2 * i + 1]);
-    a[0] = max_bf16x2(a[0], a[1]);
-    a[2] = max_bf16x2(a[2], a[3]);
-    a[0] = max_bf16x2(a[0], a[2]);
-    return fmaxf(__uint_as_float(a[0] << 16), __uint_as_float(a[0] & 0xffff0000u));
+    for (int i = 0; i < 4; ++i) vm[i] = max_bf16x2(a[2 * i], a[2 * i + 1]);
+    const uint32_t b = max_bf16x2(max_bf16x2(vm[0], vm[1]), max_bf16x2(vm[2], vm[3]));
+    return fmaxf(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
   } else {
-    float t[6];
+    float t[4];
 #pragma unroll
-    for (int i = 0; i < 5; ++i)
-      t[i] = max3f(__uint_as_float(w[3 * i]), __uint_as_float(w[3 * i + 1]), __uint_as_float(w[3 * i + 2]));
-    t[5] = __uint_as_float(w[15]);
-    return fmaxf(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]));
+    for (int i = 0; i < 4; ++i) {
+      t[i] = fmaxf(max3f(__uint_as_float(w[4 * i]), __uint_as_float(w[4 * i + 1]), __uint_as_float(w[4 * i + 2])),
+                   __uint_as_float(w[4 * i + 3]));
+      vm[i] = __float_as_uint(t[i]);
+    }
+    return fmaxf(max3f(t[0], t[1], t[2]), t[3]);
   }
+}
+
+template <int ES>
+__device__ __forceinline__ float vec_max_of(uint32_t vmk) {
+  if constexpr (ES == 2)
+    return fmaxf(__uint_as_float(vmk << 16), __uint_as_float(vmk & 0xffff0000u));
+  else
+    return __uint_as_float(vmk);
+}
+
+template <int ES>
+__device__ __forceinline__ float group_max(const uint32_t (&w)[kGroupWords]) {
+  uint32_t vm[kGroupVecs];
+  return group_max<ES>(w, vm);
 }
 
 // sum over the group of 2^(x c - mc), with packed fp32x2 FMA / add.
@@ -287,35 +307,20 @@ __device__ __forceinline__ void load_half(const uint4* sv4, int ct, int h, uint3
   }
 }
 
-// Maximum of one 16-byte vector (NaN ignored, as in group_max).
-template <int ES>
-__device__ __forceinline__ float vec_max(const uint4& q) {
-  if constexpr (ES == 2) {
-    const uint32_t t = max_bf16x2(max_bf16x2(q.x, q.y), max_bf16x2(q.z, q.w));
-    return fmaxf(__uint_as_float(t << 16), __uint_as_float(t & 0xffff0000u));
-  } else {
-    return fmaxf(max3f(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z)), __uint_as_float(q.w));
-  }
-}
-
 // Record where the thread's new maximum gmax first appears in half h of this
-// stage: the lowest vector of the half whose maximum equals gmax (a half's
-// vectors follow in increasing index order), copied to the thread's stash
-// slot stash[ct]; resolve_cand later finds the element inside it.
+// stage: the lowest vector of the half whose maximum (vm, from group_max)
+// equals gmax, copied to the thread's stash slot stash[ct]; resolve_cand
+// later finds the element inside it.
 template <int ES>
-__device__ __forceinline__ void stash_first(const uint4* sv4, uint4* stash, int ct, int h, float gmax, int jbase,
-                                            int sg, GroupCand& cand) {
-  int kf = h * kGroupVecs + kGroupVecs - 1;
-  uint4 qf = sv4[ct + kf * kK1ConsumerThreads];
+__device__ __forceinline__ void stash_first(const uint4* sv4, uint4* stash, int ct, int h,
+                                            const uint32_t (&vm)[kGroupVecs], float gmax, int jbase, int sg,
+                                            GroupCand& cand) {
+  int kf = kGroupVecs - 1;
 #pragma unroll
-  for (int k = kGroupVecs - 2; k >= 0; --k) {
-    const uint4 q = sv4[ct + (h * kGroupVecs + k) * kK1ConsumerThreads];
-    if (vec_max<ES>(q) == gmax) {
-      kf = h * kGroupVecs + k;
-      qf = q;
-    }
-  }
-  stash[ct] = qf;
+  for (int k = kGroupVecs - 2; k >= 0; --k)
+    if (vec_max_of<ES>(vm[k]) == gmax) kf = k;
+  kf += h * kGroupVecs;
+  stash[ct] = sv4[ct + kf * kK1ConsumerThreads];
   cand.stage = sg;
   cand.vec = kf;
   cand.jbase = jbase;
@@ -337,12 +342,13 @@ template <int ES>
 __device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int ct, int jbase, int sg,
                                            float c, float& m, float& mc, float& s, GroupCand& cand) {
   uint32_t w[kGroupWords];
+  uint32_t va[kGroupVecs], vb[kGroupVecs];
   load_half(sv4, ct, 0, w);
   const float sa = group_sum<ES>(w, c, mc);
-  const float ga = group_max<ES>(w);
+  const float ga = group_max<ES>(w, va);
   load_half(sv4, ct, 1, w);
   const float sb = group_sum<ES>(w, c, mc);
-  const float gb = group_max<ES>(w);
+  const float gb = group_max<ES>(w, vb);
   const float gmax = fmaxf(ga, gb);
   const float gsum = sa + sb;
   if (gmax > m) {
@@ -358,7 +364,11 @@ __device__ __forceinline__ void fold_stage(const uint4* sv4, uint4* stash, int c
     }
     m = gmax;
     mc = nmc;
-    stash_first<ES>(sv4, stash, ct, ga >= gb ? 0 : 1, gmax, jbase, sg, cand);
+    const bool lo = ga >= gb;
+    uint32_t vm[kGroupVecs];
+#pragma unroll
+    for (int k = 0; k < kGroupVecs; ++k) vm[k] = lo ? va[k] : vb[k];
+    stash_first<ES>(sv4, stash, ct, lo ? 0 : 1, vm, gmax, jbase, sg, cand);
   } else if (gmax > -INFINITY) {
     s += gsum;
   }
@@ -386,9 +396,10 @@ __device__ __forceinline__ void fold_stage_n(const uint4* sv4, uint4* stash, int
   }
   if (nh == 0) return;
   uint32_t w[kGroupWords];
+  uint32_t va[kGroupVecs];
   load_half(sv4, ct, 0, w);
   const float gsum = group_sum<ES>(w, c, mc);
-  const float gmax = group_max<ES>(w);
+  const float gmax = group_max<ES>(w, va);
   if (gmax > m) {
     const float nmc = gmax * c;
     const float d = mc - nmc;
@@ -399,7 +410,7 @@ __device__ __forceinline__ void fold_stage_n(const uint4* sv4, uint4* stash, int
     }
     m = gmax;
     mc = nmc;
-    stash_first<ES>(sv4, stash, ct, 0, gmax, jbase, sg, cand);
+    stash_first<ES>(sv4, stash, ct, 0, va, gmax, jbase, sg, cand);
   } else if (gmax > -INFINITY) {
     s += gsum;
   }
