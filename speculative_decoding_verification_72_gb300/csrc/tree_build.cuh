@@ -14,8 +14,9 @@
 // into a 3-stage shared-memory ring with 1-D bulk copies (TMA); 7 consumer
 // warps fold each stage into (max, sum of exponentials) and keep per-thread
 // top-8 lists. After the first stage the consumers agree on a bound (the 8th
-// largest of their maxima: 8 elements of the row reach it), and from then on
-// only vectors whose maximum reaches it are inserted.
+// largest of their maxima: 8 elements of the row reach it), raised again after
+// later stages as the maxima cover more of the row; only vectors whose
+// maximum reaches it are inserted.
 // tree_select_kernel: one CTA per request expands level by level (the topk
 // best nodes of a level, score descending and earlier candidate first on
 // ties, each take the topk tokens of their row), keeps the n_nodes - 1 best
@@ -325,7 +326,10 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
           s += gsum;
         }
       }
-      if (st == 0) bound = tb_consumer_bound(m, ct, sm_, &s_bound);
+      // The bound tightens as the maxima cover more of the row (after
+      // stages 0, 1, 3, 6: each refresh roughly halves the share of elements
+      // that reach it); fewer offers then interrupt the warps.
+      if (st == 0 || st == 1 || st == 3 || st == 6) bound = fmaxf(bound, tb_consumer_bound(m, ct, sm_, &s_bound));
       if (ok) {
         if (ga >= bound && (ga > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
           tb_offer_half<ES>(sv4, ct, 0, jbase, Vp, j_lo, bound, v, ix);
