@@ -31,10 +31,13 @@
 namespace sv {
 
 constexpr int kK2Threads = 256;
-// Registers sized for three decide blocks per SM, so the draw kernels launched
-// behind a stochastic call's decide kernel (programmatic dependent launch)
+// Stochastic calls size the decide kernel's registers for three blocks per
+// SM, so the draw kernels launched behind it (programmatic dependent launch)
 // still find room for their blocks on the SMs that hold a decide block.
-constexpr int kK2MinBlocks = 3;
+// Greedy calls launch nothing behind it and take two blocks per SM, which
+// leaves the kernel enough registers not to spill.
+constexpr int kK2MinBlocksDraw = 3;
+constexpr int kK2MinBlocksGreedy = 2;
 // Row-piece slots a decide block stages in shared memory per row set (one
 // merged Partial each); a larger range falls back to per-thread merges.
 constexpr int kStageSlots = 640;
@@ -144,8 +147,8 @@ __device__ __forceinline__ float row_thr(const ChainArgs& a, int b, int i) {
   return a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * a.K + i] : INFINITY;
 }
 
-template <int ES>
-__global__ void __launch_bounds__(kK2Threads, kK2MinBlocks) chain_decide_kernel(const ChainArgs a) {
+template <int ES, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kK2Threads, MIN_BLOCKS) chain_decide_kernel(const ChainArgs a) {
   __shared__ int s_first;
   __shared__ int s_status;
   __shared__ int s_fin[2];

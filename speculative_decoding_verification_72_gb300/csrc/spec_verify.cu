@@ -465,8 +465,8 @@ sv_status spec_verify_greedy_ex(const void* target_logits, int32_t dtype, int64_
   a.out_logprob = out_logprob;
   a.out_mu = out_mu;
   a.out_status = out_status;
-  e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
-              : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+  e = es == 2 ? launch(chain_decide_kernel<2, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a)
+              : launch(chain_decide_kernel<4, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -571,8 +571,8 @@ sv_status spec_verify_sample_ex(const void* target_logits, int32_t dtype, int64_
     d.out_num = out_num_accepted;
     d.draws_out = a.draws;
   } else {
-    e = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
-                : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+    e = es == 2 ? launch(chain_decide_kernel<2, kK2MinBlocksDraw>, B, kK2Threads, 0, st, true, a)
+                : launch(chain_decide_kernel<4, kK2MinBlocksDraw>, B, kK2Threads, 0, st, true, a);
     if (e != cudaSuccess) return SV_ERR_CUDA;
   }
   d.out_status = out_status;
@@ -864,8 +864,8 @@ sv_status spec_verify_greedy_early(const void* target_logits, int32_t dtype, int
   a.cta_bytes = e.cta_bytes;
   a.n_cta = e.rs.G;
   a.out_bytes = reinterpret_cast<unsigned long long*>(out_bytes_read);
-  err = es == 2 ? launch(chain_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
-                : launch(chain_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
+  err = es == 2 ? launch(chain_decide_kernel<2, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a)
+                : launch(chain_decide_kernel<4, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a);
   return err == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -72,6 +72,17 @@ __device__ __forceinline__ bool tb_before(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
+// Fold the statistics (m2, s2) into (m, s), both sums relative to their own
+// maximum: the larger maximum stays and the other sum is rescaled to it.
+__device__ __forceinline__ void tb_merge_ms(float& m, float& s, float m2, float s2, float c) {
+  if (m2 > m) {
+    s = (m == -INFINITY ? 0.f : s * ex2((m - m2) * c)) + s2;
+    m = m2;
+  } else if (m2 != -INFINITY) {
+    s += s2 * ex2((m2 - m) * c);
+  }
+}
+
 // Insert (x, j) into a thread's sorted list; the thread visits indices in
 // increasing order, so an equal value goes after the ones it already holds.
 __device__ __forceinline__ void tb_insert(float (&v)[kTbMaxK], int (&ix)[kTbMaxK], float x, int j) {
@@ -198,11 +209,12 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   __shared__ int si_[kTbThreads][kTbMaxK];
   __shared__ float sm_[kTbThreads], ss_[kTbThreads];
   __shared__ float s_bound;
-  __shared__ int s_err;
+  __shared__ int s_err, s_ncand;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {   // shared-memory setup overlaps the previous kernel
     s_err = 0;
+    s_bound = -INFINITY;   // (a piece with no copied stage never sets it)
     for (int i = 0; i < kTbStages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), kTbConsumers);
@@ -348,65 +360,95 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   }
   __syncthreads();   // the bound's scratch (sm_) is free again
 
-  // block merge: pairwise, fixed tree (the order among threads does not matter
-  // for the lists: ties are broken by index); warp 0 contributes empty lists
+  // Row statistics: each warp folds its lanes' (m, s) with shuffles (fixed
+  // order), then thread 0 folds the warps' in order.
+  float wm = m, wsum = s;
 #pragma unroll
-  for (int q = 0; q < kTbMaxK; ++q) {
-    sv_[tid][q] = v[q];
-    si_[tid][q] = ix[q];
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, wm, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, wsum, o);
+    tb_merge_ms(wm, wsum, m2, s2, c);
   }
-  sm_[tid] = m;
-  ss_[tid] = s;
-  for (int half = kTbThreads / 2; half > 0; half >>= 1) {
-    __syncthreads();
-    if (tid < half) {
-      const int o = tid + half;
-      float rv[kTbMaxK];
-      int ri[kTbMaxK];
-      int pa = 0, pb = 0;
+  if (lane == 0) {
+    sm_[warp] = wm;
+    ss_[warp] = wsum;
+  }
+  // The row's top 8 hide among the list entries that reach the final bound:
+  // the bound never exceeds the row's 8th largest value and every element
+  // that reaches it was offered, so each of the top 8 sits in its thread's
+  // list. Those entries (a dozen or so; at most every list entry) are
+  // gathered, and one warp picks the 8 first by (value desc, index asc).
+  float* cv = &sv_[0][0];
+  int* ci = &si_[0][0];
+  const float fbound = s_bound;
+  int nmine = 0;
 #pragma unroll
-      for (int q = 0; q < kTbMaxK; ++q) {   // merge two sorted lists, keep the first 8
-        const float av = pa < kTbMaxK ? sv_[tid][pa] : -INFINITY;
-        const int ai = pa < kTbMaxK ? si_[tid][pa] : INT_MAX;
-        const float bv = pb < kTbMaxK ? sv_[o][pb] : -INFINITY;
-        const int bi = pb < kTbMaxK ? si_[o][pb] : INT_MAX;
-        const bool takeA = tb_before(av, ai, bv, bi);
-        rv[q] = takeA ? av : bv;
-        ri[q] = takeA ? ai : bi;
-        pa += takeA ? 1 : 0;
-        pb += takeA ? 0 : 1;
-      }
-      float mm = sm_[tid], ssum = ss_[tid];
-      const float m2 = sm_[o], s2 = ss_[o];
-      if (m2 > mm) {
-        ssum = (mm == -INFINITY ? 0.f : ssum * ex2((mm - m2) * c)) + s2;
-        mm = m2;
-      } else if (m2 != -INFINITY) {
-        ssum += s2 * ex2((m2 - mm) * c);
-      }
+  for (int q = 0; q < kTbMaxK; ++q) nmine += v[q] >= fbound ? 1 : 0;
+  if (tid == 0) s_ncand = 0;
+  __syncthreads();
+  if (nmine) {
+    const int at = atomicAdd(&s_ncand, nmine);
 #pragma unroll
-      for (int q = 0; q < kTbMaxK; ++q) {
-        sv_[tid][q] = rv[q];
-        si_[tid][q] = ri[q];
+    for (int q = 0; q < kTbMaxK; ++q)
+      if (q < nmine) {
+        cv[at + q] = v[q];
+        ci[at + q] = ix[q];
       }
-      sm_[tid] = mm;
-      ss_[tid] = ssum;
-    }
   }
   __syncthreads();
-  if (tid == 0) {
-    TopRow r;
-    const float mm = sm_[0];
-    r.bad = !(fabsf(mm) <= FLT_MAX) ? 1 : 0;
-    r.lse2 = mm * c + log2f(ss_[0]);
-    r.err = s_err;
-    r.pad1 = 0;
+  if (warp == 0) {
+    // each lane keeps the best 8 of its strided share, then 8 rounds of a
+    // warp-wide (value desc, index asc) maximum pop one entry each
+    float lv[kTbMaxK];
+    int li[kTbMaxK];
 #pragma unroll
     for (int q = 0; q < kTbMaxK; ++q) {
-      r.val[q] = sv_[0][q];
-      r.idx[q] = si_[0][q];
+      lv[q] = -INFINITY;
+      li[q] = INT_MAX;
     }
-    a.out[blockIdx.x] = r;
+    const int n = s_ncand;
+    for (int k = lane; k < n; k += 32) tb_insert(lv, li, cv[k], ci[k]);
+    float outv = -INFINITY;
+    int outi = INT_MAX;
+    for (int r = 0; r < kTbMaxK; ++r) {
+      float bv = lv[0];
+      int bi = li[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (tb_before(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (lane == r) {
+        outv = bv;
+        outi = bi;
+      }
+      if (li[0] == bi && lv[0] == bv) {   // the owner pops its head (indices are unique)
+#pragma unroll
+        for (int q = 0; q < kTbMaxK - 1; ++q) {
+          lv[q] = lv[q + 1];
+          li[q] = li[q + 1];
+        }
+        lv[kTbMaxK - 1] = -INFINITY;
+        li[kTbMaxK - 1] = INT_MAX;
+      }
+    }
+    float mm = -INFINITY, ssum = 0.f;
+    for (int w = 0; w < kTbThreads / 32; ++w) tb_merge_ms(mm, ssum, sm_[w], ss_[w], c);
+    TopRow* out = a.out + blockIdx.x;
+    if (lane < kTbMaxK) {
+      out->val[lane] = outv;
+      out->idx[lane] = outi;
+    }
+    if (lane == 0) {
+      out->bad = !(fabsf(mm) <= FLT_MAX) ? 1 : 0;
+      out->lse2 = mm * c + log2f(ssum);
+      out->err = s_err;
+      out->pad1 = 0;
+    }
   }
 }
 
@@ -420,21 +462,10 @@ struct TreeSelectArgs {
   int32_t* out_status;    // [B] or nullptr
 };
 
-// Rank of candidate i among n candidates by (score desc, creation asc).
-__device__ __forceinline__ int tb_rank(const float* sc, const int* ids, int n, int i) {
-  int r = 0;
-  const float si = sc[ids[i]];
-  for (int k = 0; k < n; ++k) {
-    const float sk = sc[ids[k]];
-    r += (sk > si || (sk == si && ids[k] < ids[i])) ? 1 : 0;
-  }
-  return r;
-}
-
 __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSelectArgs a) {
   __shared__ float sc[kTbMaxCands];
-  __shared__ int par[kTbMaxCands], tok[kTbMaxCands], dep[kTbMaxCands], pos[kTbMaxCands];
-  __shared__ int lvl[kTbMaxK * kTbMaxK], front[kTbMaxK];
+  __shared__ int par[kTbMaxCands], tok[kTbMaxCands], dep[kTbMaxCands], pos[kTbMaxCands], bfs[kTbMaxCands];
+  __shared__ int front[kTbMaxK];
   __shared__ TopRow rows[kTbMaxRows];
   grid_dep_wait();
   grid_dep_launch();
@@ -443,8 +474,21 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
   const float ln2 = kLn2;
   int bad = 0, err = 0;
   // merge each row's piece records: top 8 by (value desc, index asc), and the
-  // log-sum-exps (pieces in order, fixed)
-  for (int r = lane; r < a.R; r += kTbSelThreads) {
+  // log-sum-exps (pieces in order, fixed); rows of one piece are copied as
+  // they are, 16 bytes per thread
+  static_assert(sizeof(TopRow) % 16 == 0, "row records move as 16-byte words");
+  constexpr int kRowWords = sizeof(TopRow) / 16;
+  if (a.P == 1) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.rows + static_cast<int64_t>(b) * a.R);
+    uint4* dst = reinterpret_cast<uint4*>(rows);
+    for (int w = lane; w < a.R * kRowWords; w += kTbSelThreads) dst[w] = src[w];
+    __syncthreads();
+    for (int r = lane; r < a.R; r += kTbSelThreads) {
+      err |= rows[r].err;
+      rows[r].bad = !(fabsf(rows[r].val[0]) <= FLT_MAX) ? 1 : 0;   // the row's maximum
+    }
+  }
+  for (int r = lane; r < a.R && a.P > 1; r += kTbSelThreads) {
     const TopRow* pr = a.rows + (static_cast<int64_t>(b) * a.R + r) * a.P;
     TopRow out = pr[0];
     err |= out.err;
@@ -486,16 +530,29 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     par[lane] = -1;
     tok[lane] = r0.idx[lane];
     dep[lane] = 1;
-    lvl[lane] = lane;
   }
   if (lane == 0) bad |= rows[0].bad;
-  int n = k, lvl_n = k;
+  // A level's candidates are consecutive: [base, base + lvl_n), creation order.
+  int n = k, base = 0, lvl_n = k;
+  const int wid = lane >> 5, wl = lane & 31;
   __syncthreads();
   for (int d = 2; d <= a.depth; ++d) {
-    // the level's best k nodes, in rank order
-    for (int i = lane; i < lvl_n; i += kTbSelThreads) {
-      const int r = tb_rank(sc, lvl, lvl_n, i);
-      if (r < k) front[r] = lvl[i];
+    // the level's best k nodes, in rank order: warp w ranks candidates
+    // w, w + 8, ... against 32 others at a time (score desc, creation asc)
+    for (int i = wid; i < lvl_n; i += kTbSelThreads / 32) {
+      const float si = sc[base + i];
+      int r = 0;
+#pragma unroll 2
+      for (int q0 = 0; q0 < lvl_n; q0 += 32) {
+        const int q = q0 + wl;
+        bool before = false;
+        if (q < lvl_n) {
+          const float sq = sc[base + q];
+          before = sq > si || (sq == si && q < i);
+        }
+        r += __popc(__ballot_sync(0xffffffffu, before));
+      }
+      if (wl == 0 && r < k) front[r] = base + i;
     }
     __syncthreads();
     for (int t = lane; t < k * k; t += kTbSelThreads) {
@@ -509,49 +566,49 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
       dep[cidx] = d;
       if (j == 0) bad |= row.bad;
     }
-    __syncthreads();
-    for (int t = lane; t < k * k; t += kTbSelThreads) lvl[t] = n + t;
+    base = n;
     n += k * k;
     lvl_n = k * k;
     __syncthreads();
   }
-  // keep the n_nodes - 1 best candidates: one warp per candidate counts,
-  // 32 at a time, the candidates ranked before it (score desc, creation asc)
+  // keep the n_nodes - 1 best candidates: thread t ranks candidates t,
+  // t + blockDim, ... against all n (score desc, creation asc; the loads are
+  // broadcasts), then the kept ones take their BFS position (depth, score
+  // desc, creation) the same way
   const int keep = a.n_nodes - 1;
-  const int wid = lane >> 5, wl = lane & 31;
-  for (int i = wid; i < n; i += kTbSelThreads / 32) {
+  for (int i = lane; i < n; i += kTbSelThreads) {
     const float si = sc[i];
     int r = 0;
-    for (int q0 = 0; q0 < n; q0 += 32) {
-      const int q = q0 + wl;
-      const bool before = q < n && (sc[q] > si || (sc[q] == si && q < i));
-      r += __popc(__ballot_sync(0xffffffffu, before));
+#pragma unroll 8
+    for (int q = 0; q < n; ++q) {
+      const float sq = sc[q];
+      r += (sq > si || (sq == si && q < i)) ? 1 : 0;
     }
-    if (wl == 0) pos[i] = r < keep ? 1 : -1;
+    pos[i] = r < keep ? 1 : -1;
   }
   __syncthreads();
-  // BFS position among the kept: (depth, score desc, creation)
-  for (int i = wid; i < n; i += kTbSelThreads / 32) {
-    if (pos[i] < 0) continue;   // warp-uniform
-    const float si = sc[i];
-    const int di = dep[i];
-    int p = 1;
-    for (int q0 = 0; q0 < n; q0 += 32) {
-      const int q = q0 + wl;
-      const bool before = q < n && pos[q] > 0 &&
-                          (dep[q] < di || (dep[q] == di && (sc[q] > si || (sc[q] == si && q < i))));
-      p += __popc(__ballot_sync(0xffffffffu, before));
+  for (int i = lane; i < n; i += kTbSelThreads) {
+    int p = -1;
+    if (pos[i] > 0) {
+      const float si = sc[i];
+      const int di = dep[i];
+      p = 1;
+#pragma unroll 8
+      for (int q = 0; q < n; ++q) {
+        const int dq = dep[q];
+        const float sq = sc[q];
+        p += (pos[q] > 0 && (dq < di || (dq == di && (sq > si || (sq == si && q < i))))) ? 1 : 0;
+      }
     }
-    __syncwarp();
-    if (wl == 0) pos[i] = p + 1000000;   // marked: BFS position + offset (still kept for the others' tests)
+    bfs[i] = p;
   }
   __syncthreads();
   const int64_t ob = static_cast<int64_t>(b) * a.n_nodes;
   for (int i = lane; i < n; i += kTbSelThreads) {
-    if (pos[i] < 1000000) continue;
-    const int p = pos[i] - 1000000;
+    const int p = bfs[i];
+    if (p < 0) continue;
     a.out_tokens[ob + p] = tok[i];
-    a.out_parents[ob + p] = par[i] < 0 ? 0 : pos[par[i]] - 1000000;
+    a.out_parents[ob + p] = par[i] < 0 ? 0 : bfs[par[i]];
     if (a.out_scores) a.out_scores[ob + p] = sc[i];
   }
   if (lane == 0) {
