@@ -13,9 +13,9 @@
 // like the verify pass: warp 0's lane 0 copies the row's 16-byte-aligned hull
 // into a 3-stage shared-memory ring with 1-D bulk copies (TMA); 7 consumer
 // warps fold each stage into (max, sum of exponentials) and keep per-thread
-// top-8 lists. After the first stage the consumers agree on a bound (the 8th
-// largest of their maxima: 8 elements of the row reach it), raised again after
-// later stages as the maxima cover more of the row; only vectors whose
+// top-8 lists. After the first stage the consumers agree on a bound (8
+// elements of the row reach it: see tb_bound), which each warp raises again
+// after later stages as the maxima cover more of the row; only vectors whose
 // maximum reaches it are inserted.
 // tree_select_kernel: one CTA per request expands level by level (the topk
 // best nodes of a level, score descending and earlier candidate first on
@@ -103,43 +103,50 @@ __device__ __forceinline__ void tb_insert(float (&v)[kTbMaxK], int (&ix)[kTbMaxK
   }
 }
 
-// The 8th largest of the consumer threads' values x (-inf if fewer than 8
-// are finite). Every consumer thread calls it (named barrier 1); scratch
-// holds kTbConsumerThreads floats.
-__device__ __forceinline__ float tb_consumer_bound(float x, int ct, float* scratch, float* s_bound) {
-  scratch[ct] = x;
-  named_barrier_sync(1, kTbConsumerThreads);
-  if (ct < 32) {
-    constexpr int L = kTbConsumerThreads / 32;
-    const int lane = ct;
-    float loc[L];
+// A lower bound on the row's 8th largest value from the consumer threads'
+// running maxima (distinct elements, each only rising). Each consumer warp
+// publishes the two largest of its lanes' maxima in slot[2 cw], slot[2 cw + 1];
+// the bound is the 8th largest of the 2 * kTbConsumers published values, read
+// once per warp (lane l loads slot l) and shared by shuffles, so the warp
+// agrees on one snapshot. Any mix of older and newer slot values is still a
+// set of element values, so the result never exceeds the row's 8th largest:
+// warps need not wait for each other (with sync, a consumer barrier between
+// publishing and reading makes every warp's current values count).
+constexpr int kTbSlots = 2 * kTbConsumers;
+static_assert(kTbSlots >= kTbMaxK && kTbSlots <= 32, "one slot per lane");
+
+__device__ __forceinline__ float tb_slots_kth(volatile float* slot, int lane) {
+  const float x = lane < kTbSlots ? slot[lane] : -INFINITY;
+  int r = 0;   // rank of (x, lane) by value desc, lane asc
 #pragma unroll
-    for (int q = 0; q < L; ++q) loc[q] = scratch[lane * L + q];
-    float kth = -INFINITY;
-    for (int r = 0; r < kTbMaxK; ++r) {   // remove the current maximum 8 times
-      float lm = loc[0];
-      int lq = 0;
-#pragma unroll
-      for (int q = 1; q < L; ++q)
-        if (loc[q] > lm) {
-          lm = loc[q];
-          lq = q;
-        }
-      float wm = lm;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-      const unsigned own = __ballot_sync(0xffffffffu, lm == wm);
-      if (lane == __ffs(own) - 1) {   // one copy of the maximum leaves
-#pragma unroll
-        for (int q = 0; q < L; ++q)
-          if (q == lq) loc[q] = -INFINITY;
-      }
-      kth = wm;
-    }
-    if (lane == 0) *s_bound = kth;
+  for (int q = 0; q < kTbSlots; ++q) {
+    const float y = __shfl_sync(0xffffffffu, x, q);
+    r += (y > x || (y == x && q < lane)) ? 1 : 0;
   }
-  named_barrier_sync(1, kTbConsumerThreads);
-  return *s_bound;
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < kTbSlots && r == kTbMaxK - 1);
+  return __shfl_sync(0xffffffffu, x, __ffs(hit) - 1);
+}
+
+__device__ __forceinline__ void tb_publish_top2(float m, int cw, int lane, volatile float* slot) {
+  float t1 = m, t2 = -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+    const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+    t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+    t1 = fmaxf(t1, o1);
+  }
+  if (lane == 0) {
+    slot[2 * cw] = t1;
+    slot[2 * cw + 1] = t2;
+  }
+}
+
+__device__ __forceinline__ float tb_bound(float m, int cw, int lane, volatile float* slot, bool sync) {
+  tb_publish_top2(m, cw, lane, slot);
+  if (sync) named_barrier_sync(1, kTbConsumerThreads);
+  else __syncwarp();
+  return tb_slots_kth(slot, lane);
 }
 
 // One element outside the copied hull: folded into (m, s) with s relative to
@@ -208,13 +215,13 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   __shared__ float sv_[kTbThreads][kTbMaxK];
   __shared__ int si_[kTbThreads][kTbMaxK];
   __shared__ float sm_[kTbThreads], ss_[kTbThreads];
-  __shared__ float s_bound;
+  __shared__ float s_slot[kTbSlots];   // published warp maxima (tb_bound)
   __shared__ int s_err, s_ncand;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {   // shared-memory setup overlaps the previous kernel
     s_err = 0;
-    s_bound = -INFINITY;   // (a piece with no copied stage never sets it)
+    for (int q = 0; q < kTbSlots; ++q) s_slot[q] = -INFINITY;
     for (int i = 0; i < kTbStages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), kTbConsumers);
@@ -341,7 +348,7 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
       // The bound tightens as the maxima cover more of the row (after
       // stages 0, 1, 3, 6: each refresh roughly halves the share of elements
       // that reach it); fewer offers then interrupt the warps.
-      if (st == 0 || st == 1 || st == 3 || st == 6) bound = fmaxf(bound, tb_consumer_bound(m, ct, sm_, &s_bound));
+      if (st == 0 || st == 1 || st == 3 || st == 6) bound = fmaxf(bound, tb_bound(m, ct >> 5, lane, s_slot, st == 0));
       if (ok) {
         if (ga >= bound && (ga > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
           tb_offer_half<ES>(sv4, ct, 0, jbase, Vp, j_lo, bound, v, ix);
@@ -357,8 +364,9 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
     }
     for (int j = c_hi + ct; j < Vp; j += kTbConsumerThreads) tb_visit_ref(Elem<ES>::load(row, j), j_lo + j, c, m, mc, s, v, ix);
     if (m > -INFINITY) s = s * ex2(mc - m * c);   // s relative to m c for the merge (mc == m c already)
+    tb_publish_top2(m, ct >> 5, lane, s_slot);   // final maxima for the gather threshold
   }
-  __syncthreads();   // the bound's scratch (sm_) is free again
+  __syncthreads();   // the final maxima are published
 
   // Row statistics: each warp folds its lanes' (m, s) with shuffles (fixed
   // order), then thread 0 folds the warps' in order.
@@ -380,7 +388,7 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   // gathered, and one warp picks the 8 first by (value desc, index asc).
   float* cv = &sv_[0][0];
   int* ci = &si_[0][0];
-  const float fbound = s_bound;
+  const float fbound = tb_slots_kth(s_slot, lane);   // every warp, same final snapshot
   int nmine = 0;
 #pragma unroll
   for (int q = 0; q < kTbMaxK; ++q) nmine += v[q] >= fbound ? 1 : 0;
