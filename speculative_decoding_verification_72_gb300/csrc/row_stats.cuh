@@ -448,13 +448,27 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
   const int row0 = static_cast<int>(E0 / a.V);   // the one division; pieces then step row by row
   const int j00 = static_cast<int>(E0 - static_cast<int64_t>(row0) * a.V);
 
-  // Shared-memory setup overlaps the previous kernel's tail.
+  // Shared-memory setup overlaps the previous kernel's tail, and so does an
+  // L2 prefetch of the bytes of the CTA's first kK1Stages copies: a prefetch
+  // returns nothing to the program and L2 is where the previous kernel's
+  // writes land, so it may run before the dependency wait; the copies after
+  // the wait then find those bytes in L2 instead of waiting on DRAM.
   if (tid == 0) {
     for (int i = 0; i < kK1Stages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
       mbar_init(smem_u32(&empty_bar[i]), kK1Consumers);
     }
     fence_barrier_init();
+    int st = 0;
+    for (int row = row0, j0 = j00; E0 < E1 && st < kK1Stages; ++row, j0 = 0) {
+      const Piece p = make_piece<ES>(a, row, j0, E1);
+      for (int s = 0; s < p.nst && st < kK1Stages; ++s, ++st) {
+        const uint32_t off = static_cast<uint32_t>(s) * kK1StageBytes;
+        bulk_prefetch_l2(reinterpret_cast<const void*>(p.cp_lo + off),
+                         min(static_cast<uint32_t>(kK1StageBytes), static_cast<uint32_t>(p.cp_hi - p.cp_lo) - off));
+      }
+      if (static_cast<int64_t>(row) * a.V + p.j1 >= E1) break;
+    }
   }
   __syncthreads();
 

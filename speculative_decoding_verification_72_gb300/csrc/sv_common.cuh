@@ -135,6 +135,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (a hint: no data reaches the
+// program). src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Warp-wide maximum of a float in one instruction (redux.sync, sm_100 and
 // later). NaN inputs are ignored, as with fmaxf.
 __device__ __forceinline__ float warp_max(float v) {
