@@ -228,9 +228,6 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
     }
     fence_barrier_init();
   }
-  __syncthreads();
-  grid_dep_wait();
-  grid_dep_launch();
   // this CTA's piece: elements [j_lo, j_lo + Vp) of row blockIdx.x / P
   const int rowi = blockIdx.x / a.P;
   const int piece = blockIdx.x - rowi * a.P;
@@ -251,6 +248,16 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   const int nst = static_cast<int>((nbytes + kTbStageBytes - 1) / kTbStageBytes);
   const int c_lo = nbytes ? max(0, e0) : Vp;             // copied piece elements [c_lo, c_hi)
   const int c_hi = nbytes ? min(Vp, e0 + static_cast<int>(nbytes / ES)) : Vp;
+
+  // The first copies' bytes go to L2 before the dependency wait (a prefetch
+  // returns nothing to the program; the previous kernel's writes land in L2).
+  if (tid == 0)
+    for (int st = 0; st < nst && st < kTbStages; ++st)
+      bulk_prefetch_l2(reinterpret_cast<const void*>(clo + static_cast<uint32_t>(st) * kTbStageBytes),
+                       min(static_cast<uint32_t>(kTbStageBytes), nbytes - static_cast<uint32_t>(st) * kTbStageBytes));
+  __syncthreads();
+  grid_dep_wait();
+  grid_dep_launch();
 
   float m = -INFINITY, s = 0.f;
   float v[kTbMaxK];
