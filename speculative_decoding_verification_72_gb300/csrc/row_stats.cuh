@@ -698,10 +698,18 @@ __device__ __forceinline__ void merge_row_half(const Partial* __restrict__ parts
     const int g_lo = cta_of(e0, T, G), g_hi = cta_of(e0 + V - 1, T, G);
     const int n = (g_hi - g_lo + 1) * kK1Consumers;
     const Partial* p = parts + (row + g_lo) * kK1Consumers;
-    for (int k = lane16; k < n; k += 16) {
-      const Partial v = p[k];
-      merge_stats(m, s, idx, v.m, v.s, v.idx, c);
-      err |= v.err;
+    // two of the lane's partials per iteration, both loaded before either is
+    // merged (the same merge order, one L2 round trip for rows of <= 32)
+    for (int k = lane16; k < n; k += 32) {
+      const Partial v0 = p[k];
+      Partial v1;
+      if (k + 16 < n) v1 = p[k + 16];
+      merge_stats(m, s, idx, v0.m, v0.s, v0.idx, c);
+      err |= v0.err;
+      if (k + 16 < n) {
+        merge_stats(m, s, idx, v1.m, v1.s, v1.idx, c);
+        err |= v1.err;
+      }
     }
   }
 #pragma unroll
