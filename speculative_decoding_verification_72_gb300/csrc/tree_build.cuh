@@ -357,10 +357,12 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
       // that reach it); fewer offers then interrupt the warps.
       if (st == 0 || st == 1 || st == 3 || st == 6) bound = fmaxf(bound, tb_bound(m, ct >> 5, lane, s_slot, st == 0));
       if (ok) {
-        if (ga >= bound && (ga > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
-          tb_offer_half<ES>(sv4, ct, 0, jbase, Vp, j_lo, bound, v, ix);
-        if (gb >= bound && (gb > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
-          tb_offer_half<ES>(sv4, ct, 1, jbase, Vp, j_lo, bound, v, ix);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {   // one copy of the offer path
+          const float gh = h ? gb : ga;
+          if (gh >= bound && (gh > v[kTbMaxK - 1] || ix[kTbMaxK - 1] == INT_MAX))
+            tb_offer_half<ES>(sv4, ct, h, jbase, Vp, j_lo, bound, v, ix);
+        }
       }
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
