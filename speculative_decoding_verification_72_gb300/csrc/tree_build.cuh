@@ -597,9 +597,9 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     const float si = sc[i];
     int r = 0;
 #pragma unroll 8
-    for (int q = 0; q < n; ++q) {
+    for (int q = 0; q < n; ++q) {   // branch-free: bitwise, not short-circuit, tests
       const float sq = sc[q];
-      r += (sq > si || (sq == si && q < i)) ? 1 : 0;
+      r += static_cast<int>((sq > si) | ((sq == si) & (q < i)));
     }
     pos[i] = r < keep ? 1 : -1;
   }
@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
       for (int q = 0; q < n; ++q) {
         const int dq = dep[q];
         const float sq = sc[q];
-        p += (pos[q] > 0 && (dq < di || (dq == di && (sq > si || (sq == si && q < i))))) ? 1 : 0;
+        p += static_cast<int>((pos[q] > 0) & ((dq < di) | ((dq == di) & ((sq > si) | ((sq == si) & (q < i))))));
       }
     }
     bfs[i] = p;
