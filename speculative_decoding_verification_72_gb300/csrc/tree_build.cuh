@@ -549,45 +549,45 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     dep[lane] = 1;
   }
   if (lane == 0) bad |= rows[0].bad;
-  // A level's candidates are consecutive: [base, base + lvl_n), creation order.
-  int n = k, base = 0, lvl_n = k;
+  // A level's candidates are consecutive: [base, base + lvl_n), creation
+  // order. One warp expands the levels (no block barriers): lane l ranks
+  // candidates l, l + 32, ... of the level against all of them (score desc,
+  // creation asc), then lanes expand the best k, k children each.
   const int wid = lane >> 5, wl = lane & 31;
+  const int n = k + (a.depth - 1) * k * k;   // candidates after the last level
   __syncthreads();
-  for (int d = 2; d <= a.depth; ++d) {
-    // the level's best k nodes, in rank order: warp w ranks candidates
-    // w, w + 8, ... against 32 others at a time (score desc, creation asc)
-    for (int i = wid; i < lvl_n; i += kTbSelThreads / 32) {
-      const float si = sc[base + i];
-      int r = 0;
-#pragma unroll 2
-      for (int q0 = 0; q0 < lvl_n; q0 += 32) {
-        const int q = q0 + wl;
-        bool before = false;
-        if (q < lvl_n) {
+  if (wid == 0) {
+    int nn = k, base = 0, lvl_n = k;
+    for (int d = 2; d <= a.depth; ++d) {
+      for (int i = wl; i < lvl_n; i += 32) {
+        const float si = sc[base + i];
+        int r = 0;
+#pragma unroll 4
+        for (int q = 0; q < lvl_n; ++q) {
           const float sq = sc[base + q];
-          before = sq > si || (sq == si && q < i);
+          r += static_cast<int>((sq > si) | ((sq == si) & (q < i)));
         }
-        r += __popc(__ballot_sync(0xffffffffu, before));
+        if (r < k) front[r] = base + i;
       }
-      if (wl == 0 && r < k) front[r] = base + i;
+      __syncwarp();
+      for (int t = wl; t < k * k; t += 32) {
+        const int r = t / k, j = t - r * k;
+        const int node = front[r];
+        const TopRow& row = rows[1 + (d - 2) * k + r];
+        const int cidx = nn + t;
+        sc[cidx] = sc[node] + fminf(0.f, (row.val[j] * a.c - row.lse2) * ln2);
+        par[cidx] = node;
+        tok[cidx] = row.idx[j];
+        dep[cidx] = d;
+        if (j == 0) bad |= row.bad;
+      }
+      __syncwarp();
+      base = nn;
+      nn += k * k;
+      lvl_n = k * k;
     }
-    __syncthreads();
-    for (int t = lane; t < k * k; t += kTbSelThreads) {
-      const int r = t / k, j = t - r * k;
-      const int node = front[r];
-      const TopRow& row = rows[1 + (d - 2) * k + r];
-      const int cidx = n + t;
-      sc[cidx] = sc[node] + fminf(0.f, (row.val[j] * a.c - row.lse2) * ln2);
-      par[cidx] = node;
-      tok[cidx] = row.idx[j];
-      dep[cidx] = d;
-      if (j == 0) bad |= row.bad;
-    }
-    base = n;
-    n += k * k;
-    lvl_n = k * k;
-    __syncthreads();
   }
+  __syncthreads();
   // keep the n_nodes - 1 best candidates: thread t ranks candidates t,
   // t + blockDim, ... against all n (score desc, creation asc; the loads are
   // broadcasts), then the kept ones take their BFS position (depth, score
