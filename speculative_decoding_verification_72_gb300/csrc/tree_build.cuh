@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {   // shared-memory setup overlaps the previous kernel
     s_err = 0;
+    s_ncand = 0;
     for (int q = 0; q < kTbSlots; ++q) s_slot[q] = -INFINITY;
     for (int i = 0; i < kTbStages; ++i) {
       mbar_init(smem_u32(&full_bar[i]), 1);
@@ -401,9 +402,7 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
   int nmine = 0;
 #pragma unroll
   for (int q = 0; q < kTbMaxK; ++q) nmine += v[q] >= fbound ? 1 : 0;
-  if (tid == 0) s_ncand = 0;
-  __syncthreads();
-  if (nmine) {
+  if (nmine) {   // (s_ncand was zeroed at the start)
     const int at = atomicAdd(&s_ncand, nmine);
 #pragma unroll
     for (int q = 0; q < kTbMaxK; ++q)
@@ -453,19 +452,19 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
         li[kTbMaxK - 1] = INT_MAX;
       }
     }
-    float mm = -INFINITY, ssum = 0.f;
-    for (int w = 0; w < kTbThreads / 32; ++w) tb_merge_ms(mm, ssum, sm_[w], ss_[w], c);
     TopRow* out = a.out + blockIdx.x;
     if (lane < kTbMaxK) {
       out->val[lane] = outv;
       out->idx[lane] = outi;
     }
-    if (lane == 0) {
-      out->bad = !(fabsf(mm) <= FLT_MAX) ? 1 : 0;
-      out->lse2 = mm * c + log2f(ssum);
-      out->err = s_err;
-      out->pad1 = 0;
-    }
+  } else if (warp == 1 && lane == 0) {   // the row statistics, beside the selection
+    float mm = -INFINITY, ssum = 0.f;
+    for (int w = 0; w < kTbThreads / 32; ++w) tb_merge_ms(mm, ssum, sm_[w], ss_[w], c);
+    TopRow* out = a.out + blockIdx.x;
+    out->bad = !(fabsf(mm) <= FLT_MAX) ? 1 : 0;
+    out->lse2 = mm * c + log2f(ssum);
+    out->err = s_err;
+    out->pad1 = 0;
   }
 }
 
