@@ -412,7 +412,31 @@ __global__ void __launch_bounds__(kTbThreads, kTbCtasPerSm) row_topk_kernel(cons
       }
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 0 && s_ncand <= 32) {
+    // one candidate per lane: its rank by (value desc, index asc) against
+    // all others in one pass of shuffles; ranks 0..7 are the top 8 (the
+    // bound guarantees at least 8 candidates unless it is -inf, and then every
+    // list entry is gathered, more than 32)
+    const int n = s_ncand;
+    const float x = lane < n ? cv[lane] : -INFINITY;
+    const int xi = lane < n ? ci[lane] : INT_MAX;
+    int r = 0;
+#pragma unroll 8
+    for (int q = 0; q < 32; ++q) {
+      const float y = __shfl_sync(0xffffffffu, x, q);
+      const int yi = __shfl_sync(0xffffffffu, xi, q);
+      r += (q < n && q != lane && tb_before(y, yi, x, xi)) ? 1 : 0;
+    }
+    TopRow* out = a.out + blockIdx.x;
+    if (lane < n && r < kTbMaxK) {
+      out->val[r] = x;
+      out->idx[r] = xi;
+    }
+    if (lane >= n && lane < kTbMaxK) {   // (fewer than 8 candidates: empty slots)
+      out->val[lane] = -INFINITY;
+      out->idx[lane] = INT_MAX;
+    }
+  } else if (warp == 0) {
     // each lane keeps the best 8 of its strided share, then 8 rounds of a
     // warp-wide (value desc, index asc) maximum pop one entry each
     float lv[kTbMaxK];
