@@ -518,14 +518,14 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
   // they are, 16 bytes per thread
   static_assert(sizeof(TopRow) % 16 == 0, "row records move as 16-byte words");
   constexpr int kRowWords = sizeof(TopRow) / 16;
-  if (a.P == 1) {
+  if (a.P == 1) {   // (the row pass set bad from the same maximum)
+    static_assert(offsetof(TopRow, err) == 8, "err is the third word of a record's first 16 bytes");
     const uint4* src = reinterpret_cast<const uint4*>(a.rows + static_cast<int64_t>(b) * a.R);
     uint4* dst = reinterpret_cast<uint4*>(rows);
-    for (int w = lane; w < a.R * kRowWords; w += kTbSelThreads) dst[w] = src[w];
-    __syncthreads();
-    for (int r = lane; r < a.R; r += kTbSelThreads) {
-      err |= rows[r].err;
-      rows[r].bad = !(fabsf(rows[r].val[0]) <= FLT_MAX) ? 1 : 0;   // the row's maximum
+    for (int w = lane; w < a.R * kRowWords; w += kTbSelThreads) {
+      const uint4 q = src[w];
+      dst[w] = q;
+      if (w % kRowWords == 0) err |= static_cast<int>(q.z);
     }
   }
   for (int r = lane; r < a.R && a.P > 1; r += kTbSelThreads) {
@@ -562,24 +562,24 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     rows[r] = out;
   }
   __syncthreads();
-  // level 1: the root row's top tokens
-  if (lane < k) {
-    const TopRow& r0 = rows[0];
-    // log-probs are <= 0 (clamped: fp32 rounding must not let a child outscore its parent)
-    sc[lane] = fminf(0.f, (r0.val[lane] * a.c - r0.lse2) * ln2);
-    par[lane] = -1;
-    tok[lane] = r0.idx[lane];
-    dep[lane] = 1;
-  }
-  if (lane == 0) bad |= rows[0].bad;
-  // A level's candidates are consecutive: [base, base + lvl_n), creation
-  // order. One warp expands the levels (no block barriers): lane l ranks
-  // candidates l, l + 32, ... of the level against all of them (score desc,
-  // creation asc), then lanes expand the best k, k children each.
+  // Level 1 is the root row's top tokens. A level's candidates are
+  // consecutive: [base, base + lvl_n), creation order. One warp builds the
+  // levels (no block barriers): lane l ranks candidates l, l + 32, ... of the
+  // level against all of them (score desc, creation asc), then lanes expand
+  // the best k, k children each.
   const int wid = lane >> 5, wl = lane & 31;
   const int n = k + (a.depth - 1) * k * k;   // candidates after the last level
-  __syncthreads();
   if (wid == 0) {
+    if (wl < k) {
+      const TopRow& r0 = rows[0];
+      // log-probs are <= 0 (clamped: fp32 rounding must not let a child outscore its parent)
+      sc[wl] = fminf(0.f, (r0.val[wl] * a.c - r0.lse2) * ln2);
+      par[wl] = -1;
+      tok[wl] = r0.idx[wl];
+      dep[wl] = 1;
+    }
+    if (wl == 0) bad |= rows[0].bad;
+    __syncwarp();
     int nn = k, base = 0, lvl_n = k;
     for (int d = 2; d <= a.depth; ++d) {
       for (int i = wl; i < lvl_n; i += 32) {
