@@ -505,12 +505,15 @@ struct TreeSelectArgs {
 __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSelectArgs a) {
   __shared__ float sc[kTbMaxCands];
   __shared__ int par[kTbMaxCands], tok[kTbMaxCands], dep[kTbMaxCands], pos[kTbMaxCands], bfs[kTbMaxCands];
+  __shared__ int s_excl[kTbMaxCands];
+  __shared__ int s_nexcl;
   __shared__ int front[kTbMaxK];
   __shared__ TopRow rows[kTbMaxRows];
   grid_dep_wait();
   grid_dep_launch();
   const int b = blockIdx.x, lane = threadIdx.x;
   const int k = a.topk;
+  if (lane == 0) s_nexcl = 0;
   const float ln2 = kLn2;
   int bad = 0, err = 0;
   // merge each row's piece records: top 8 by (value desc, index asc), and the
@@ -611,34 +614,44 @@ __global__ void __launch_bounds__(kTbSelThreads) tree_select_kernel(const TreeSe
     }
   }
   __syncthreads();
-  // keep the n_nodes - 1 best candidates: thread t ranks candidates t,
-  // t + blockDim, ... against all n (score desc, creation asc; the loads are
-  // broadcasts), then the kept ones take their BFS position (depth, score
-  // desc, creation) the same way
+  // Keep the n_nodes - 1 best candidates and give the kept ones their BFS
+  // position (depth, score desc, creation), in one pass: thread t takes
+  // candidates t, t + blockDim, ... and counts, over all n (broadcast loads,
+  // branch-free tests), the candidates ranked before it by score and those
+  // before it in BFS order. The excluded ones (the n - keep last by score, a
+  // handful) are gathered, and a kept candidate's position is its BFS count
+  // less the excluded candidates before it.
   const int keep = a.n_nodes - 1;
   for (int i = lane; i < n; i += kTbSelThreads) {
     const float si = sc[i];
-    int r = 0;
+    const int di = dep[i];
+    int r = 0, pb = 0;
 #pragma unroll 8
-    for (int q = 0; q < n; ++q) {   // branch-free: bitwise, not short-circuit, tests
+    for (int q = 0; q < n; ++q) {
       const float sq = sc[q];
-      r += static_cast<int>((sq > si) | ((sq == si) & (q < i)));
+      const int dq = dep[q];
+      const bool by_score = (sq > si) | ((sq == si) & (q < i));
+      r += static_cast<int>(by_score);
+      pb += static_cast<int>((dq < di) | ((dq == di) & by_score));
     }
-    pos[i] = r < keep ? 1 : -1;
+    const bool kept = r < keep;
+    if (!kept) s_excl[atomicAdd(&s_nexcl, 1)] = i;
+    pos[i] = kept ? pb : -1;
   }
   __syncthreads();
+  const int nexcl = s_nexcl;
   for (int i = lane; i < n; i += kTbSelThreads) {
-    int p = -1;
-    if (pos[i] > 0) {
+    int p = pos[i];
+    if (p >= 0) {
       const float si = sc[i];
       const int di = dep[i];
-      p = 1;
-#pragma unroll 8
-      for (int q = 0; q < n; ++q) {
-        const int dq = dep[q];
+      for (int e = 0; e < nexcl; ++e) {
+        const int q = s_excl[e];
         const float sq = sc[q];
-        p += static_cast<int>((pos[q] > 0) & ((dq < di) | ((dq == di) & ((sq > si) | ((sq == si) & (q < i))))));
+        const int dq = dep[q];
+        p -= static_cast<int>((dq < di) | ((dq == di) & ((sq > si) | ((sq == si) & (q < i)))));
       }
+      p += 1;   // position 0 is the root
     }
     bfs[i] = p;
   }
