@@ -585,7 +585,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_kernel(const RowStatsArgs a) {
       out.s = ws;
       out.idx = widx;
       out.err = ok ? 0 : 1;
-      a.partials[(static_cast<int64_t>(p.row) + g) * kK1Consumers + cw] = out;
+      store_partial_keep(a.partials + (static_cast<int64_t>(p.row) + g) * kK1Consumers + cw, out);
     }
     if (static_cast<int64_t>(row) * a.V + p.j1 >= E1) break;
   }

@@ -141,6 +141,18 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Store of one Partial that asks L2 to keep the line (evict_last): the
+// decide kernels read the partials after the row pass, which meanwhile
+// streams far more than L2 holds, and partials written early in it would
+// otherwise have left L2 by then.
+__device__ __forceinline__ void store_partial_keep(Partial* dst, const Partial& v) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(__float_as_uint(v.m)),
+               "r"(__float_as_uint(v.s)), "r"(static_cast<uint32_t>(v.idx)), "r"(static_cast<uint32_t>(v.err)), "l"(pol)
+               : "memory");
+}
+
 // Warp-wide maximum of a float in one instruction (redux.sync, sm_100 and
 // later). NaN inputs are ignored, as with fmaxf.
 __device__ __forceinline__ float warp_max(float v) {
