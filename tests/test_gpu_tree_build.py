@@ -120,3 +120,29 @@ def test_rows_longer_than_one_piece():
     # V > 2^20: each row is read by two CTAs whose records the selection merges
     y = W.draft_tree_rows(B=2, V=(1 << 20) + 4099, depth=2, topk=2, dtype=torch.bfloat16, seed=7707, device=DEV)
     _check(y, 2, 2, 7, max_ties=1.0)
+
+
+def test_rows_with_many_tied_maxima():
+    """More than 32 entries reach a row's final bound when its top value is
+    shared by 40 tokens: the row pass takes its general top-8 selection
+    (lowest index first on ties) instead of the one-pass ranks. The tied
+    maxima dominate every row's log-sum-exp, so level-2 scores of different
+    rows fall within the oracle's near-tie distance and whole trees are only
+    checked for validity; the tie rule itself is checked exactly: the root's
+    children are its four lowest-index tied tokens, and the children of the
+    level-1 node of rank r are the four lowest-index tied tokens of row 1 + r."""
+    B, V, depth, topk = 8, 5000, 2, 4
+    y = W.draft_tree_rows(B=B, V=V, depth=depth, topk=topk, dtype=torch.float32, std=1.0, seed=7708, device=DEV)
+    rng = np.random.default_rng(7709)
+    for b in range(B):
+        for r in range(y.shape[1]):
+            tied = rng.choice(V, size=40, replace=False)
+            y[b, r, torch.as_tensor(tied, device=DEV)] = 10.0
+    got = _check(y, depth, topk, 1 + topk + topk * topk, max_ties=1.0)
+    tok, par, yh = host(got["tokens"]), host(got["parents"]), host(y)
+    for b in range(B):
+        lowest = [np.sort(np.nonzero(yh[b, r] == 10.0)[0])[:topk] for r in range(yh.shape[1])]
+        assert np.array_equal(tok[b, 1:1 + topk], lowest[0]), b   # equal scores: creation order
+        for n in range(1 + topk, 1 + topk + topk * topk):
+            rank = par[b, n] - 1
+            assert 0 <= rank < topk and tok[b, n] in lowest[1 + rank], (b, n)
