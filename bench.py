@@ -134,6 +134,8 @@ _CALL_SOURCES = {
     "greedy": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "spec_verify.cu"),
     "draw": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "draw.cuh", "rules.cuh",
              "spec_verify.cu"),
+    "tree_draw": ("sv_common.cuh", "row_stats.cuh", "decide.cuh", "finish.cuh", "draw.cuh", "rules.cuh",
+                  "tree_draw.cuh", "spec_verify.cu"),
     "early": ("sv_common.cuh", "row_stats.cuh", "row_stats_early.cuh", "decide.cuh", "finish.cuh",
               "spec_verify.cu"),
     "tree_build": ("sv_common.cuh", "row_stats.cuh", "tree_build.cuh", "spec_verify.cu"),
@@ -150,9 +152,9 @@ def source_hash(cfg=None):
     if cfg is None:
         names = [n for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh"))]
     else:
-        draws = cfg["kind"] == "sample" or (cfg["kind"] == "tree" and cfg.get("T"))
         kind = ("early" if cfg.get("early") else cfg["kind"] if cfg["kind"] in ("tree_build", "kv_compact")
-                else "draw" if draws else "greedy")
+                else "draw" if cfg["kind"] == "sample" else "tree_draw" if cfg["kind"] == "tree" and cfg.get("T")
+                else "greedy")
         names = sorted(_CALL_SOURCES[kind])
     for name in names:
         with open(os.path.join(csrc, name), "rb") as f:

@@ -25,6 +25,7 @@
 #include "row_stats_early.cuh"
 #include "rules.cuh"
 #include "tree_build.cuh"
+#include "tree_draw.cuh"
 #include "kv_compact.cuh"
 #include "selftest.cuh"
 
@@ -126,7 +127,7 @@ int sm_count() {
 
 // Runs `set` (kernel attribute calls) once per device for the attribute group
 // `bit`; a failed attempt is retried on the next call.
-enum AttrBit : uint32_t { kAttrK1 = 1, kAttrK1Early = 2, kAttrRowTopk = 4, kAttrDraw = 8 };
+enum AttrBit : uint32_t { kAttrK1 = 1, kAttrK1Early = 2, kAttrRowTopk = 4, kAttrDraw = 8, kAttrTreeDraw = 16 };
 
 template <typename F>
 cudaError_t once_per_device(uint32_t bit, F&& set) {
@@ -315,6 +316,18 @@ cudaError_t launch_draw(const DrawArgs& d, cudaStream_t stream) {
   e = launch(draw_sum_kernel<ES>, d.G, kK3Threads, kK3SmemBytes, stream, true, d);
   if (e != cudaSuccess) return e;
   return launch(draw_pick_kernel<ES>, d.B, kK3PickThreads, 0, stream, true, d);
+}
+
+// Stochastic tree call: merge, walk and draw in one cluster kernel (one
+// cluster of kTwCluster CTAs per request).
+template <int ES>
+cudaError_t launch_tree_walk_draw(const TwArgs& w, cudaStream_t stream) {
+  const cudaError_t e = once_per_device(kAttrTreeDraw << (ES == 2 ? 0 : 8), [] {
+    return set_smem_attrs(tree_walk_draw_kernel<ES>, static_cast<int>(tw_layout(kMaxTreeNodes, kTwMaxChunks).total));
+  });
+  if (e != cudaSuccess) return e;
+  return launch(tree_walk_draw_kernel<ES>, w.t.B * kTwCluster, kTwThreads, tw_layout(w.t.N, w.nch).total, stream,
+                true, w);
 }
 
 // Finish-step arguments of a call (disabled when fin is null).
@@ -695,6 +708,19 @@ sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t 
   a.draws = reinterpret_cast<DrawDesc*>(w + pl.off_draw);
   a.excl = reinterpret_cast<int32_t*>(w + pl.off_excl);
   a.excl_stride = pl.excl_stride;
+  // One kernel for the stochastic walk and its draw when every chunk of a
+  // row starts on a 16-byte boundary and a row's chunks fit the cluster.
+  if (!greedy && aligned(target_logits, 16) && (row_stride * es) % 16 == 0 && pl.P <= kTwMaxP) {
+    TwArgs tw;
+    std::memset(&tw, 0, sizeof(tw));
+    tw.t = a;
+    tw.tgt_hi = row_set(target_logits, row_stride, rows, V, es).safe_hi;
+    tw.P = pl.P;
+    tw.chunk_elems = pl.chunk_elems;
+    tw.nch = (pl.P + kTwCluster - 1) / kTwCluster;
+    e = es == 2 ? launch_tree_walk_draw<2>(tw, st) : launch_tree_walk_draw<4>(tw, st);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  }
   e = es == 2 ? launch(tree_decide_kernel<2>, B, kK2Threads, 0, st, true, a)
               : launch(tree_decide_kernel<4>, B, kK2Threads, 0, st, true, a);
   if (e != cudaSuccess) return SV_ERR_CUDA;

@@ -1,0 +1,664 @@
+// Stochastic tree verification in one kernel: the row-statistics merge, the
+// walk (nanospec README, tree configuration) and the draw that ends it (the
+// masked or bonus sample; spec-decode README, "How it works" for the inverse
+// CDF), for one request per thread-block cluster.
+//
+// The same computation as tree_decide_kernel followed by draw_sum_kernel and
+// draw_pick_kernel, without their two kernel boundaries and global round
+// trips. A cluster of kTwCluster CTAs serves request b:
+//
+//  1. CTA r merges the K1 partials of rows [r * per, (r + 1) * per) of the
+//     request (per = ceil(N / kTwCluster); the staged merge order of the
+//     decide kernel, so the statistics are the same bits) and stores them
+//     into CTA 0's shared memory (distributed shared memory).
+//  2. Cluster barrier. CTA 0 forms every node's log2 p in parallel, then one
+//     thread walks from the root as the decide kernel does (same arithmetic
+//     and order) and writes the accepted path. The draw descriptor and the
+//     rejected tokens are stored into every CTA's shared memory.
+//  3. Cluster barrier. CTA r copies chunks [r * nch, (r + 1) * nch) of the
+//     drawn row (kK3ChunkBytes each, 1-D bulk copies) into its shared memory,
+//     masks the rejected tokens and the row's end with -inf, sums (w, p) per
+//     chunk and stores the sums into every CTA's shared memory.
+//  4. Cluster barrier. Every CTA finds the chunk where u * S falls (the pick
+//     kernel's warp scan over the chunk sums); the CTA holding that chunk
+//     resolves the token with a block scan of its shared-memory copy and
+//     writes the draw, the status and the finish step.
+//
+// After barrier 3 no CTA touches another's shared memory, so the CTAs not
+// holding the drawn chunk simply exit. The copies wait on an mbarrier with
+// the bounded wait; a wait that gives up makes the chunk sums NaN, and the
+// request reports SV_STATUS_TIMEOUT. Requires 16-byte-aligned rows (the base
+// and the row stride) so each chunk starts on a 16-byte boundary; the host
+// uses the three-kernel path otherwise.
+#pragma once
+
+#include "decide.cuh"
+#include "draw.cuh"
+#include "finish.cuh"
+
+namespace sv {
+
+constexpr int kTwCluster = 8;                 // CTAs per request
+constexpr int kTwThreads = 256;
+constexpr int kTwWarps = kTwThreads / 32;
+constexpr int kTwMaxChunks = 6;               // chunks of the drawn row one CTA holds
+constexpr int kTwMaxP = kTwCluster * kTwMaxChunks;
+constexpr int kTwVecs = kK3ChunkBytes / 16;   // 16-byte vectors per chunk
+constexpr int kTwVecsPerThread = kTwVecs / kTwThreads;
+static_assert(kTwVecsPerThread * kTwThreads == kTwVecs, "whole vectors per thread");
+
+// The walk's result, as CTA 0 hands it to the cluster.
+struct TwDraw {
+  int32_t type;     // DrawType
+  int32_t t_row;    // global target row
+  int32_t pos;      // output column
+  int32_t n_excl;   // rejected tokens (masked draw)
+  int32_t status;   // the walk's status bits
+  float u, lp2, scale;
+};
+static_assert(sizeof(TwDraw) == 32, "eight 32-bit words");
+
+struct TwArgs {
+  TreeArgs t;          // tree inputs, outputs, K1 partials, rule, finish step
+  uintptr_t tgt_hi;    // end of the target buffer (bytes)
+  int32_t P;           // chunks per row
+  int32_t chunk_elems;
+  int32_t nch;         // chunks per CTA: ceil(P / kTwCluster)
+};
+
+// ------------------------------------------------ cluster / distributed shared memory
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster(uint32_t addr, float v) { st_cluster(addr, __float_as_uint(v)); }
+
+// Cluster-wide barrier: every thread of every CTA arrives (release: its
+// earlier stores, shared and global, become visible to the waiters) and
+// waits (acquire).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Dynamic shared-memory layout for N nodes and nch chunks per CTA (the host
+// sizes the launch with the same function).
+struct TwLayout {
+  uint32_t m, l2, g, u, lp, racc, xp, am, tok, par, first, next, bad, excl, slots, chunks, total;
+};
+
+__host__ __device__ constexpr uint32_t tw_align(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline TwLayout tw_layout(int N, int nch) {
+  TwLayout L{};
+  const uint32_t n4 = tw_align(static_cast<uint32_t>(N), 4) * 4u;   // one 32-bit word per node
+  uint32_t o = 0;
+  L.m = o;     o += n4;
+  L.l2 = o;    o += n4;
+  L.g = o;     o += n4;
+  L.u = o;     o += n4;
+  L.lp = o;    o += n4;
+  L.racc = o;  o += n4;
+  L.xp = o;    o += n4;
+  L.am = o;    o += n4;
+  L.tok = o;   o += n4;
+  L.par = o;   o += n4;
+  L.first = o; o += n4;
+  L.next = o;  o += n4;
+  L.bad = o;   o += n4;
+  L.excl = o;  o += n4;
+  o = tw_align(o, 16);
+  L.slots = o; o += static_cast<uint32_t>(kStageSlots * sizeof(Partial));
+  o = tw_align(o, 128);
+  L.chunks = o; o += static_cast<uint32_t>(nch) * kK3ChunkBytes;
+  L.total = o;
+  return L;
+}
+
+template <int ES>
+__global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
+    tree_walk_draw_kernel(const TwArgs w) {
+  constexpr int NV = Elem<ES>::kVec;   // elements per 16-byte vector
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t s_bar;           // the chunk copies
+  __shared__ TwDraw s_draw;                          // CTA 0 stores it into every CTA
+  __shared__ float2 s_csum[kTwMaxP];                 // (sum w, sum p) per chunk, in every CTA
+  __shared__ float s_red[kTwMaxChunks][kTwWarps];    // warp sums of w per local chunk
+  __shared__ float s_scan[kTwVecsPerThread][kTwWarps];
+  __shared__ int s_stop[kMaxStopIds];
+  __shared__ FinishPre fpre;
+  __shared__ int s_fin[2];
+  __shared__ int s_err, s_pick, s_lastpos, s_chunk, s_usep, s_link;
+  __shared__ float s_thr, s_S;
+
+  const TreeArgs& a = w.t;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const int b = static_cast<int>(blockIdx.x) / kTwCluster;
+  const int N = a.N, W = a.max_depth + 1;
+  const float c = a.c;
+  const TwLayout L = tw_layout(N, w.nch);
+  float* sm_m = reinterpret_cast<float*>(smem + L.m);       // row max
+  float* sm_l2 = reinterpret_cast<float*>(smem + L.l2);     // row lse, log2 domain
+  float* sm_g = reinterpret_cast<float*>(smem + L.g);       // node token's logit in its parent's row
+  float* sm_u = reinterpret_cast<float*>(smem + L.u);       // node's uniform
+  float* sm_lp = reinterpret_cast<float*>(smem + L.lp);     // node token's log2 p in its parent's row
+  float* sm_racc = reinterpret_cast<float*>(smem + L.racc); // relaxed rule: the node's acceptance (0 / 1)
+  float* sm_xp = reinterpret_cast<float*>(smem + L.xp);     // p of each rejected token (draw masking)
+  int* sm_am = reinterpret_cast<int*>(smem + L.am);         // row argmax
+  int* sm_tok = reinterpret_cast<int*>(smem + L.tok);
+  int* sm_par = reinterpret_cast<int*>(smem + L.par);       // -1 for the root and bad links
+  int* sm_first = reinterpret_cast<int*>(smem + L.first);   // first child
+  int* sm_next = reinterpret_cast<int*>(smem + L.next);     // next sibling
+  int* sm_bad = reinterpret_cast<int*>(smem + L.bad);       // row not finite / timed out
+  int* s_excl = reinterpret_cast<int*>(smem + L.excl);      // rejected tokens of the draw's node
+  Partial* s_slots = reinterpret_cast<Partial*>(smem + L.slots);
+  uint8_t* chunks = smem + L.chunks;
+
+  cluster_arrive_relaxed();   // barrier 0: this CTA has started (awaited before any remote store)
+  if (tid == 0) {
+    s_err = 0;
+    s_link = 0;
+    mbar_init(smem_u32(&s_bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Call inputs (CTA 0 walks): links, tokens, uniforms and the gathered logits.
+  if (rank == 0) {
+    for (int n = tid; n < N; n += kTwThreads) {
+      const int64_t row = static_cast<int64_t>(b) * N + n;
+      const int par = a.parents[row];
+      const int tok = a.tokens[row];
+      const bool link_ok = (n == 0) ? (par == -1) : (par >= 0 && par < n);
+      if (!link_ok) atomicOr(&s_link, SV_STATUS_BAD_PARENT);
+      const int p = (n > 0 && link_ok) ? par : -1;
+      sm_par[n] = p;
+      sm_tok[n] = tok;
+      sm_u[n] = a.uniforms[row];
+      float gl = -INFINITY;
+      if (p >= 0 && tok >= 0 && tok < a.V)
+        gl = Elem<ES>::load(a.tgt + (static_cast<int64_t>(b) * N + p) * a.tgt_stride, tok);
+      sm_g[n] = gl;
+      sm_first[n] = -1;
+    }
+  }
+  finish_prefetch(a.fin, b, s_stop, fpre);
+  __syncthreads();
+  if (rank == 0 && tid == 0) {
+    for (int n = N - 1; n >= 1; --n) {   // reverse insertion: lists in increasing index
+      const int p = sm_par[n];
+      if (p >= 0) {
+        sm_next[n] = sm_first[p];
+        sm_first[p] = n;
+      }
+    }
+  }
+
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // ---- 1. this CTA's rows: staged merge, statistics into CTA 0
+  const int per = (N + kTwCluster - 1) / kTwCluster;
+  const int n0 = min(N, static_cast<int>(rank) * per), n1 = min(N, n0 + per);
+  const int64_t rb = static_cast<int64_t>(b) * N;
+  SlotRange sr;
+  sr.lo = 0;
+  sr.n = 0;
+  bool staged = false;
+  if (n1 > n0) {
+    sr = slot_range(rb + n0, rb + n1 - 1, a.V, a.T, a.G);
+    staged = sr.n <= kStageSlots;
+    if (staged) {
+      SlotRange none;
+      none.lo = 0;
+      none.n = 0;
+      stage_slots(a.part, sr, s_slots, none, nullptr, c);
+    }
+  }
+  __syncthreads();
+  cluster_wait();   // barrier 0: every CTA of the cluster runs
+  for (int n = n0 + tid; n < n1; n += kTwThreads) {
+    float m, s;
+    int idx, err;
+    if (staged) merge_row_staged(s_slots, sr, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
+    else merge_row_serial(a.part, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
+    const int bad = ((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? SV_STATUS_NONFINITE_ROW : 0) |
+                    (err ? SV_STATUS_TIMEOUT : 0);
+    st_cluster(map_rank(smem_u32(sm_m + n), 0), m);
+    st_cluster(map_rank(smem_u32(sm_l2 + n), 0), m * c + log2f(s));
+    st_cluster(map_rank(smem_u32(sm_am + n), 0), static_cast<uint32_t>(idx));
+    st_cluster(map_rank(smem_u32(sm_bad + n), 0), static_cast<uint32_t>(bad));
+  }
+  cluster_sync();   // barrier 1: CTA 0 holds every row's statistics
+
+  // ---- 2. CTA 0: every node's log2 p (and relaxed acceptance), then the walk
+  if (rank == 0) {
+    for (int n = tid; n < N; n += kTwThreads) {
+      const int p = sm_par[n];
+      const float lp2 = p >= 0 ? sm_g[n] * c - sm_l2[p] : -INFINITY;
+      sm_lp[n] = lp2;
+      if (a.rule.rule == 1 && p >= 0) {
+        const float thr = a.rule.thr ? a.rule.thr[rb + p] : INFINITY;
+        sm_racc[n] = relaxed_accepts(a.rule, lp2, sm_g[n], thr) ? 1.f : 0.f;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int status = s_link;
+      int cur = 0, depth = 0;
+      const int64_t ob = static_cast<int64_t>(b) * W;
+      TwDraw d;
+      while (true) {
+        a.out_nodes[ob + depth] = cur;
+        status |= sm_bad[cur];
+        int kid = sm_first[cur];
+        if (depth == a.max_depth && kid >= 0) {
+          status |= SV_STATUS_DEPTH_EXCEEDED;
+          kid = -1;
+        }
+        // rest = 1 - (rejected mass) as an unevaluated fp32 sum rest_hi + rest_lo
+        float rest_hi = 1.f, rest_lo = 0.f, reach = 1.f;
+        int nrej = 0, accepted = -1;
+        for (; kid >= 0; kid = sm_next[kid]) {
+          const int t = sm_tok[kid];
+          float acc = 0.f;
+          float lp2 = -INFINITY;
+          bool counted = false;
+          if (t < 0 || t >= a.V) {
+            status |= SV_STATUS_BAD_TOKEN;
+          } else {
+            bool dup = false;
+            for (int r = 0; r < nrej; ++r) dup |= (s_excl[r] == t);
+            if (!dup) {
+              counted = true;
+              lp2 = sm_lp[kid];
+              const float p = ex2(lp2);
+              if (a.rule.rule == 1) {
+                acc = sm_racc[kid];
+              } else {
+                const float rest = rest_hi + rest_lo;
+                const float ratio = rest <= 0.f ? 1.f : fminf(1.f, p / rest);
+                acc = (a.rule.rule == 2) ? exp2f(a.rule.alpha * log2f(ratio)) : ratio;
+              }
+              two_sum_sub(rest_hi, rest_lo, p);
+            }
+          }
+          if (sm_u[kid] < acc) {
+            accepted = kid;
+            a.out_tokens[ob + depth] = t;
+            if (a.out_logprob) a.out_logprob[ob + depth] = lp2 * kLn2;
+            if (a.out_mu) a.out_mu[ob + depth] = reach * acc;
+            break;
+          }
+          reach *= (1.f - acc);
+          if (counted) s_excl[nrej++] = t;
+        }
+        if (accepted >= 0) {
+          cur = accepted;
+          ++depth;
+          continue;
+        }
+        d.type = nrej > 0 ? kDrawMaskedP : kDrawP;
+        d.t_row = static_cast<int32_t>(rb + cur);
+        d.pos = depth;
+        d.n_excl = nrej;
+        d.u = sm_u[0];
+        d.lp2 = sm_l2[cur];
+        d.scale = reach;
+        break;
+      }
+      a.out_num[b] = depth;
+      for (int j = depth + 1; j < W; ++j) {
+        a.out_tokens[ob + j] = -1;
+        a.out_nodes[ob + j] = -1;
+        if (a.out_logprob) a.out_logprob[ob + j] = 0.f;
+        if (a.out_mu) a.out_mu[ob + j] = 0.f;
+      }
+      d.status = status;
+      s_draw = d;
+    }
+    __syncthreads();
+    // The draw and the rejected tokens into the other CTAs.
+    const int nw = 8 + s_draw.n_excl;
+    const uint32_t* dw = reinterpret_cast<const uint32_t*>(&s_draw);
+    for (int q = tid; q < (kTwCluster - 1) * nw; q += kTwThreads) {
+      const int dst = 1 + q / nw, k = q - (q / nw) * nw;
+      if (k < 8) st_cluster(map_rank(smem_u32(dw + k), dst), dw[k]);
+      else st_cluster(map_rank(smem_u32(s_excl + (k - 8)), dst), static_cast<uint32_t>(s_excl[k - 8]));
+    }
+  }
+  cluster_sync();   // barrier 2: every CTA holds the draw
+
+  // ---- 3. this CTA's chunks of the drawn row: copy, mask, sum
+  const TwDraw d = s_draw;
+  const int ce = w.chunk_elems;
+  const int k0 = static_cast<int>(rank) * w.nch;
+  const int nloc = max(0, min(w.P, k0 + w.nch) - k0);
+  const uint8_t* trow = a.tgt + static_cast<int64_t>(d.t_row) * a.tgt_stride;
+  // Bytes copied for local chunk ci: the chunk rounded up to whole vectors,
+  // cut back to whole vectors inside the buffer at its very end.
+  auto copy_bytes = [&](int ci) -> uint32_t {
+    const int lo = (k0 + ci) * ce, hi = min(a.V, lo + ce);
+    const uintptr_t src = reinterpret_cast<uintptr_t>(trow) + static_cast<uintptr_t>(lo) * ES;
+    uint32_t nb = static_cast<uint32_t>(((hi - lo) * ES + 15) & ~15);
+    if (src + nb > w.tgt_hi) nb = static_cast<uint32_t>((w.tgt_hi - src) & ~static_cast<uintptr_t>(15));
+    return nb;
+  };
+  if (tid == 0) {
+    uint32_t total = 0;
+    for (int ci = 0; ci < nloc; ++ci) total += copy_bytes(ci);
+    const uint32_t bar = smem_u32(&s_bar);
+    mbar_arrive_expect_tx(bar, total);
+    for (int ci = 0; ci < nloc; ++ci) {
+      const uint32_t nb = copy_bytes(ci);
+      if (nb) bulk_g2s(smem_u32(chunks + ci * kK3ChunkBytes), trow + static_cast<int64_t>(k0 + ci) * ce * ES, nb, bar);
+    }
+  }
+  if (!mbar_wait_bounded(smem_u32(&s_bar), 0)) atomicOr(&s_err, 1);
+  // Elements a cut-back copy left out (from global memory), and -inf past the
+  // row's end up to the vector boundary (a full copy brought the next row's
+  // first elements or the stride's padding there).
+  for (int ci = 0; ci < nloc; ++ci) {
+    const int lo = (k0 + ci) * ce, hi = min(a.V, lo + ce);
+    const int got = static_cast<int>(copy_bytes(ci)) / ES;
+    const int vend = (hi - lo + NV - 1) / NV * NV;
+    const int j = min(got, hi - lo) + tid;
+    if (j < vend) {
+      uint8_t* e = chunks + ci * kK3ChunkBytes + j * ES;
+      if constexpr (ES == 4) {
+        *reinterpret_cast<float*>(e) = lo + j < hi ? Elem<4>::load(trow, lo + j) : -INFINITY;
+      } else {
+        *reinterpret_cast<unsigned short*>(e) =
+            lo + j < hi ? __ldg(reinterpret_cast<const unsigned short*>(trow) + lo + j) : static_cast<unsigned short>(0xff80u);
+      }
+    }
+  }
+  __syncthreads();
+  // Rejected tokens: their p (for the unmasked sums), then -inf in the copy.
+  const int nex = d.type == kDrawMaskedP ? d.n_excl : 0;
+  const int lo_cta = k0 * ce, hi_cta = min(a.V, (k0 + nloc) * ce);
+  for (int e = tid; e < nex; e += kTwThreads) {
+    const int t = s_excl[e];
+    float xp = 0.f;
+    if (t >= lo_cta && t < hi_cta) {
+      uint8_t* el = chunks + ((t - lo_cta) / ce) * kK3ChunkBytes + ((t - lo_cta) % ce) * ES;
+      float x;
+      if constexpr (ES == 4) {
+        x = *reinterpret_cast<float*>(el);
+        *reinterpret_cast<float*>(el) = -INFINITY;
+      } else {
+        x = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<unsigned short*>(el)) << 16);
+        *reinterpret_cast<unsigned short*>(el) = static_cast<unsigned short>(0xff80u);
+      }
+      xp = ex2(fmaf(x, c, -d.lp2));
+    }
+    sm_xp[e] = xp;
+  }
+  __syncthreads();
+  // Per-chunk sums of w (the masked copy): vectors tid, tid + 256, ...
+  {
+    float sw[kTwMaxChunks];
+#pragma unroll
+    for (int ci = 0; ci < kTwMaxChunks; ++ci) {
+      sw[ci] = 0.f;
+      if (ci < nloc) {
+        const int lo = (k0 + ci) * ce, hi = min(a.V, lo + ce);
+        const int nvec = (hi - lo + NV - 1) / NV;
+        const uint4* cv = reinterpret_cast<const uint4*>(chunks + ci * kK3ChunkBytes);
+#pragma unroll
+        for (int i = 0; i < kTwVecsPerThread; ++i) {
+          const int v = i * kTwThreads + tid;
+          if (v < nvec) {
+            float x[NV];
+            Elem<ES>::unpack(cv[v], x);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) sw[ci] += ex2(fmaf(x[e], c, -d.lp2));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sw[ci] += __shfl_xor_sync(0xffffffffu, sw[ci], o);
+      if (lane == 0 && ci < nloc) s_red[ci][warp] = sw[ci];
+    }
+  }
+  __syncthreads();
+  if (tid < nloc) {
+    const int ci = tid;
+    const int lo = (k0 + ci) * ce, hi = lo + ce;
+    float cw = 0.f, xp = 0.f;
+#pragma unroll
+    for (int q = 0; q < kTwWarps; ++q) cw += s_red[ci][q];
+    for (int e = 0; e < nex; ++e) {
+      const int t = s_excl[e];
+      if (t >= lo && t < hi) xp += sm_xp[e];
+    }
+    float2 v = make_float2(cw, cw + xp);
+    if (s_err) v = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+    const uint32_t addr = smem_u32(&s_csum[k0 + ci]);
+#pragma unroll
+    for (int r = 0; r < kTwCluster; ++r) {
+      const uint32_t ra = map_rank(addr, r);
+      st_cluster(ra, v.x);
+      st_cluster(ra + 4, v.y);
+    }
+  }
+  cluster_sync();   // barrier 3: every CTA holds every chunk's sums
+
+  // ---- 4. the chunk holding u * S (every CTA finds the same one)
+  if (warp == 0) {
+    float sw = 0.f, sp = 0.f;
+    for (int k = lane; k < w.P; k += 32) {
+      sw += s_csum[k].x;
+      sp += s_csum[k].y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sw += __shfl_xor_sync(0xffffffffu, sw, o);
+      sp += __shfl_xor_sync(0xffffffffu, sp, o);
+    }
+    const int usep = !(sw > 0.f);
+    const float S = usep ? sp : sw;
+    const float thr = d.u * S;
+    float run = 0.f, pre = 0.f, pre_last = 0.f;
+    int cstar = -1, last_pos = -1;
+    for (int base = 0; base < w.P; base += 32) {
+      const int k = base + lane;
+      const float wk = k < w.P ? (usep ? s_csum[k].y : s_csum[k].x) : 0.f;
+      float incl = wk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const float excl = run + (incl - wk);
+      const unsigned hit = __ballot_sync(0xffffffffu, k < w.P && excl + wk > thr);
+      if (cstar < 0 && hit) {
+        const int l = __ffs(hit) - 1;
+        cstar = base + l;
+        pre = __shfl_sync(0xffffffffu, excl, l);
+      }
+      const unsigned pos = __ballot_sync(0xffffffffu, k < w.P && wk > 0.f);
+      if (pos) {   // last chunk with weight so far (the fallback when rounding leaves no crossing)
+        const int l = 31 - __clz(pos);
+        last_pos = base + l;
+        pre_last = __shfl_sync(0xffffffffu, excl, l);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (cstar < 0) {
+      cstar = last_pos >= 0 ? last_pos : w.P - 1;
+      pre = last_pos >= 0 ? pre_last : 0.f;
+    }
+    if (lane == 0) {
+      s_chunk = cstar;
+      s_usep = usep | (S == S ? 0 : 2);   // bit 1: a chunk sum was NaN (a wait gave up)
+      s_thr = thr - pre;
+      s_S = S;
+      s_pick = INT_MAX;
+      s_lastpos = -1;
+    }
+  }
+  // a copy that a given-up wait left in flight lands before the CTA exits
+  if (s_err && tid == 0) (void)mbar_wait_bounded(smem_u32(&s_bar), 0);
+  __syncthreads();
+  const int cstar = s_chunk;
+  if (cstar < k0 || cstar >= k0 + nloc) return;   // another CTA holds the drawn chunk
+
+  // ---- 5. the owner: block scan of the chunk in index order
+  const int ci = cstar - k0;
+  const int lo = cstar * ce, hi = min(a.V, lo + ce);
+  const int nvec = (hi - lo + NV - 1) / NV;
+  const int usep = s_usep & 1;
+  const float thr = s_thr;
+  uint8_t* cs = chunks + ci * kK3ChunkBytes;
+  if (usep && nex) {   // drawing from p: the rejected tokens count again
+    for (int e = tid; e < nex; e += kTwThreads) {
+      const int t = s_excl[e];
+      if (t >= lo && t < hi) {
+        if constexpr (ES == 4) reinterpret_cast<float*>(cs)[t - lo] = Elem<4>::load(trow, t);
+        else reinterpret_cast<unsigned short*>(cs)[t - lo] = __ldg(reinterpret_cast<const unsigned short*>(trow) + t);
+      }
+    }
+    __syncthreads();
+  }
+  // Thread t holds vectors t, t + 256, t + 512, t + 768: four interleaved
+  // sequences, each scanned over the block; vector v = i * 256 + t starts at
+  // element lo + v * NV.
+  const uint4* cv = reinterpret_cast<const uint4*>(cs);
+  float wv[kTwVecsPerThread][NV];
+  float av[kTwVecsPerThread];
+  int lastpos = -1;
+#pragma unroll
+  for (int i = 0; i < kTwVecsPerThread; ++i) {
+    const int v = i * kTwThreads + tid;
+    av[i] = 0.f;
+    if (v < nvec) {
+      float x[NV];
+      Elem<ES>::unpack(cv[v], x);
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        wv[i][e] = ex2(fmaf(x[e], c, -d.lp2));
+        av[i] += wv[i][e];
+        if (wv[i][e] > 0.f) lastpos = lo + v * NV + e;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < NV; ++e) wv[i][e] = 0.f;
+    }
+  }
+  float incl[kTwVecsPerThread];
+#pragma unroll
+  for (int i = 0; i < kTwVecsPerThread; ++i) incl[i] = av[i];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < kTwVecsPerThread; ++i) {
+      const float t = __shfl_up_sync(0xffffffffu, incl[i], o);
+      if (lane >= o) incl[i] += t;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < kTwVecsPerThread; ++i) s_scan[i][warp] = incl[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // per sequence: exclusive prefix over the warps, plus the totals of the
+    // sequences before it
+    float base = 0.f;
+#pragma unroll
+    for (int i = 0; i < kTwVecsPerThread; ++i) {
+      const float t = lane < kTwWarps ? s_scan[i][lane] : 0.f;
+      float ti = t;
+#pragma unroll
+      for (int o = 1; o < kTwWarps; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, ti, o);
+        if (lane >= o) ti += u;
+      }
+      const float tot = __shfl_sync(0xffffffffu, ti, kTwWarps - 1);
+      __syncwarp();
+      if (lane < kTwWarps) s_scan[i][lane] = base + (ti - t);
+      base += tot;
+    }
+  }
+  __syncthreads();
+  float ex[kTwVecsPerThread];
+#pragma unroll
+  for (int i = 0; i < kTwVecsPerThread; ++i) {
+    ex[i] = s_scan[i][warp] + (incl[i] - av[i]);
+    if (ex[i] + av[i] > thr && av[i] > 0.f) atomicMin(&s_pick, i * kTwThreads + tid);
+  }
+  if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
+  __syncthreads();
+  // The thread holding the drawn element: the crossing, else the last
+  // element with weight, else the chunk's last element.
+  int j_out = -1;
+  float x_out = 0.f;
+  const int pick = s_pick;
+  if (pick != INT_MAX) {
+    if (pick % kTwThreads == tid) {
+      const int ip = pick / kTwThreads;
+#pragma unroll
+      for (int i = 0; i < kTwVecsPerThread; ++i) {
+        if (i == ip) {
+          float part = 0.f;
+          int last_here = -1;
+          bool found = false;
+#pragma unroll
+          for (int e = 0; e < NV; ++e) {
+            part += wv[i][e];
+            if (wv[i][e] > 0.f) last_here = e;
+            if (!found && ex[i] + part > thr && wv[i][e] > 0.f) {
+              j_out = e;
+              found = true;
+            }
+          }
+          if (!found) j_out = last_here;   // rounding left no crossing inside the vector
+          j_out = lo + pick * NV + j_out;
+        }
+      }
+    }
+  } else {
+    const int jf = s_lastpos >= 0 ? s_lastpos : hi - 1;
+    if (((jf - lo) / NV) % kTwThreads == tid) j_out = jf;
+  }
+  if (j_out >= 0) {
+    if (j_out - lo < nvec * NV) {
+      if constexpr (ES == 4) x_out = reinterpret_cast<const float*>(cs)[j_out - lo];
+      else x_out = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(cs)[j_out - lo]) << 16);
+    }
+    if (x_out == -INFINITY) x_out = Elem<ES>::load(trow, j_out);   // a masked element (no weight anywhere)
+    const float p = ex2(fmaf(x_out, c, -d.lp2));
+    const int64_t o = static_cast<int64_t>(b) * W + d.pos;
+    a.out_tokens[o] = j_out;
+    if (a.out_logprob) a.out_logprob[o] = (x_out * c - d.lp2) * kLn2;
+    if (a.out_mu) a.out_mu[o] = d.type == kDrawMaskedP ? d.scale * p / s_S : p;
+    if (a.out_status) a.out_status[b] = d.status | ((s_usep & 2) ? kStatusWaitErr : 0);
+  }
+  if (a.fin.out_len) {   // this kernel ends the call
+    __syncthreads();
+    finish_request(a.fin, fpre, s_stop, b, d.pos, W, a.out_tokens, a.out_logprob, a.out_mu, a.out_nodes,
+                   a.out_status, s_fin);
+  }
+}
+
+}  // namespace sv
