@@ -87,6 +87,10 @@ __device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
 
 __device__ __forceinline__ void st_cluster(uint32_t addr, float v) { st_cluster(addr, __float_as_uint(v)); }
 
+__device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
 // Cluster-wide barrier: every thread of every CTA arrives (release: its
 // earlier stores, shared and global, become visible to the waiters) and
 // waits (acquire).
@@ -103,7 +107,7 @@ __device__ __forceinline__ void cluster_sync() {
 // Dynamic shared-memory layout for N nodes and nch chunks per CTA (the host
 // sizes the launch with the same function).
 struct TwLayout {
-  uint32_t m, l2, g, u, lp, racc, xp, am, tok, par, first, next, bad, excl, slots, chunks, total;
+  uint32_t m, l2, g, u, lp, racc, xp, am, tok, par, first, next, bad, excl, slots, vsum, chunks, total;
 };
 
 __host__ __device__ constexpr uint32_t tw_align(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -128,6 +132,7 @@ __host__ __device__ inline TwLayout tw_layout(int N, int nch) {
   L.excl = o;  o += n4;
   o = tw_align(o, 16);
   L.slots = o; o += static_cast<uint32_t>(kStageSlots * sizeof(Partial));
+  L.vsum = o;  o += static_cast<uint32_t>(nch) * kTwVecs * 4u;   // weight sum of each 16-byte vector
   o = tw_align(o, 128);
   L.chunks = o; o += static_cast<uint32_t>(nch) * kK3ChunkBytes;
   L.total = o;
@@ -135,7 +140,7 @@ __host__ __device__ inline TwLayout tw_layout(int N, int nch) {
 }
 
 template <int ES>
-__global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
+__global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads, 1)
     tree_walk_draw_kernel(const TwArgs w) {
   constexpr int NV = Elem<ES>::kVec;   // elements per 16-byte vector
   extern __shared__ __align__(128) uint8_t smem[];
@@ -143,11 +148,13 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
   __shared__ TwDraw s_draw;                          // CTA 0 stores it into every CTA
   __shared__ float2 s_csum[kTwMaxP];                 // (sum w, sum p) per chunk, in every CTA
   __shared__ float s_red[kTwMaxChunks][kTwWarps];    // warp sums of w per local chunk
-  __shared__ float s_scan[kTwVecsPerThread][kTwWarps];
+  __shared__ float s_wsum[kTwWarps];                 // the owner's block scan: warp totals
   __shared__ int s_stop[kMaxStopIds];
   __shared__ FinishPre fpre;
   __shared__ int s_fin[2];
-  __shared__ int s_err, s_pick, s_lastpos, s_chunk, s_usep, s_link;
+  __shared__ int s_cand[kTwWarps];                   // first crossing thread per warp
+  __shared__ int s_wlast[kTwWarps];                  // last thread with weight per warp
+  __shared__ int s_err, s_chunk, s_usep, s_link;
   __shared__ float s_thr, s_S;
 
   const TreeArgs& a = w.t;
@@ -172,6 +179,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
   int* sm_bad = reinterpret_cast<int*>(smem + L.bad);       // row not finite / timed out
   int* s_excl = reinterpret_cast<int*>(smem + L.excl);      // rejected tokens of the draw's node
   Partial* s_slots = reinterpret_cast<Partial*>(smem + L.slots);
+  float* s_vsum = reinterpret_cast<float*>(smem + L.vsum);   // [nch][kTwVecs]
   uint8_t* chunks = smem + L.chunks;
 
   cluster_arrive_relaxed();   // barrier 0: this CTA has started (awaited before any remote store)
@@ -414,7 +422,8 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
     sm_xp[e] = xp;
   }
   __syncthreads();
-  // Per-chunk sums of w (the masked copy): vectors tid, tid + 256, ...
+  // Per-vector and per-chunk sums of w (the masked copy): vectors tid,
+  // tid + 256, ... (the vector sums stay for the pick)
   {
     float sw[kTwMaxChunks];
 #pragma unroll
@@ -427,12 +436,15 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
 #pragma unroll
         for (int i = 0; i < kTwVecsPerThread; ++i) {
           const int v = i * kTwThreads + tid;
+          float av = 0.f;
           if (v < nvec) {
             float x[NV];
             Elem<ES>::unpack(cv[v], x);
 #pragma unroll
-            for (int e = 0; e < NV; ++e) sw[ci] += ex2(fmaf(x[e], c, -d.lp2));
+            for (int e = 0; e < NV; ++e) av += ex2(fmaf(x[e], c, -d.lp2));
           }
+          s_vsum[ci * kTwVecs + v] = av;
+          sw[ci] += av;
         }
       }
 #pragma unroll
@@ -441,8 +453,8 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
     }
   }
   __syncthreads();
-  if (tid < nloc) {
-    const int ci = tid;
+  if (tid < nloc * kTwCluster) {   // thread (chunk ci, destination CTA r)
+    const int ci = tid / kTwCluster, r = tid - ci * kTwCluster;
     const int lo = (k0 + ci) * ce, hi = lo + ce;
     float cw = 0.f, xp = 0.f;
 #pragma unroll
@@ -453,68 +465,62 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
     }
     float2 v = make_float2(cw, cw + xp);
     if (s_err) v = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
-    const uint32_t addr = smem_u32(&s_csum[k0 + ci]);
-#pragma unroll
-    for (int r = 0; r < kTwCluster; ++r) {
-      const uint32_t ra = map_rank(addr, r);
-      st_cluster(ra, v.x);
-      st_cluster(ra + 4, v.y);
-    }
+    st_cluster(map_rank(smem_u32(&s_csum[k0 + ci]), r), v);
   }
   cluster_sync();   // barrier 3: every CTA holds every chunk's sums
 
-  // ---- 4. the chunk holding u * S (every CTA finds the same one)
+  // ---- 4. the chunk holding u * S (every CTA finds the same one). Lane l
+  // holds chunks l and l + 32; inclusive scans of the chunk sums give the
+  // totals and the crossing together.
   if (warp == 0) {
-    float sw = 0.f, sp = 0.f;
-    for (int k = lane; k < w.P; k += 32) {
-      sw += s_csum[k].x;
-      sp += s_csum[k].y;
-    }
+    const float2 c0 = lane < w.P ? s_csum[lane] : make_float2(0.f, 0.f);
+    const float2 c1 = lane + 32 < w.P ? s_csum[lane + 32] : make_float2(0.f, 0.f);
+    float iw0 = c0.x, ip0 = c0.y, iw1 = c1.x, ip1 = c1.y;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      sw += __shfl_xor_sync(0xffffffffu, sw, o);
-      sp += __shfl_xor_sync(0xffffffffu, sp, o);
+    for (int o = 1; o < 32; o <<= 1) {
+      const float a0 = __shfl_up_sync(0xffffffffu, iw0, o), b0 = __shfl_up_sync(0xffffffffu, ip0, o);
+      const float a1 = __shfl_up_sync(0xffffffffu, iw1, o), b1 = __shfl_up_sync(0xffffffffu, ip1, o);
+      if (lane >= o) {
+        iw0 += a0;
+        ip0 += b0;
+        iw1 += a1;
+        ip1 += b1;
+      }
     }
-    const int usep = !(sw > 0.f);
+    iw1 += __shfl_sync(0xffffffffu, iw0, 31);
+    ip1 += __shfl_sync(0xffffffffu, ip0, 31);
+    const float sw = __shfl_sync(0xffffffffu, iw1, 31), sp = __shfl_sync(0xffffffffu, ip1, 31);
+    const int usep = !(sw > 0.f);   // no mass left after the removals: draw from p
     const float S = usep ? sp : sw;
     const float thr = d.u * S;
-    float run = 0.f, pre = 0.f, pre_last = 0.f;
-    int cstar = -1, last_pos = -1;
-    for (int base = 0; base < w.P; base += 32) {
-      const int k = base + lane;
-      const float wk = k < w.P ? (usep ? s_csum[k].y : s_csum[k].x) : 0.f;
-      float incl = wk;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const float excl = run + (incl - wk);
-      const unsigned hit = __ballot_sync(0xffffffffu, k < w.P && excl + wk > thr);
-      if (cstar < 0 && hit) {
-        const int l = __ffs(hit) - 1;
-        cstar = base + l;
-        pre = __shfl_sync(0xffffffffu, excl, l);
-      }
-      const unsigned pos = __ballot_sync(0xffffffffu, k < w.P && wk > 0.f);
-      if (pos) {   // last chunk with weight so far (the fallback when rounding leaves no crossing)
-        const int l = 31 - __clz(pos);
-        last_pos = base + l;
-        pre_last = __shfl_sync(0xffffffffu, excl, l);
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
+    const float a0 = usep ? c0.y : c0.x, a1 = usep ? c1.y : c1.x;
+    const float i0 = usep ? ip0 : iw0, i1 = usep ? ip1 : iw1;
+    const float x0 = i0 - a0, x1 = i1 - a1;   // exclusive prefixes
+    const unsigned h0 = __ballot_sync(0xffffffffu, lane < w.P && i0 > thr);
+    const unsigned h1 = __ballot_sync(0xffffffffu, lane + 32 < w.P && i1 > thr);
+    const unsigned g0 = __ballot_sync(0xffffffffu, lane < w.P && a0 > 0.f);
+    const unsigned g1 = __ballot_sync(0xffffffffu, lane + 32 < w.P && a1 > 0.f);
+    // the first chunk whose inclusive prefix passes u * S; else (rounding)
+    // the last chunk with weight; else the last chunk
+    int cstar = w.P - 1, half = -1, l = 0;
+    if (h0 | h1) {
+      half = h0 ? 0 : 1;
+      l = __ffs(h0 ? h0 : h1) - 1;
+    } else if (g0 | g1) {
+      half = g1 ? 1 : 0;
+      l = 31 - __clz(g1 ? g1 : g0);
     }
-    if (cstar < 0) {
-      cstar = last_pos >= 0 ? last_pos : w.P - 1;
-      pre = last_pos >= 0 ? pre_last : 0.f;
+    const float pre0 = __shfl_sync(0xffffffffu, x0, l), pre1 = __shfl_sync(0xffffffffu, x1, l);
+    float pre = 0.f;
+    if (half >= 0) {
+      cstar = half * 32 + l;
+      pre = half ? pre1 : pre0;
     }
     if (lane == 0) {
       s_chunk = cstar;
       s_usep = usep | (S == S ? 0 : 2);   // bit 1: a chunk sum was NaN (a wait gave up)
       s_thr = thr - pre;
       s_S = S;
-      s_pick = INT_MAX;
-      s_lastpos = -1;
     }
   }
   // a copy that a given-up wait left in flight lands before the CTA exits
@@ -523,13 +529,21 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
   const int cstar = s_chunk;
   if (cstar < k0 || cstar >= k0 + nloc) return;   // another CTA holds the drawn chunk
 
-  // ---- 5. the owner: block scan of the chunk in index order
+  // ---- 5. the owner: the element of the chunk where u * S falls
   const int ci = cstar - k0;
   const int lo = cstar * ce, hi = min(a.V, lo + ce);
   const int nvec = (hi - lo + NV - 1) / NV;
   const int usep = s_usep & 1;
   const float thr = s_thr;
   uint8_t* cs = chunks + ci * kK3ChunkBytes;
+  const uint4* cv = reinterpret_cast<const uint4*>(cs);
+  float* vs = s_vsum + ci * kTwVecs;
+  auto weights = [&](int v, float (&wv)[NV]) {   // the weights of vector v, in element order
+    float x[NV];
+    Elem<ES>::unpack(cv[v], x);
+#pragma unroll
+    for (int e = 0; e < NV; ++e) wv[e] = ex2(fmaf(x[e], c, -d.lp2));
+  };
   if (usep && nex) {   // drawing from p: the rejected tokens count again
     for (int e = tid; e < nex; e += kTwThreads) {
       const int t = s_excl[e];
@@ -539,113 +553,95 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads)
       }
     }
     __syncthreads();
-  }
-  // Thread t holds vectors t, t + 256, t + 512, t + 768: four interleaved
-  // sequences, each scanned over the block; vector v = i * 256 + t starts at
-  // element lo + v * NV.
-  const uint4* cv = reinterpret_cast<const uint4*>(cs);
-  float wv[kTwVecsPerThread][NV];
-  float av[kTwVecsPerThread];
-  int lastpos = -1;
 #pragma unroll
-  for (int i = 0; i < kTwVecsPerThread; ++i) {
-    const int v = i * kTwThreads + tid;
-    av[i] = 0.f;
-    if (v < nvec) {
-      float x[NV];
-      Elem<ES>::unpack(cv[v], x);
+    for (int i = 0; i < kTwVecsPerThread; ++i) {
+      const int v = i * kTwThreads + tid;
+      float av = 0.f;
+      if (v < nvec) {
+        float wv[NV];
+        weights(v, wv);
 #pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        wv[i][e] = ex2(fmaf(x[e], c, -d.lp2));
-        av[i] += wv[i][e];
-        if (wv[i][e] > 0.f) lastpos = lo + v * NV + e;
+        for (int e = 0; e < NV; ++e) av += wv[e];
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < NV; ++e) wv[i][e] = 0.f;
+      vs[v] = av;
     }
+    __syncthreads();
   }
-  float incl[kTwVecsPerThread];
+  // Thread t holds vectors 4t .. 4t + 3 (index order). Block exclusive scan
+  // of the thread sums; then each thread's running prefix over its four
+  // vectors (the same additions the crossing test below repeats).
+  const float4 q4 = reinterpret_cast<const float4*>(vs)[tid];
+  const float av[kTwVecsPerThread] = {q4.x, q4.y, q4.z, q4.w};
+  float tsum = 0.f;
 #pragma unroll
-  for (int i = 0; i < kTwVecsPerThread; ++i) incl[i] = av[i];
+  for (int k = 0; k < kTwVecsPerThread; ++k) tsum += av[k];
+  float incl = tsum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-    for (int i = 0; i < kTwVecsPerThread; ++i) {
-      const float t = __shfl_up_sync(0xffffffffu, incl[i], o);
-      if (lane >= o) incl[i] += t;
-    }
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
-  if (lane == 31) {
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  float ex = 0.f;
+  for (int q = 0; q < warp; ++q) ex += s_wsum[q];
+  ex += incl - tsum;
+  float run = ex;
 #pragma unroll
-    for (int i = 0; i < kTwVecsPerThread; ++i) s_scan[i][warp] = incl[i];
+  for (int k = 0; k < kTwVecsPerThread; ++k) run += av[k];
+  const unsigned hit = __ballot_sync(0xffffffffu, run > thr && tsum > 0.f);
+  const unsigned pos = __ballot_sync(0xffffffffu, tsum > 0.f);
+  if (lane == 0) {
+    s_cand[warp] = hit ? warp * 32 + __ffs(hit) - 1 : INT_MAX;
+    s_wlast[warp] = pos ? warp * 32 + 31 - __clz(pos) : -1;
   }
   __syncthreads();
-  if (warp == 0) {
-    // per sequence: exclusive prefix over the warps, plus the totals of the
-    // sequences before it
-    float base = 0.f;
+  int pick = INT_MAX, lastt = -1;
 #pragma unroll
-    for (int i = 0; i < kTwVecsPerThread; ++i) {
-      const float t = lane < kTwWarps ? s_scan[i][lane] : 0.f;
-      float ti = t;
-#pragma unroll
-      for (int o = 1; o < kTwWarps; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, ti, o);
-        if (lane >= o) ti += u;
-      }
-      const float tot = __shfl_sync(0xffffffffu, ti, kTwWarps - 1);
-      __syncwarp();
-      if (lane < kTwWarps) s_scan[i][lane] = base + (ti - t);
-      base += tot;
-    }
+  for (int q = 0; q < kTwWarps; ++q) {
+    pick = min(pick, s_cand[q]);
+    lastt = max(lastt, s_wlast[q]);
   }
-  __syncthreads();
-  float ex[kTwVecsPerThread];
-#pragma unroll
-  for (int i = 0; i < kTwVecsPerThread; ++i) {
-    ex[i] = s_scan[i][warp] + (incl[i] - av[i]);
-    if (ex[i] + av[i] > thr && av[i] > 0.f) atomicMin(&s_pick, i * kTwThreads + tid);
-  }
-  if (lastpos >= 0) atomicMax(&s_lastpos, lastpos);
-  __syncthreads();
-  // The thread holding the drawn element: the crossing, else the last
-  // element with weight, else the chunk's last element.
+  // The drawn element: the first whose inclusive prefix passes u * S; with
+  // no crossing (rounding), the last element with weight; else the chunk's
+  // last element.
   int j_out = -1;
-  float x_out = 0.f;
-  const int pick = s_pick;
-  if (pick != INT_MAX) {
-    if (pick % kTwThreads == tid) {
-      const int ip = pick / kTwThreads;
+  if (pick != INT_MAX ? tid == pick : tid == lastt) {
+    const bool cross = pick != INT_MAX;
+    float r = ex;
+    int ksel = -1;
 #pragma unroll
-      for (int i = 0; i < kTwVecsPerThread; ++i) {
-        if (i == ip) {
-          float part = 0.f;
-          int last_here = -1;
-          bool found = false;
-#pragma unroll
-          for (int e = 0; e < NV; ++e) {
-            part += wv[i][e];
-            if (wv[i][e] > 0.f) last_here = e;
-            if (!found && ex[i] + part > thr && wv[i][e] > 0.f) {
-              j_out = e;
-              found = true;
-            }
-          }
-          if (!found) j_out = last_here;   // rounding left no crossing inside the vector
-          j_out = lo + pick * NV + j_out;
+    for (int k = 0; k < kTwVecsPerThread; ++k) {
+      if (cross) {
+        if (ksel < 0) {
+          if (r + av[k] > thr && av[k] > 0.f) ksel = k;
+          else r += av[k];
         }
+      } else if (av[k] > 0.f) {
+        ksel = k;
       }
     }
-  } else {
-    const int jf = s_lastpos >= 0 ? s_lastpos : hi - 1;
-    if (((jf - lo) / NV) % kTwThreads == tid) j_out = jf;
+    if (ksel >= 0) {   // always, by construction; guarded for safety
+      const int v = 4 * tid + ksel;
+      float wv[NV];
+      weights(v, wv);
+      float part = 0.f;
+      int e_sel = -1, e_last = -1;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        part += wv[e];
+        if (wv[e] > 0.f) e_last = e;
+        if (cross && e_sel < 0 && r + part > thr && wv[e] > 0.f) e_sel = e;
+      }
+      j_out = lo + v * NV + (e_sel >= 0 ? e_sel : e_last);
+    }
+  } else if (pick == INT_MAX && lastt < 0 && ((hi - 1 - lo) / NV) / kTwVecsPerThread == tid) {
+    j_out = hi - 1;
   }
   if (j_out >= 0) {
-    if (j_out - lo < nvec * NV) {
-      if constexpr (ES == 4) x_out = reinterpret_cast<const float*>(cs)[j_out - lo];
-      else x_out = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(cs)[j_out - lo]) << 16);
-    }
+    float x_out;
+    if constexpr (ES == 4) x_out = reinterpret_cast<const float*>(cs)[j_out - lo];
+    else x_out = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(cs)[j_out - lo]) << 16);
     if (x_out == -INFINITY) x_out = Elem<ES>::load(trow, j_out);   // a masked element (no weight anywhere)
     const float p = ex2(fmaf(x_out, c, -d.lp2));
     const int64_t o = static_cast<int64_t>(b) * W + d.pos;
