@@ -63,6 +63,15 @@ __device__ __forceinline__ bool relaxed_accepts(const RuleArgs& r, float lp2, fl
   return ex2(lp2) >= r.tau || (r.top_k > 0 && x >= thr);
 }
 
+// Tree acceptance of a child with log2 p = lp2 when `rest` of the parent
+// row's mass is left (exact and power rules): min(1, p / rest)^alpha, formed
+// in the log2 domain as 2^(alpha * min(0, lp2 - log2 rest)); rest <= 0 (all
+// mass removed, by rounding) accepts.
+__device__ __forceinline__ float tree_accept(const RuleArgs& r, float lp2, float rest) {
+  const float r2 = rest <= 0.f ? 0.f : fminf(0.f, lp2 - lg2(rest));
+  return ex2(r.rule == 2 ? r.alpha * r2 : r2);
+}
+
 struct ChainArgs {
   const uint8_t* tgt;
   int64_t tgt_stride;    // bytes
@@ -554,9 +563,7 @@ __global__ void __launch_bounds__(kK2Threads) tree_decide_kernel(const TreeArgs 
               const float thr = a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * N + cur] : INFINITY;
               acc = relaxed_accepts(a.rule, lp2, sm_g[kid], thr) ? 1.f : 0.f;
             } else {
-              const float rest = rest_hi + rest_lo;
-              const float ratio = rest <= 0.f ? 1.f : fminf(1.f, p / rest);
-              acc = (a.rule.rule == 2) ? exp2f(a.rule.alpha * log2f(ratio)) : ratio;
+              acc = tree_accept(a.rule, lp2, rest_hi + rest_lo);
             }
             two_sum_sub(rest_hi, rest_lo, p);
           }

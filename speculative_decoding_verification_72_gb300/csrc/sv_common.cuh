@@ -62,6 +62,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// SFU base-2 logarithm (PTX lg2.approx.ftz.f32): absolute error ~2^-22 in
+// the result; +0 -> -inf.
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // --------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

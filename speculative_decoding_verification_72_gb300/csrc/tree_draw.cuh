@@ -107,7 +107,7 @@ __device__ __forceinline__ void cluster_sync() {
 // Dynamic shared-memory layout for N nodes and nch chunks per CTA (the host
 // sizes the launch with the same function).
 struct TwLayout {
-  uint32_t m, l2, g, u, lp, racc, xp, am, tok, par, first, next, bad, excl, slots, vsum, chunks, total;
+  uint32_t m, l2, g, u, lp, p, racc, xp, am, tok, par, first, next, dup, bad, excl, slots, vsum, chunks, total;
 };
 
 __host__ __device__ constexpr uint32_t tw_align(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -121,6 +121,7 @@ __host__ __device__ inline TwLayout tw_layout(int N, int nch) {
   L.g = o;     o += n4;
   L.u = o;     o += n4;
   L.lp = o;    o += n4;
+  L.p = o;     o += n4;
   L.racc = o;  o += n4;
   L.xp = o;    o += n4;
   L.am = o;    o += n4;
@@ -128,6 +129,7 @@ __host__ __device__ inline TwLayout tw_layout(int N, int nch) {
   L.par = o;   o += n4;
   L.first = o; o += n4;
   L.next = o;  o += n4;
+  L.dup = o;   o += n4;
   L.bad = o;   o += n4;
   L.excl = o;  o += n4;
   o = tw_align(o, 16);
@@ -169,6 +171,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
   float* sm_g = reinterpret_cast<float*>(smem + L.g);       // node token's logit in its parent's row
   float* sm_u = reinterpret_cast<float*>(smem + L.u);       // node's uniform
   float* sm_lp = reinterpret_cast<float*>(smem + L.lp);     // node token's log2 p in its parent's row
+  float* sm_p = reinterpret_cast<float*>(smem + L.p);       // 2^lp
   float* sm_racc = reinterpret_cast<float*>(smem + L.racc); // relaxed rule: the node's acceptance (0 / 1)
   float* sm_xp = reinterpret_cast<float*>(smem + L.xp);     // p of each rejected token (draw masking)
   int* sm_am = reinterpret_cast<int*>(smem + L.am);         // row argmax
@@ -176,6 +179,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
   int* sm_par = reinterpret_cast<int*>(smem + L.par);       // -1 for the root and bad links
   int* sm_first = reinterpret_cast<int*>(smem + L.first);   // first child
   int* sm_next = reinterpret_cast<int*>(smem + L.next);     // next sibling
+  int* sm_dup = reinterpret_cast<int*>(smem + L.dup);       // an earlier sibling offers the same token
   int* sm_bad = reinterpret_cast<int*>(smem + L.bad);       // row not finite / timed out
   int* s_excl = reinterpret_cast<int*>(smem + L.excl);      // rejected tokens of the draw's node
   Partial* s_slots = reinterpret_cast<Partial*>(smem + L.slots);
@@ -211,13 +215,25 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
   }
   finish_prefetch(a.fin, b, s_stop, fpre);
   __syncthreads();
-  if (rank == 0 && tid == 0) {
-    for (int n = N - 1; n >= 1; --n) {   // reverse insertion: lists in increasing index
-      const int p = sm_par[n];
-      if (p >= 0) {
-        sm_next[n] = sm_first[p];
-        sm_first[p] = n;
+  if (rank == 0) {
+    if (tid == 0) {
+      for (int n = N - 1; n >= 1; --n) {   // reverse insertion: lists in increasing index
+        const int p = sm_par[n];
+        if (p >= 0) {
+          sm_next[n] = sm_first[p];
+          sm_first[p] = n;
+        }
       }
+    }
+    __syncthreads();
+    // A child whose in-range token an earlier sibling already offered is not
+    // tested again (its token was removed from the parent's row).
+    for (int n = tid; n < N; n += kTwThreads) {
+      const int t = sm_tok[n], p = sm_par[n];
+      int dup = 0;
+      if (p >= 0 && t >= 0 && t < a.V)
+        for (int m = sm_first[p]; m >= 0 && m != n; m = sm_next[m]) dup |= sm_tok[m] == t;
+      sm_dup[n] = dup;
     }
   }
 
@@ -264,6 +280,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
       const int p = sm_par[n];
       const float lp2 = p >= 0 ? sm_g[n] * c - sm_l2[p] : -INFINITY;
       sm_lp[n] = lp2;
+      sm_p[n] = ex2(lp2);
       if (a.rule.rule == 1 && p >= 0) {
         const float thr = a.rule.thr ? a.rule.thr[rb + p] : INFINITY;
         sm_racc[n] = relaxed_accepts(a.rule, lp2, sm_g[n], thr) ? 1.f : 0.f;
@@ -294,20 +311,11 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
           if (t < 0 || t >= a.V) {
             status |= SV_STATUS_BAD_TOKEN;
           } else {
-            bool dup = false;
-            for (int r = 0; r < nrej; ++r) dup |= (s_excl[r] == t);
-            if (!dup) {
+            if (!sm_dup[kid]) {
               counted = true;
               lp2 = sm_lp[kid];
-              const float p = ex2(lp2);
-              if (a.rule.rule == 1) {
-                acc = sm_racc[kid];
-              } else {
-                const float rest = rest_hi + rest_lo;
-                const float ratio = rest <= 0.f ? 1.f : fminf(1.f, p / rest);
-                acc = (a.rule.rule == 2) ? exp2f(a.rule.alpha * log2f(ratio)) : ratio;
-              }
-              two_sum_sub(rest_hi, rest_lo, p);
+              acc = a.rule.rule == 1 ? sm_racc[kid] : tree_accept(a.rule, lp2, rest_hi + rest_lo);
+              two_sum_sub(rest_hi, rest_lo, sm_p[kid]);
             }
           }
           if (sm_u[kid] < acc) {
