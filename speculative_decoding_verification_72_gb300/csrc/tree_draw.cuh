@@ -7,29 +7,29 @@
 // draw_pick_kernel, without their two kernel boundaries and global round
 // trips. A cluster of kTwCluster CTAs serves request b:
 //
-//  1. CTA r merges the K1 partials of rows [r * per, (r + 1) * per) of the
-//     request (per = ceil(N / kTwCluster); the staged merge order of the
-//     decide kernel, so the statistics are the same bits) and stores them
-//     into CTA 0's shared memory (distributed shared memory).
-//  2. Cluster barrier. CTA 0 forms every node's log2 p in parallel, then one
-//     thread walks from the root as the decide kernel does (same arithmetic
-//     and order) and writes the accepted path. The draw descriptor and the
-//     rejected tokens are stored into every CTA's shared memory.
-//  3. Cluster barrier. CTA r copies chunks [r * nch, (r + 1) * nch) of the
+//  1. CTA 0 merges the K1 partials of the request's N rows (the decide
+//     kernel's staged merge, so the statistics are the same bits), forms
+//     every node's log2 p in parallel, and one thread walks from the root as
+//     the decide kernel does (same arithmetic and order), writing the
+//     accepted path. The draw descriptor and the rejected tokens are stored
+//     into every CTA's shared memory (distributed shared memory).
+//  2. Cluster barrier 1. CTA r copies chunks [r * nch, (r + 1) * nch) of the
 //     drawn row (kK3ChunkBytes each, 1-D bulk copies) into its shared memory,
-//     masks the rejected tokens and the row's end with -inf, sums (w, p) per
-//     chunk and stores the sums into every CTA's shared memory.
-//  4. Cluster barrier. Every CTA finds the chunk where u * S falls (the pick
-//     kernel's warp scan over the chunk sums); the CTA holding that chunk
-//     resolves the token with a block scan of its shared-memory copy and
+//     masks the rejected tokens and the row's end with -inf, sums the weights
+//     per 16-byte vector and per chunk, and stores the chunk sums into every
+//     CTA's shared memory.
+//  3. Cluster barrier 2. Every CTA finds the chunk where u * S falls (warp
+//     scans over the chunk sums); the CTA holding that chunk scans its
+//     vector sums, resolves the token inside the crossing vector, and
 //     writes the draw, the status and the finish step.
 //
-// After barrier 3 no CTA touches another's shared memory, so the CTAs not
-// holding the drawn chunk simply exit. The copies wait on an mbarrier with
-// the bounded wait; a wait that gives up makes the chunk sums NaN, and the
-// request reports SV_STATUS_TIMEOUT. Requires 16-byte-aligned rows (the base
-// and the row stride) so each chunk starts on a 16-byte boundary; the host
-// uses the three-kernel path otherwise.
+// After barrier 2 no CTA touches another's shared memory, so the CTAs not
+// holding the drawn chunk simply exit. (Barrier 0, every CTA of the cluster
+// running, precedes the first remote store.) The copies wait on an mbarrier
+// with the bounded wait; a wait that gives up makes the chunk sums NaN, and
+// the request reports SV_STATUS_TIMEOUT. Requires 16-byte-aligned rows (the
+// base and the row stride) so each chunk starts on a 16-byte boundary; the
+// host uses the three-kernel path otherwise.
 #pragma once
 
 #include "decide.cuh"
@@ -240,39 +240,34 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
   grid_dep_wait();
   grid_dep_launch();
 
-  // ---- 1. this CTA's rows: staged merge, statistics into CTA 0
-  const int per = (N + kTwCluster - 1) / kTwCluster;
-  const int n0 = min(N, static_cast<int>(rank) * per), n1 = min(N, n0 + per);
+  cluster_wait();   // barrier 0: every CTA of the cluster runs (before any remote store)
   const int64_t rb = static_cast<int64_t>(b) * N;
-  SlotRange sr;
-  sr.lo = 0;
-  sr.n = 0;
-  bool staged = false;
-  if (n1 > n0) {
-    sr = slot_range(rb + n0, rb + n1 - 1, a.V, a.T, a.G);
-    staged = sr.n <= kStageSlots;
+
+  // ---- 1. CTA 0: the rows' statistics (the decide kernel's staged merge;
+  // the merge is one L2 round trip however many rows a CTA takes)
+  if (rank == 0) {
+    const SlotRange sr = slot_range(rb, rb + N - 1, a.V, a.T, a.G);
+    const bool staged = sr.n <= kStageSlots;
     if (staged) {
       SlotRange none;
       none.lo = 0;
       none.n = 0;
       stage_slots(a.part, sr, s_slots, none, nullptr, c);
+      __syncthreads();
     }
+    for (int n = tid; n < N; n += kTwThreads) {
+      float m, s;
+      int idx, err;
+      if (staged) merge_row_staged(s_slots, sr, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
+      else merge_row_serial(a.part, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
+      sm_m[n] = m;
+      sm_l2[n] = m * c + log2f(s);
+      sm_am[n] = idx;
+      sm_bad[n] = ((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? SV_STATUS_NONFINITE_ROW : 0) |
+                  (err ? SV_STATUS_TIMEOUT : 0);
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  cluster_wait();   // barrier 0: every CTA of the cluster runs
-  for (int n = n0 + tid; n < n1; n += kTwThreads) {
-    float m, s;
-    int idx, err;
-    if (staged) merge_row_staged(s_slots, sr, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
-    else merge_row_serial(a.part, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
-    const int bad = ((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? SV_STATUS_NONFINITE_ROW : 0) |
-                    (err ? SV_STATUS_TIMEOUT : 0);
-    st_cluster(map_rank(smem_u32(sm_m + n), 0), m);
-    st_cluster(map_rank(smem_u32(sm_l2 + n), 0), m * c + log2f(s));
-    st_cluster(map_rank(smem_u32(sm_am + n), 0), static_cast<uint32_t>(idx));
-    st_cluster(map_rank(smem_u32(sm_bad + n), 0), static_cast<uint32_t>(bad));
-  }
-  cluster_sync();   // barrier 1: CTA 0 holds every row's statistics
 
   // ---- 2. CTA 0: every node's log2 p (and relaxed acceptance), then the walk
   if (rank == 0) {
@@ -362,7 +357,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
       else st_cluster(map_rank(smem_u32(s_excl + (k - 8)), dst), static_cast<uint32_t>(s_excl[k - 8]));
     }
   }
-  cluster_sync();   // barrier 2: every CTA holds the draw
+  cluster_sync();   // barrier 1: every CTA holds the draw
 
   // ---- 3. this CTA's chunks of the drawn row: copy, mask, sum
   const TwDraw d = s_draw;
@@ -475,7 +470,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
     if (s_err) v = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
     st_cluster(map_rank(smem_u32(&s_csum[k0 + ci]), r), v);
   }
-  cluster_sync();   // barrier 3: every CTA holds every chunk's sums
+  cluster_sync();   // barrier 2: every CTA holds every chunk's sums
 
   // ---- 4. the chunk holding u * S (every CTA finds the same one). Lane l
   // holds chunks l and l + 32; inclusive scans of the chunk sums give the
