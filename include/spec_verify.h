@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define SPEC_VERIFY_ABI_VERSION 2
+#define SPEC_VERIFY_ABI_VERSION 3
 
 /* Return codes. */
 typedef int32_t sv_status;
@@ -390,6 +390,40 @@ sv_status spec_verify_greedy_static(const void* target_logits, int32_t dtype, in
                                     int32_t* out_tokens, int32_t* out_num_accepted,
                                     float* out_logprob, float* out_mu, int32_t* out_status,
                                     void* stream);
+
+/* Greedy chain verification of logits that sit in HOST memory (the same
+ * verification as spec_verify_greedy, mini-sglang PR #134, verify_drafts;
+ * the transfer schedule is this library's). The requests go to the GPU in
+ * groups of `group` (0: the library picks groups of about
+ * SV_HOST_GROUP_BYTES of logits): group i is copied into one of two device
+ * staging slots on a copy stream of the library's while group i - 1 is
+ * verified on `stream`, and each group's outputs are copied back to the host
+ * outputs on `stream` after its verification. The copy engine then carries
+ * the logits back to back and the kernels run in its shadow.
+ *   target_logits, draft_tokens: host memory, laid out as for
+ *     spec_verify_greedy (request b's K+1 rows contiguous at row b*(K+1)).
+ *     Page-locked (cudaHostAlloc / cudaHostRegister) memory copies at full
+ *     speed; pageable memory works but each copy then blocks the host.
+ *   out_*: host memory, as for spec_verify_greedy (out_logprob, out_mu,
+ *     out_status may be NULL).
+ *   workspace: device memory of spec_verify_greedy_host_workspace_size(B, K,
+ *     V, dtype, group) bytes, 256-byte aligned; nothing in it needs to start
+ *     at zero. Results are the same as spec_verify_greedy's on the same
+ *     groups of requests: tokens, counts and status are identical to a
+ *     single device call; log-probabilities agree to float rounding.
+ * The call returns once the work is enqueued; the host outputs are valid
+ * after `stream` completes (cudaStreamSynchronize). Calls on one device
+ * share the library's copy stream, and each call orders its copies after
+ * the work already enqueued on `stream`. Errors as for spec_verify_greedy;
+ * SV_ERR_CUDA also when the copy stream or an event cannot be created. */
+#define SV_HOST_GROUP_BYTES (256ull << 20)
+size_t spec_verify_greedy_host_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype,
+                                              int32_t group);
+sv_status spec_verify_greedy_host(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                  const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                  int32_t group, int32_t* out_tokens, int32_t* out_num_accepted,
+                                  float* out_logprob, float* out_mu, int32_t* out_status,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -12,5 +12,6 @@ from .verify import (  # noqa: F401
     STATUS_NONFINITE_ROW, STATUS_STOPPED, STATUS_TIMEOUT, STATUS_ZERO_MASS, SV_ERR_TIMEOUT,
     SpecVerifyError, library_path, load_library,
     spec_kv_compact, spec_tree_build, spec_verify_check_status, spec_verify_greedy, spec_verify_greedy_early,
+    spec_verify_greedy_host,
     spec_verify_sample, spec_verify_selftest_wait, spec_verify_tree, spec_verify_workspace_size,
 )

@@ -12,6 +12,7 @@
 // results after it (the top-k kernel waits first, so a wait on it also
 // covers K1).
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -931,6 +932,174 @@ sv_status spec_verify_greedy_static(const void* target_logits, int32_t dtype, in
   return spec_verify_greedy(target_logits, dtype, row_stride, draft_tokens, B, K, V, out_tokens,
                             out_num_accepted, out_logprob, out_mu, out_status, scratch,
                             SV_STATIC_SCRATCH_BYTES, stream);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------- host-resident logits
+//
+// spec_verify_greedy_host: two device staging slots, a copy stream per
+// device (created on first use, kept for the life of the process), and per
+// group of requests: copy (copy stream) -> verify -> outputs back (caller's
+// stream), with the next group's copy enqueued before this group's outputs
+// so the copy engine never waits on the host.
+namespace {
+cudaStream_t g_copy_stream[kMaxDevices] = {nullptr};
+
+cudaStream_t host_copy_stream() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_cache_mu);
+  if (!g_copy_stream[dev]) {
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    g_copy_stream[dev] = s;
+  }
+  return g_copy_stream[dev];
+}
+
+constexpr size_t kHostAlign = 256;
+
+struct HostPlan {
+  int32_t g = 0;   // requests per group
+  size_t slot = 0, off_slot[2] = {0, 0}, off_drafts = 0, off_tok = 0, off_num = 0, off_lp = 0, off_mu = 0,
+         off_st = 0, off_ws = 0, ws_bytes = 0, total = 0;
+};
+
+// Device layout of the host-path workspace: the staging slots hold rows
+// packed at stride V.
+bool host_plan(int32_t B, int32_t K, int32_t V, int32_t dtype, int32_t group, HostPlan* hp) {
+  const int es = elem_size(dtype);
+  if (es == 0 || B < 0 || K < 0 || V < 1 || group < 0) return false;
+  const int64_t R = static_cast<int64_t>(K) + 1;
+  const int64_t req_bytes = R * V * es;
+  int64_t g = group > 0 ? group : static_cast<int64_t>(SV_HOST_GROUP_BYTES) / req_bytes;
+  if (g < 1) g = 1;
+  if (g > B) g = B > 0 ? B : 1;
+  hp->g = static_cast<int32_t>(g);
+  hp->ws_bytes = spec_verify_greedy_workspace_size(hp->g, K, V, dtype);
+  if (hp->ws_bytes == 0) return false;
+  size_t o = 0;
+  hp->slot = align_up(static_cast<size_t>(g * req_bytes), kHostAlign);
+  hp->off_slot[0] = o;
+  o += hp->slot;
+  hp->off_slot[1] = o;
+  o += hp->slot;
+  hp->off_drafts = o;
+  o += align_up(static_cast<size_t>(B) * K * 4, kHostAlign);
+  hp->off_tok = o;
+  o += align_up(static_cast<size_t>(B * R) * 4, kHostAlign);
+  hp->off_num = o;
+  o += align_up(static_cast<size_t>(B) * 4, kHostAlign);
+  hp->off_lp = o;
+  o += align_up(static_cast<size_t>(B * R) * 4, kHostAlign);
+  hp->off_mu = o;
+  o += align_up(static_cast<size_t>(B * R) * 4, kHostAlign);
+  hp->off_st = o;
+  o += align_up(static_cast<size_t>(B) * 4, kHostAlign);
+  hp->off_ws = o;
+  o += align_up(hp->ws_bytes, kHostAlign);
+  hp->total = o;
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_greedy_host_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype, int32_t group) {
+  HostPlan hp;
+  return host_plan(B, K, V, dtype, group, &hp) ? hp.total : 0;
+}
+
+sv_status spec_verify_greedy_host(const void* target_logits, int32_t dtype, int64_t row_stride,
+                                  const int32_t* draft_tokens, int32_t B, int32_t K, int32_t V,
+                                  int32_t group, int32_t* out_tokens, int32_t* out_num_accepted,
+                                  float* out_logprob, float* out_mu, int32_t* out_status,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const int es = elem_size(dtype);
+  if (es == 0) return SV_ERR_UNSUPPORTED_DTYPE;
+  if (B < 0 || K < 0 || V < 1 || row_stride < V || group < 0) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target_logits || (K > 0 && !draft_tokens) || !out_tokens || !out_num_accepted || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (!aligned(target_logits, es) || !aligned(workspace, kHostAlign) || !aligned(draft_tokens, 4) ||
+      !outputs_aligned(out_tokens, out_num_accepted, out_logprob, out_mu, out_status))
+    return SV_ERR_INVALID_ARG;
+  HostPlan hp;
+  if (!host_plan(B, K, V, dtype, group, &hp)) return SV_ERR_INVALID_ARG;
+  if (workspace_bytes < hp.total) return SV_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = host_copy_stream();
+  if (!cs) return SV_ERR_CUDA;
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};   // start, ready[2], done[2]
+  auto fail = [&]() {
+    for (cudaEvent_t e : ev)
+      if (e) cudaEventDestroy(e);   // released once pending work on it completes
+    return SV_ERR_CUDA;
+  };
+  for (cudaEvent_t& e : ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return fail();
+  cudaEvent_t ev_start = ev[0], *ready = ev + 1, *done = ev + 3;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  const int64_t R = static_cast<int64_t>(K) + 1;
+  const int32_t* d_drafts = reinterpret_cast<const int32_t*>(w + hp.off_drafts);
+  int32_t* d_tok = reinterpret_cast<int32_t*>(w + hp.off_tok);
+  int32_t* d_num = reinterpret_cast<int32_t*>(w + hp.off_num);
+  float* d_lp = reinterpret_cast<float*>(w + hp.off_lp);
+  float* d_mu = reinterpret_cast<float*>(w + hp.off_mu);
+  int32_t* d_st = reinterpret_cast<int32_t*>(w + hp.off_st);
+  const int ngroups = static_cast<int>((static_cast<int64_t>(B) + hp.g - 1) / hp.g);
+  const size_t row_bytes = static_cast<size_t>(V) * es;
+  // The copy stream follows the work already on `stream` (earlier users of
+  // the workspace).
+  if (cudaEventRecord(ev_start, st) != cudaSuccess || cudaStreamWaitEvent(cs, ev_start, 0) != cudaSuccess)
+    return fail();
+  if (K > 0 && cudaMemcpyAsync(w + hp.off_drafts, draft_tokens, static_cast<size_t>(B) * K * 4,
+                               cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return fail();
+  // Group i's logits into slot i % 2 once the verification of group i - 2
+  // (the slot's last user) is done.
+  auto copy_group = [&](int i) -> bool {
+    const int s = i & 1;
+    const int64_t b0 = static_cast<int64_t>(i) * hp.g;
+    const int64_t gb = std::min<int64_t>(hp.g, B - b0);
+    if (i >= 2 && cudaStreamWaitEvent(cs, done[s], 0) != cudaSuccess) return false;
+    uint8_t* dst = w + hp.off_slot[s];
+    const uint8_t* src = static_cast<const uint8_t*>(target_logits) + b0 * R * row_stride * es;
+    cudaError_t e;
+    if (row_stride == V)
+      e = cudaMemcpyAsync(dst, src, static_cast<size_t>(gb * R) * row_bytes, cudaMemcpyHostToDevice, cs);
+    else
+      e = cudaMemcpy2DAsync(dst, row_bytes, src, static_cast<size_t>(row_stride) * es, row_bytes,
+                            static_cast<size_t>(gb * R), cudaMemcpyHostToDevice, cs);
+    return e == cudaSuccess && cudaEventRecord(ready[s], cs) == cudaSuccess;
+  };
+  if (!copy_group(0)) return fail();
+  for (int i = 0; i < ngroups; ++i) {
+    if (i + 1 < ngroups && !copy_group(i + 1)) return fail();
+    const int s = i & 1;
+    const int64_t b0 = static_cast<int64_t>(i) * hp.g;
+    const int32_t gb = static_cast<int32_t>(std::min<int64_t>(hp.g, B - b0));
+    if (cudaStreamWaitEvent(st, ready[s], 0) != cudaSuccess) return fail();
+    const sv_status r = spec_verify_greedy(w + hp.off_slot[s], dtype, V, d_drafts + b0 * K, gb, K, V,
+                                           d_tok + b0 * R, d_num + b0, d_lp + b0 * R, d_mu + b0 * R, d_st + b0,
+                                           w + hp.off_ws, hp.ws_bytes, st);
+    if (r != SV_OK) {
+      fail();
+      return r;
+    }
+    const size_t nrow = static_cast<size_t>(gb) * R * 4, nreq = static_cast<size_t>(gb) * 4;
+    bool ok = cudaMemcpyAsync(out_tokens + b0 * R, d_tok + b0 * R, nrow, cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+              cudaMemcpyAsync(out_num_accepted + b0, d_num + b0, nreq, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    if (ok && out_logprob)
+      ok = cudaMemcpyAsync(out_logprob + b0 * R, d_lp + b0 * R, nrow, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    if (ok && out_mu) ok = cudaMemcpyAsync(out_mu + b0 * R, d_mu + b0 * R, nrow, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    if (ok && out_status)
+      ok = cudaMemcpyAsync(out_status + b0, d_st + b0, nreq, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    if (!ok || cudaEventRecord(done[s], st) != cudaSuccess) return fail();
+  }
+  for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  return SV_OK;
 }
 
 }  // extern "C"

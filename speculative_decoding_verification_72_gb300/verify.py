@@ -81,6 +81,9 @@ _SIGS = {
                                 _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_greedy_static": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                          _P, _P, _P, _P, _P, _P]),
+    "spec_verify_greedy_host_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "spec_verify_greedy_host": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32, _I32,
+                                       _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_verify_greedy_early": (_I32, [_P, _I32, _I64, _P, _I32, _I32, _I32,
                                         _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spec_tree_build_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
@@ -272,6 +275,51 @@ def spec_verify_greedy(target_logits, draft_tokens, workspace=None, out=None,
                                    _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]), fin,
                                    _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
     _check(rc)
+    return out
+
+
+def spec_verify_greedy_host(target_logits, draft_tokens, group=0, device=None, workspace=None, out=None):
+    """Greedy chain verification of host-resident logits (spec_verify_greedy_host
+    in include/spec_verify.h): target_logits [B, K+1, V] (bf16 / fp32) and
+    draft_tokens [B, K] are CPU tensors (pinned for full copy speed); the
+    call streams groups of `group` requests (0: the library's choice) to
+    `device` (default: the current CUDA device) and returns CPU tensors
+    tokens, num_accepted, logprob, mu, status (the caller's `out` dict of
+    contiguous CPU tensors if given), valid once the current stream has
+    completed (the function synchronizes it before returning)."""
+    lib = load_library()
+    if target_logits.dim() != 3 or target_logits.is_cuda:
+        raise SpecVerifyError("target_logits must be a [B, rows, V] CPU tensor")
+    x = target_logits
+    if x.stride(2) != 1 or (x.shape[0] > 1 and x.stride(0) != x.shape[1] * x.stride(1)) or x.stride(1) < x.shape[2]:
+        x = x.contiguous()
+    B, R, V = x.shape
+    K = R - 1
+    stride = x.stride(1) if R > 1 else (x.stride(0) if B > 1 else V)
+    d = draft_tokens
+    if d.is_cuda or d.dtype != torch.int32 or tuple(d.shape) != (B, K) or not d.is_contiguous():
+        raise SpecVerifyError(f"draft_tokens must be a contiguous int32 ({B}, {K}) CPU tensor")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = _outputs(B, R, torch.device("cpu"))
+    else:
+        for k, shp in {"tokens": (B, R), "num_accepted": (B,), "logprob": (B, R), "mu": (B, R),
+                       "status": (B,)}.items():
+            t = out.get(k)
+            if t is None or tuple(t.shape) != shp or not t.is_contiguous() or t.is_cuda:
+                raise SpecVerifyError(f"out[{k!r}] must be a contiguous {shp} CPU tensor")
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        need = lib.spec_verify_greedy_host_workspace_size(B, K, V, _dtype_code(x), int(group))
+        if need == 0 and B > 0:
+            raise SpecVerifyError("invalid sizes")
+        ws = _ws(workspace, need, dev, stream)
+        rc = lib.spec_verify_greedy_host(_ptr(x), _dtype_code(x), stride, _ptr(d), B, K, V, int(group),
+                                         _ptr(out["tokens"]), _ptr(out["num_accepted"]),
+                                         _ptr(out["logprob"]), _ptr(out["mu"]), _ptr(out["status"]),
+                                         _ptr(ws), ws.numel() * ws.element_size(), ctypes.c_void_p(stream))
+        _check(rc)
+        torch.cuda.current_stream(dev).synchronize()
     return out
 
 

@@ -49,7 +49,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.spec_verify_abi_version() == 2
+    assert lib.spec_verify_abi_version() == 3
     for code in range(7):
         s = lib.spec_verify_status_string(code).decode()
         assert s and "unknown" not in s
@@ -155,6 +155,41 @@ def test_greedy_host_validation(lib):
     assert _greedy(lib, ws=FAKE + 8) == SV_ERR_INVALID_ARG         # workspace not 16-byte aligned
     assert _greedy(lib, wsb=16) == SV_ERR_WORKSPACE_TOO_SMALL
     assert _greedy(lib, B=0, x=0, d=0, tok=0, num=0, ws=0) == SV_OK  # nothing to do
+
+
+def _greedy_host(lib, **kw):
+    a = dict(x=FAKE, dtype=1, stride=100, d=FAKE, B=2, K=3, V=100, group=0,
+             tok=FAKE, num=FAKE, lp=FAKE, mu=FAKE, st=FAKE, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify_greedy_host(P(a["x"]), a["dtype"], a["stride"], P(a["d"]), a["B"], a["K"],
+                                       a["V"], a["group"], P(a["tok"]), P(a["num"]), P(a["lp"]), P(a["mu"]),
+                                       P(a["st"]), P(a["ws"]), a["wsb"], P(0))
+
+
+def test_greedy_host_path_sizes_and_validation(lib):
+    one = lib.spec_verify_greedy_host_workspace_size
+    B, K, Vv = 8, 4095, 50257                        # 411.7 MB of bf16 logits per request
+    req = (K + 1) * Vv * 2
+    w_auto = one(B, K, Vv, 1, 0)                     # 256 MB groups: one request each
+    assert w_auto == one(B, K, Vv, 1, 1)
+    assert 2 * req <= w_auto < 2 * req + lib.spec_verify_greedy_workspace_size(1, K, Vv, 1) + (1 << 20)
+    assert one(B, K, Vv, 1, 3) >= 2 * 3 * req        # two staging slots of 3 requests
+    assert one(B, K, Vv, 1, 100) == one(B, K, Vv, 1, B)   # a group never exceeds B
+    small = one(32, 5, 128256, 1, 0)                 # 32 requests fit one 256 MB group
+    assert small >= 2 * 32 * 6 * 128256 * 2 and small % 256 == 0
+    assert one(4, 5, 0, 1, 0) == 0 and one(4, 5, 100, 7, 0) == 0 and one(4, 5, 100, 1, -1) == 0
+    assert one(-1, 5, 100, 1, 0) == 0
+    assert _greedy_host(lib, dtype=3) == SV_ERR_UNSUPPORTED_DTYPE
+    assert _greedy_host(lib, V=0) == SV_ERR_INVALID_ARG
+    assert _greedy_host(lib, stride=99) == SV_ERR_INVALID_ARG
+    assert _greedy_host(lib, group=-2) == SV_ERR_INVALID_ARG
+    assert _greedy_host(lib, x=0) == SV_ERR_INVALID_ARG
+    assert _greedy_host(lib, d=0) == SV_ERR_INVALID_ARG
+    assert _greedy_host(lib, num=0) == SV_ERR_INVALID_ARG
+    assert _greedy_host(lib, ws=FAKE + 16) == SV_ERR_INVALID_ARG   # staging wants 256-byte alignment
+    assert _greedy_host(lib, wsb=4096) == SV_ERR_WORKSPACE_TOO_SMALL
+    assert _greedy_host(lib, B=0, x=0, d=0, tok=0, num=0, ws=0) == SV_OK
 
 
 def _sample(lib, rule=(0, 0.0, 0, 1.0), T=1.0, draft=FAKE, **kw):
