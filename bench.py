@@ -94,9 +94,12 @@ NEXT_CONFIGS = ("llama_greedy_finish", "long_chain_early", "eagle_tree_build", "
 DEFAULT_CONFIG = "long_chain"
 # row pass + decide, plus the draw's two kernels (chunk sums, pick) when a
 # call samples; a stochastic chain of at most 16 rows with draft logits and
-# the exact rule decides inside the chunk-sum kernel (no decide kernel)
+# the exact rule decides inside the chunk-sum kernel (no decide kernel); a
+# stochastic tree call whose rows start on 16-byte boundaries and hold at
+# most 48 chunks of 16 KB merges, walks and draws in one cluster kernel
 KERNELS_PER_CALL = {"greedy": 2, "sample": 4, "tree": 2, "tree_build": 2, "kv_compact": 1}
 FUSED_MAX_ROWS = 16
+TREE_CLUSTER_MAX_CHUNKS = 48
 FALLBACK_HBM_GBS = 6800.0
 MIN_REPS = 5                 # timed repetitions per workload (median reported)
 MAX_REPS = 2000
@@ -251,9 +254,20 @@ def algorithmic_bytes(cfg):
     return rows, logits + small + outs
 
 
+def tree_cluster_path(cfg):
+    """Stochastic tree call on the one-kernel cluster path (the bench's rows
+    are contiguous and 16-byte aligned, so only the chunk count decides)."""
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    row_bytes = cfg["V"] * es
+    return (cfg["kind"] == "tree" and bool(cfg.get("T")) and row_bytes % 16 == 0 and
+            -(-row_bytes // 16384) <= TREE_CLUSTER_MAX_CHUNKS)
+
+
 def launches_per_call(cfg):
     if cfg["kind"] == "sample" and cfg["K"] + 1 <= FUSED_MAX_ROWS:
         return 3
+    if tree_cluster_path(cfg):
+        return 2
     return KERNELS_PER_CALL[cfg["kind"]] + (2 if cfg["kind"] == "tree" and cfg.get("T") else 0)
 
 
@@ -739,6 +753,9 @@ def kernel_desc(cfg):
         d = "one build call: row_topk_kernel (all draft logit bytes) + tree_select_kernel"
     elif cfg["kind"] == "kv_compact":
         d = "one compaction call: kv_compact_kernel (path rows read + written)"
+    elif tree_cluster_path(cfg):
+        d = ("one verify call: row_stats_kernel (all logit bytes) + tree_walk_draw_kernel (row merges, walk "
+             "and draw, one cluster of 8 CTAs per request)")
     elif launches_per_call(cfg) == 3:
         d = "one verify call: row_stats_kernel (all logit bytes) + draw kernels (chunk sums with the decision, pick)"
     else:
