@@ -74,42 +74,60 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int st = 0, slot = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      unsigned long long bytes = 0;
-      // Take a free slot (its previous use released) and describe it.
-      auto claim = [&](int row, int sg, int nst) -> bool {
-        if (st >= kK1Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) return false;
-        meta_row[slot] = row;
-        meta_sg[slot] = sg;
-        meta_nst[slot] = nst;
-        return true;
-      };
-      auto advance = [&]() {
-        ++st;
-        if (++slot == kK1Stages) {
-          slot = 0;
-          phase ^= 1;
-        }
-      };
-      for (int k = g; k < rows && ok; k += a.G) {
+    // The warp checks the CTA's next 32 rows against the state words at once
+    // (one load per lane); lane 0 streams the first row still needed, and
+    // the rows after it get a fresh check. Skipped rows cost a round trip
+    // per 32, not one each.
+    int st = 0, slot = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    unsigned long long bytes = 0;
+    // Take a free slot (its previous use released) and describe it.
+    auto claim = [&](int row, int sg, int nst) -> bool {
+      if (st >= kK1Stages && !mbar_wait_bounded(smem_u32(&empty_bar[slot]), phase ^ 1)) return false;
+      meta_row[slot] = row;
+      meta_sg[slot] = sg;
+      meta_nst[slot] = nst;
+      return true;
+    };
+    auto advance = [&]() {
+      ++st;
+      if (++slot == kK1Stages) {
+        slot = 0;
+        phase ^= 1;
+      }
+    };
+    int k0 = g;
+    while (k0 < rows && ok) {
+      const int64_t kl = static_cast<int64_t>(k0) + static_cast<int64_t>(lane) * a.G;
+      bool need = false;
+      if (kl < rows) {
+        const int i = static_cast<int>(kl) / e.B;
+        const int sb = ld_relaxed(e.state + (static_cast<int>(kl) - i * e.B));
+        need = !(sb != 0 && 0x7fffffff - sb < i);   // no mismatch known before position i
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, need);
+      if (m == 0) {
+        const long long nx = static_cast<long long>(k0) + 32ll * a.G;
+        k0 = nx < rows ? static_cast<int>(nx) : rows;
+        continue;
+      }
+      const int k = k0 + (__ffs(m) - 1) * a.G;
+      k0 = k < rows - a.G ? k + a.G : rows;
+      if (lane == 0) {
         const int i = k / e.B;
         const int b = k - i * e.B;
-        const int sb = ld_relaxed(e.state + b);
-        if (sb != 0 && 0x7fffffff - sb < i) continue;   // a mismatch is known before position i
         const int row = b * e.R + i;
         const Piece p = make_piece<ES>(a, row, 0, static_cast<int64_t>(row + 1) * a.V);
         bytes += static_cast<unsigned long long>(p.cp_hi - p.cp_lo) +
                  static_cast<unsigned long long>((p.head_end - p.j0) + (p.j1 - p.tail_begin)) * ES;
         if (p.nst == 0) {   // scalar elements only: a descriptor with no copy
-          if (!(ok = claim(row, 0, 0))) break;
-          mbar_arrive(smem_u32(&full_bar[slot]));
-          advance();
-          continue;
+          if ((ok = claim(row, 0, 0))) {
+            mbar_arrive(smem_u32(&full_bar[slot]));
+            advance();
+          }
         }
-        for (int s = 0; s < p.nst; ++s) {
+        for (int s = 0; s < p.nst && ok; ++s) {
           if (!(ok = claim(row, s, p.nst))) break;
           const uint32_t off = static_cast<uint32_t>(s) * kK1StageBytes;
           const uint32_t nb = min(static_cast<uint32_t>(kK1StageBytes), static_cast<uint32_t>(p.cp_hi - p.cp_lo) - off);
@@ -119,6 +137,9 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
           advance();
         }
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (lane == 0) {
       if (ok) ok = claim(-1, 0, 0);   // end of stream
       if (ok) {
         mbar_arrive(smem_u32(&full_bar[slot]));
