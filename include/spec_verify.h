@@ -279,9 +279,11 @@ sv_status spec_verify_tree_ex(const void* target_logits, int32_t dtype, int64_t 
  * reads rows position by position across the batch and stops reading a
  * request's rows once a mismatch at an earlier position is known, so a long
  * chain that is rejected early costs a fraction of its logit bytes.
- *   state           [B] int32 device array owned by the caller: zero-filled
- *                   before its first use; every call leaves it zero again.
- *                   Calls that overlap on the GPU need separate state arrays.
+ *   state           [2B] int32 device array owned by the caller (per request
+ *                   the smallest known mismatch, then the rows finished):
+ *                   zero-filled before its first use; every call leaves it
+ *                   zero again. Calls that overlap on the GPU need separate
+ *                   state arrays.
  *   out_bytes_read  [1] uint64 device: logit bytes this call actually read
  *                   (at least the bytes of rows 0..n of every request, at
  *                   most all rows); may be NULL. */

@@ -380,7 +380,10 @@ __global__ void __launch_bounds__(kK2Threads, MIN_BLOCKS) chain_decide_kernel(co
   if (tid == 0) {
     a.out_num[b] = n;
     if (a.out_status) a.out_status[b] = s_status;
-    if (a.early_state) a.early_state[b] = 0;   // ready for the next call
+    if (a.early_state) {   // ready for the next call: mismatch word and finished-row count
+      a.early_state[b] = 0;
+      a.early_state[a.B + b] = 0;
+    }
   }
   if (a.out_bytes && b == 0) {   // bytes the early-exit K1 read, summed in a fixed order
     __shared__ unsigned long long s_bytes[kK2Threads];

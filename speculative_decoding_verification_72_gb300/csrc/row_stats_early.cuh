@@ -8,9 +8,15 @@
 // so the low positions of all requests are read first. The CTA that finishes
 // row i of request b compares its argmax with draft i and, on a mismatch,
 // raises state[b] to 0x7fffffff - i (an atomic max, so the smallest known
-// mismatching position wins). Before streaming row i of request b the
-// producer reads state[b] and skips the row when a mismatch is known at a
-// smaller position. No row at or before a request's first mismatch is ever
+// mismatching position wins); then it counts the row in done[b]. Before
+// streaming row i of request b the producer reads state[b] and skips the row
+// when a mismatch is known at a smaller position. A row of a later wave (the
+// rows k in [w G, (w + 1) G) form wave w) first waits, boundedly, until
+// done[b] covers the request's rows in the earlier waves or a mismatch before
+// it is known: the rows of a wave land at about the same time, so without the
+// wait a CTA would read its next row before the earlier wave's mismatches are
+// published. Every skipped row lies after a known mismatch, so the wait ends;
+// if it hits its limit the row is read. No row at or before a request's first mismatch is ever
 // skipped, so the decide kernel sees exactly the statistics it needs; rows
 // after it may be skipped and their partial slots keep stale values, which
 // the decide kernel never uses. A CTA whose bounded waits gave up marks its
@@ -34,6 +40,7 @@ struct EarlyArgs {
   int32_t B, R;               // requests, rows per request (K + 1)
   const int32_t* drafts;      // [B, K]
   int32_t* state;             // [B]: 0, or 0x7fffffff - (smallest known mismatching position)
+  int32_t* done;              // [B]: rows of the request finished in this call
   unsigned long long* cta_bytes;  // [G]
 };
 
@@ -42,6 +49,16 @@ __device__ __forceinline__ int ld_relaxed(const int32_t* p) {
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Polling limit of the wave gate (a performance wait: when it runs out the
+// row is simply read).
+constexpr uint64_t kWaveGateNs = 200ull * 1000ull;   // 200 us
 
 template <int ES>
 __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e) {
@@ -118,23 +135,46 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
         const int i = k / e.B;
         const int b = k - i * e.B;
         const int row = b * e.R + i;
-        const Piece p = make_piece<ES>(a, row, 0, static_cast<int64_t>(row + 1) * a.V);
-        bytes += static_cast<unsigned long long>(p.cp_hi - p.cp_lo) +
-                 static_cast<unsigned long long>((p.head_end - p.j0) + (p.j1 - p.tail_begin)) * ES;
-        if (p.nst == 0) {   // scalar elements only: a descriptor with no copy
-          if ((ok = claim(row, 0, 0))) {
-            mbar_arrive(smem_u32(&full_bar[slot]));
-            advance();
+        // Wave gate: request b has ceil((wave start - b) / B) rows in the
+        // earlier waves; wait for them to finish, or for a mismatch before i.
+        const long long ws0 = static_cast<long long>(k / a.G) * a.G;
+        const int need_done = ws0 > b ? static_cast<int>((ws0 - b + e.B - 1) / e.B) : 0;
+        bool skip = false;
+        if (need_done > 0) {
+          const uint64_t t0 = global_timer_ns();
+          for (int it = 0; it < (1 << 20); ++it) {
+            const int sb = ld_relaxed(e.state + b);
+            if (sb != 0 && 0x7fffffff - sb < i) {
+              skip = true;
+              break;
+            }
+            if (ld_acquire(e.done + b) >= need_done || global_timer_ns() - t0 > kWaveGateNs) break;
+            __nanosleep(200);
+          }
+          if (!skip) {   // a mismatch published just before the last count
+            const int sb = ld_relaxed(e.state + b);
+            skip = sb != 0 && 0x7fffffff - sb < i;
           }
         }
-        for (int s = 0; s < p.nst && ok; ++s) {
-          if (!(ok = claim(row, s, p.nst))) break;
-          const uint32_t off = static_cast<uint32_t>(s) * kK1StageBytes;
-          const uint32_t nb = min(static_cast<uint32_t>(kK1StageBytes), static_cast<uint32_t>(p.cp_hi - p.cp_lo) - off);
-          const uint32_t fb = smem_u32(&full_bar[slot]);
-          mbar_arrive_expect_tx(fb, nb);
-          bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off), nb, fb);
-          advance();
+        if (!skip) {
+          const Piece p = make_piece<ES>(a, row, 0, static_cast<int64_t>(row + 1) * a.V);
+          bytes += static_cast<unsigned long long>(p.cp_hi - p.cp_lo) +
+                   static_cast<unsigned long long>((p.head_end - p.j0) + (p.j1 - p.tail_begin)) * ES;
+          if (p.nst == 0) {   // scalar elements only: a descriptor with no copy
+            if ((ok = claim(row, 0, 0))) {
+              mbar_arrive(smem_u32(&full_bar[slot]));
+              advance();
+            }
+          }
+          for (int s = 0; s < p.nst && ok; ++s) {
+            if (!(ok = claim(row, s, p.nst))) break;
+            const uint32_t off = static_cast<uint32_t>(s) * kK1StageBytes;
+            const uint32_t nb = min(static_cast<uint32_t>(kK1StageBytes), static_cast<uint32_t>(p.cp_hi - p.cp_lo) - off);
+            const uint32_t fb = smem_u32(&full_bar[slot]);
+            mbar_arrive_expect_tx(fb, nb);
+            bulk_g2s(smem_u32(ring + slot * kK1StageBytes), reinterpret_cast<const void*>(p.cp_lo + off), nb, fb);
+            advance();
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -268,6 +308,8 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
           const int d = e.drafts[static_cast<int64_t>(b) * K + i];
           if (d < 0 || d >= a.V || d != ri) atomicMax(e.state + b, 0x7fffffff - i);
         }
+        __threadfence();   // the partial and the mismatch before the count
+        atomicAdd(e.done + b, 1);
       }
     }
   }

@@ -864,6 +864,7 @@ sv_status spec_verify_greedy_early(const void* target_logits, int32_t dtype, int
   e.R = K + 1;
   e.drafts = draft_tokens;
   e.state = state;
+  e.done = state + B;
   // one partial per row at slot `row`; the spare kK1MaxCtas slots after them hold the CTAs' byte counts
   e.cta_bytes = reinterpret_cast<unsigned long long*>(e.rs.partials + rows);
   cudaError_t err = es == 2 ? launch_row_stats_early<2>(e, st) : launch_row_stats_early<4>(e, st);

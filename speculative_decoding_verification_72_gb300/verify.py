@@ -395,7 +395,7 @@ _EARLY_STATE = {}
 def spec_verify_greedy_early(target_logits, draft_tokens, state=None, workspace=None, out=None):
     """Early-exit greedy chain verification (include/spec_verify.h): the same
     outputs as spec_verify_greedy, plus out["bytes_read"] (int64 [1], logit
-    bytes the call read). `state` is the caller's zero-filled int32 [B]
+    bytes the call read). `state` is the caller's zero-filled int32 [2B]
     request state (left zero after each call); by default one cached per
     device, stream and B is used."""
     lib = load_library()
@@ -412,9 +412,10 @@ def spec_verify_greedy_early(target_logits, draft_tokens, state=None, workspace=
         key = (dev.index, stream, B)
         state = _EARLY_STATE.get(key)
         if state is None:
-            state = _EARLY_STATE[key] = torch.zeros((B,), dtype=torch.int32, device=dev)
-    elif state.dtype != torch.int32 or tuple(state.shape) != (B,) or not state.is_contiguous() or state.device != dev:
-        raise SpecVerifyError(f"state must be a contiguous int32 ({B},) tensor on {dev}")
+            state = _EARLY_STATE[key] = torch.zeros((2 * B,), dtype=torch.int32, device=dev)
+    elif (state.dtype != torch.int32 or tuple(state.shape) != (2 * B,) or not state.is_contiguous() or
+          state.device != dev):
+        raise SpecVerifyError(f"state must be a contiguous int32 ({2 * B},) tensor on {dev}")
     need = lib.spec_verify_greedy_workspace_size(B, K, V, _dtype_code(x))
     if need == 0 and B > 0:
         raise SpecVerifyError("invalid sizes")

@@ -44,7 +44,7 @@ def _bytes_ok(got, ci, es):
 def test_long_chain_reads_a_fraction_and_matches():
     B, K, Vv = 8, 4095, 50257
     ci = W.greedy_chain(B=B, K=K, V=Vv, dtype=torch.bfloat16, p_match=0.95, seed=7600, device=DEV)
-    state = torch.zeros(B, dtype=torch.int32, device=DEV)
+    state = torch.zeros(2 * B, dtype=torch.int32, device=DEV)
     plain = sv.spec_verify_greedy(ci.target, ci.draft_tokens)
     for _ in range(2):                                   # the state is reused
         got = sv.spec_verify_greedy_early(ci.target, ci.draft_tokens, state=state)
