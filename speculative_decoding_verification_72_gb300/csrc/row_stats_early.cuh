@@ -114,6 +114,18 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
         phase ^= 1;
       }
     };
+    // The CTA's rows k = g + j G belong to requests (g + j G) mod B, which
+    // repeat with period B / gcd(B, G); positions only grow along the
+    // sequence and a request's known mismatch position only falls, so once
+    // a checked batch covering a whole period is all skipped, every later
+    // row is too.
+    int gcd_bg = e.B, rem = a.G % e.B;
+    while (rem != 0) {
+      const int t = gcd_bg % rem;
+      gcd_bg = rem;
+      rem = t;
+    }
+    const bool batch_spans_period = e.B / gcd_bg <= 32;
     int k0 = g;
     while (k0 < rows && ok) {
       const int64_t kl = static_cast<int64_t>(k0) + static_cast<int64_t>(lane) * a.G;
@@ -125,6 +137,7 @@ __global__ void __maxnreg__(kK1MaxRegs) row_stats_early_kernel(const EarlyArgs e
       }
       const unsigned m = __ballot_sync(0xffffffffu, need);
       if (m == 0) {
+        if (batch_spans_period && static_cast<long long>(k0) + 31ll * a.G < rows) break;
         const long long nx = static_cast<long long>(k0) + 32ll * a.G;
         k0 = nx < rows ? static_cast<int>(nx) : rows;
         continue;
