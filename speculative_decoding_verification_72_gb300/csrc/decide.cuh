@@ -385,15 +385,18 @@ __global__ void __launch_bounds__(kK2Threads, MIN_BLOCKS) chain_decide_kernel(co
       a.early_state[a.B + b] = 0;
     }
   }
-  if (a.out_bytes && b == 0) {   // bytes the early-exit K1 read, summed in a fixed order
-    __shared__ unsigned long long s_bytes[kK2Threads];
+  if (a.out_bytes && b == 0) {   // bytes the early-exit K1 read: per-thread, warp, then block sums
+    __shared__ unsigned long long s_bytes[kK2Threads / 32];
     unsigned long long t = 0;
     for (int g2 = tid; g2 < a.n_cta; g2 += kK2Threads) t += a.cta_bytes[g2] & ~kEarlyAbortBit;
-    s_bytes[tid] = t;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if ((tid & 31) == 0) s_bytes[tid >> 5] = t;
     __syncthreads();
     if (tid == 0) {
       unsigned long long tot = 0;
-      for (int k = 0; k < kK2Threads; ++k) tot += s_bytes[k];
+#pragma unroll
+      for (int k = 0; k < kK2Threads / 32; ++k) tot += s_bytes[k];
       a.out_bytes[0] = tot;
     }
   }
