@@ -257,10 +257,10 @@ def algorithmic_bytes(cfg):
 def tree_cluster_path(cfg):
     """Stochastic tree call on the one-kernel cluster path (the bench's rows
     are contiguous and 16-byte aligned, so only the chunk count decides)."""
-    es = 2 if cfg["dtype"] == "bf16" else 4
-    row_bytes = cfg["V"] * es
-    return (cfg["kind"] == "tree" and bool(cfg.get("T")) and row_bytes % 16 == 0 and
-            -(-row_bytes // 16384) <= TREE_CLUSTER_MAX_CHUNKS)
+    if cfg["kind"] != "tree" or not cfg.get("T"):
+        return False
+    row_bytes = cfg["V"] * (2 if cfg["dtype"] == "bf16" else 4)
+    return row_bytes % 16 == 0 and -(-row_bytes // 16384) <= TREE_CLUSTER_MAX_CHUNKS
 
 
 def launches_per_call(cfg):

@@ -72,3 +72,19 @@ def test_whole_job_rate_is_from_the_slowest_rank():
 
 def test_single_rank_reduction_is_identity():
     assert bench.reduce_over_ranks(4.5, "max", "cpu", 1) == 4.5
+
+
+def test_bench_describes_every_workload():
+    """Host-side helpers of bench.py hold for every workload it can time (no
+    GPU): launch counts, kernel description, algorithmic bytes, config."""
+    import bench
+    for name, cfg in bench.CONFIGS.items():
+        n = bench.launches_per_call(cfg)
+        assert 1 <= n <= 4, name
+        assert bench.kernel_desc(cfg), name
+        rows, alg = bench.algorithmic_bytes(cfg)
+        assert rows > 0 and alg > 0, name
+        assert bench.config_dict(cfg, name, 1)["name"] == name
+    # stochastic tree workloads run on the cluster path: row pass + one kernel
+    assert bench.launches_per_call(bench.CONFIGS["eagle_tree_power"]) == 2
+    assert bench.launches_per_call(bench.CONFIGS["eagle_tree_greedy"]) == 2
