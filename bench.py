@@ -568,12 +568,21 @@ class OraclePool:
             p.join(timeout=10)
 
 
-def cpu_baseline(cfg, budget_s):
-    """The oracle on a bounded host sample: one thread, then every host core."""
+def cpu_baseline_prepare(cfg):
+    """The host sample and the forked oracle pool, made before any CUDA call;
+    the workers wait idle until cpu_baseline_run drives them."""
     small, xh = cpu_sample(cfg)
     nreq = small["B"]
+    return {"xh": xh, "nreq": nreq, "pool": OraclePool(cfg, xh, nreq)}
+
+
+def cpu_baseline_run(cfg, prep, budget_s):
+    """The oracle on the prepared host sample: one thread, then every host
+    core. Run after the GPU timings: oracle work before them was measured to
+    slow the later host-to-device copies of the e2e leg (long chain: 15.9 ms
+    per step with no oracle work before, 18.0-18.4 ms after either leg)."""
+    xh, nreq, pool = prep["xh"], prep["nreq"], prep["pool"]
     one, done1 = oracle_one_core(cfg, xh, nreq, budget_s)
-    pool = OraclePool(cfg, xh, nreq)
     rows, wall, k = 0, 0.0, 0
     try:
         while wall < budget_s or k == 0:
@@ -890,11 +899,12 @@ def run_gpu(args, cfg, name):
     steps = args.steps if args.steps is not None else 200
     warmup = max(3, args.warmup if args.warmup is not None else 20)
 
-    # The CPU oracle legs run first: the all-core leg forks, which must happen
-    # before this process makes any CUDA call.
-    cpu = None
+    # The CPU oracle legs' sample and forked pool are made first (the fork
+    # must happen before this process makes any CUDA call); the legs run after
+    # the GPU timings.
+    cpu_prep = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(cfg, args.cpu_budget)
+        cpu_prep = cpu_baseline_prepare(cfg)
 
     import torch
     import torch.distributed as dist
@@ -942,6 +952,7 @@ def run_gpu(args, cfg, name):
             torch.cuda.empty_cache()
     time.sleep(0.3)
     sampler.stop()
+    cpu = cpu_baseline_run(cfg, cpu_prep, args.cpu_budget) if cpu_prep is not None else None
 
     line = {
         "metric": metric_name(cfg), "value": value, "unit": "rows/s", "n_gpus": world,
