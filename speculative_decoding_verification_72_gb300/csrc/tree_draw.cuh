@@ -107,7 +107,7 @@ __device__ __forceinline__ void cluster_sync() {
 // Dynamic shared-memory layout for N nodes and nch chunks per CTA (the host
 // sizes the launch with the same function).
 struct TwLayout {
-  uint32_t m, l2, g, u, lp, p, racc, xp, am, tok, par, first, next, dup, bad, excl, slots, vsum, chunks, total;
+  uint32_t l2, g, u, lp, p, racc, xp, tok, par, first, next, dup, bad, excl, slots, vsum, chunks, total;
 };
 
 __host__ __device__ constexpr uint32_t tw_align(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -116,7 +116,6 @@ __host__ __device__ inline TwLayout tw_layout(int N, int nch) {
   TwLayout L{};
   const uint32_t n4 = tw_align(static_cast<uint32_t>(N), 4) * 4u;   // one 32-bit word per node
   uint32_t o = 0;
-  L.m = o;     o += n4;
   L.l2 = o;    o += n4;
   L.g = o;     o += n4;
   L.u = o;     o += n4;
@@ -124,7 +123,6 @@ __host__ __device__ inline TwLayout tw_layout(int N, int nch) {
   L.p = o;     o += n4;
   L.racc = o;  o += n4;
   L.xp = o;    o += n4;
-  L.am = o;    o += n4;
   L.tok = o;   o += n4;
   L.par = o;   o += n4;
   L.first = o; o += n4;
@@ -166,7 +164,6 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
   const int N = a.N, W = a.max_depth + 1;
   const float c = a.c;
   const TwLayout L = tw_layout(N, w.nch);
-  float* sm_m = reinterpret_cast<float*>(smem + L.m);       // row max
   float* sm_l2 = reinterpret_cast<float*>(smem + L.l2);     // row lse, log2 domain
   float* sm_g = reinterpret_cast<float*>(smem + L.g);       // node token's logit in its parent's row
   float* sm_u = reinterpret_cast<float*>(smem + L.u);       // node's uniform
@@ -174,7 +171,6 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
   float* sm_p = reinterpret_cast<float*>(smem + L.p);       // 2^lp
   float* sm_racc = reinterpret_cast<float*>(smem + L.racc); // relaxed rule: the node's acceptance (0 / 1)
   float* sm_xp = reinterpret_cast<float*>(smem + L.xp);     // p of each rejected token (draw masking)
-  int* sm_am = reinterpret_cast<int*>(smem + L.am);         // row argmax
   int* sm_tok = reinterpret_cast<int*>(smem + L.tok);
   int* sm_par = reinterpret_cast<int*>(smem + L.par);       // -1 for the root and bad links
   int* sm_first = reinterpret_cast<int*>(smem + L.first);   // first child
@@ -260,9 +256,7 @@ __global__ void __cluster_dims__(kTwCluster, 1, 1) __launch_bounds__(kTwThreads,
       int idx, err;
       if (staged) merge_row_staged(s_slots, sr, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
       else merge_row_serial(a.part, rb + n, a.V, a.T, a.G, c, m, s, idx, err);
-      sm_m[n] = m;
       sm_l2[n] = m * c + log2f(s);
-      sm_am[n] = idx;
       sm_bad[n] = ((!(fabsf(m) <= FLT_MAX) || !(s > 0.f && s <= FLT_MAX)) ? SV_STATUS_NONFINITE_ROW : 0) |
                   (err ? SV_STATUS_TIMEOUT : 0);
     }
