@@ -156,7 +156,9 @@ __device__ __forceinline__ float row_thr(const ChainArgs& a, int b, int i) {
   return a.rule.thr ? a.rule.thr[static_cast<int64_t>(b) * a.K + i] : INFINITY;
 }
 
-template <int ES, int MIN_BLOCKS>
+// WIDE: the rows span many row-pass CTAs (small batches), so the half-warp
+// merge loads four partials per lane per round trip instead of two.
+template <int ES, int MIN_BLOCKS, bool WIDE = false>
 __global__ void __launch_bounds__(kK2Threads, MIN_BLOCKS) chain_decide_kernel(const ChainArgs a) {
   __shared__ int s_first;
   __shared__ int s_status;
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kK2Threads, MIN_BLOCKS) chain_decide_kernel(co
                                     : static_cast<int64_t>(b) * R + h;
       float hm, hs;
       int hi, he;
-      merge_row_half(a.part, row, valid, a.V, a.T, a.G, c, tid & 15, hm, hs, hi, he);
+      merge_row_half<WIDE ? 4 : 2>(a.part, row, valid, a.V, a.T, a.G, c, tid & 15, hm, hs, hi, he);
       if (valid && (tid & 15) == 0) {
         Partial o;
         o.m = hm;

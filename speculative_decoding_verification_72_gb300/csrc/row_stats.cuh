@@ -685,7 +685,11 @@ __device__ __forceinline__ void merge_row_staged(const Partial* staged, const Sl
 // merge the lanes, so every lane of the half ends with the row's statistics.
 // All 32 lanes of the warp must call it (valid = false: a half with no row,
 // which contributes nothing); merge_stats is symmetric, so both partners of a
-// shuffle compute the same value and the result is deterministic.
+// shuffle compute the same value and the result is deterministic. LOADS
+// partials per lane are loaded before any of them is merged (one L2 round
+// trip for rows of up to 16 LOADS partials); a lane merges its partials in
+// increasing k whatever LOADS is, so the result does not depend on it.
+template <int LOADS = 2>
 __device__ __forceinline__ void merge_row_half(const Partial* __restrict__ parts, int64_t row, bool valid, int V,
                                                int64_t T, int G, float c, int lane16, float& m, float& s, int& idx,
                                                int& err) {
@@ -698,17 +702,31 @@ __device__ __forceinline__ void merge_row_half(const Partial* __restrict__ parts
     const int g_lo = cta_of(e0, T, G), g_hi = cta_of(e0 + V - 1, T, G);
     const int n = (g_hi - g_lo + 1) * kK1Consumers;
     const Partial* p = parts + (row + g_lo) * kK1Consumers;
-    // two of the lane's partials per iteration, both loaded before either is
-    // merged (the same merge order, one L2 round trip for rows of <= 32)
-    for (int k = lane16; k < n; k += 32) {
-      const Partial v0 = p[k];
-      Partial v1;
-      if (k + 16 < n) v1 = p[k + 16];
-      merge_stats(m, s, idx, v0.m, v0.s, v0.idx, c);
-      err |= v0.err;
-      if (k + 16 < n) {
-        merge_stats(m, s, idx, v1.m, v1.s, v1.idx, c);
-        err |= v1.err;
+    if constexpr (LOADS == 2) {
+      for (int k = lane16; k < n; k += 32) {
+        const Partial v0 = p[k];
+        Partial v1;
+        if (k + 16 < n) v1 = p[k + 16];
+        merge_stats(m, s, idx, v0.m, v0.s, v0.idx, c);
+        err |= v0.err;
+        if (k + 16 < n) {
+          merge_stats(m, s, idx, v1.m, v1.s, v1.idx, c);
+          err |= v1.err;
+        }
+      }
+    } else {
+      for (int k0 = lane16; k0 < n; k0 += 16 * LOADS) {
+        Partial v[LOADS];
+#pragma unroll
+        for (int u = 0; u < LOADS; ++u)
+          if (k0 + 16 * u < n) v[u] = p[k0 + 16 * u];
+#pragma unroll
+        for (int u = 0; u < LOADS; ++u) {
+          if (k0 + 16 * u < n) {
+            merge_stats(m, s, idx, v[u].m, v[u].s, v[u].idx, c);
+            err |= v[u].err;
+          }
+        }
       }
     }
   }

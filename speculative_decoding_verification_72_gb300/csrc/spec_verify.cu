@@ -479,8 +479,15 @@ sv_status spec_verify_greedy_ex(const void* target_logits, int32_t dtype, int64_
   a.out_logprob = out_logprob;
   a.out_mu = out_mu;
   a.out_status = out_status;
-  e = es == 2 ? launch(chain_decide_kernel<2, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a)
-              : launch(chain_decide_kernel<4, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a);
+  // Rows that span more than ~3.5 row-pass CTAs (small batches) have more
+  // partials than one round trip of two loads per lane covers.
+  const bool wide = static_cast<double>(V) * r.G > 3.5 * static_cast<double>(r.T);
+  if (wide)
+    e = es == 2 ? launch(chain_decide_kernel<2, kK2MinBlocksGreedy, true>, B, kK2Threads, 0, st, true, a)
+                : launch(chain_decide_kernel<4, kK2MinBlocksGreedy, true>, B, kK2Threads, 0, st, true, a);
+  else
+    e = es == 2 ? launch(chain_decide_kernel<2, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a)
+                : launch(chain_decide_kernel<4, kK2MinBlocksGreedy>, B, kK2Threads, 0, st, true, a);
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
