@@ -416,8 +416,13 @@ sv_status spec_verify_greedy_static(const void* target_logits, int32_t dtype, in
  * The call returns once the work is enqueued; the host outputs are valid
  * after `stream` completes (cudaStreamSynchronize). Calls on one device
  * share the library's copy stream, and each call orders its copies after
- * the work already enqueued on `stream`. Errors as for spec_verify_greedy;
- * SV_ERR_CUDA also when the copy stream or an event cannot be created. */
+ * the work already enqueued on `stream`. The copy stream is created by the
+ * first call on each device (with that device current) and kept for the life
+ * of the process; after cudaDeviceReset (or anything else that destroys the
+ * device's primary context) it is stale, and this entry point must not be
+ * called again on that device in the same process. Errors as for
+ * spec_verify_greedy; SV_ERR_CUDA also when the copy stream or an event
+ * cannot be created. */
 #define SV_HOST_GROUP_BYTES (256ull << 20)
 size_t spec_verify_greedy_host_workspace_size(int32_t B, int32_t K, int32_t V, int32_t dtype,
                                               int32_t group);
