@@ -62,14 +62,17 @@ __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(const KvCompactA
   const int b = blockIdx.x / a.chunks;
   const int ch = blockIdx.x - b * a.chunks;
   const int tid = threadIdx.x;
+  const int32_t* nodes = a.path_nodes + static_cast<int64_t>(b) * a.path_cols;
+  // The count and the thread's first path entry are loaded together (the
+  // entry is inside the row whatever the count is).
+  const int v_first = tid < a.path_cols ? nodes[tid] : 0;
   const int n = a.num_accepted[b];
   const int64_t base = a.seq_base[b];
-  const int32_t* nodes = a.path_nodes + static_cast<int64_t>(b) * a.path_cols;
   // validate the whole path (every CTA of the request reaches the same answer)
   bool ok = n >= 0 && n < a.path_cols;
   if (ok) {
     for (int j = tid; j <= n; j += kKvThreads) {
-      const int v = nodes[j];
+      const int v = j == tid ? v_first : nodes[j];
       ok = ok && v >= 0 && v < a.max_nodes && kv_offset(a, b, base + v) >= 0 && kv_offset(a, b, base + j) >= 0;
     }
   }
