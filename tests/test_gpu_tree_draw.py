@@ -11,8 +11,9 @@ float64 oracle.
 Cases: a row end inside a 16-byte vector (the copy's extra elements masked),
 a copy cut back at the buffer's end (elements read from global memory), one
 chunk per row (most CTAs of the cluster hold none), the most chunks a
-cluster holds (six per CTA) and one past it, and rejected tokens spread
-over many chunks and CTAs.
+cluster holds (six per CTA) and one past it, rejected tokens spread over
+many chunks and CTAs, a root alone, a depth cap of 0, and more nodes than the
+staged merge holds.
 """
 
 import numpy as np
@@ -122,3 +123,27 @@ def test_many_requests_and_repeat_calls_are_identical():
     ref = O.verify_tree(f64(ti.target), host(ti.node_tokens), host(ti.parents), ti.max_depth, 1.0,
                         f64(ti.uniforms), rule=O.RULE_POWER, alpha=0.3)
     compare(a, ref, stochastic=True, max_exempt=12)
+
+
+@pytest.mark.parametrize("N,max_depth", [(1, 3), (2, 0), (5, 1), (700, 40)])
+def test_tree_sizes_on_the_cluster_path(N, max_depth):
+    """Random trees on the cluster path: a root alone (bonus draw from row 0),
+    a depth cap of 0 (the root's children are never tested), and more nodes
+    than the staged merge holds (700 rows: per-row serial merges)."""
+    B, V = 3, 4096
+    rng = np.random.default_rng(8500 + N)
+    par = np.zeros((B, N), dtype=np.int32)
+    par[:, 0] = -1
+    for n in range(1, N):
+        par[:, n] = rng.integers(0, n, size=B)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    tok[:, 0] = 0
+    g = torch.Generator(device="cpu").manual_seed(8500 + N)
+    x = (torch.randn((B, N, V), generator=g) * 3).to(torch.bfloat16).to(DEV)
+    u = rng.random((B, N)).astype(np.float32)
+    got = sv.spec_verify_tree(x, torch.from_numpy(tok).to(DEV), torch.from_numpy(par).to(DEV), max_depth,
+                              temperature=1.0, uniforms=torch.from_numpy(u).to(DEV), rule=sv.RULE_POWER, alpha=0.3)
+    ref = O.verify_tree(f64(x), tok, par, max_depth, 1.0, u.astype(np.float64), rule=O.RULE_POWER, alpha=0.3)
+    compare(got, ref, stochastic=True)
+    if max_depth == 0 and N > 1:
+        assert (host(got["status"]) & sv.STATUS_DEPTH_EXCEEDED).all()
